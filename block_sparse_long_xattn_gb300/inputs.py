@@ -1,0 +1,132 @@
+"""Seeded synthetic workloads (Q, K, V) shaped like the pages' Llama-3.1-8B layer.
+
+This module only draws random numbers and plants a direction in them; it holds
+none of the method's arithmetic.  Both the CUDA path (through tests and the
+benchmark) and the fp64 oracle read the arrays it returns, so both sides see
+bit-identical inputs.
+
+Recipe (per seed):
+  * Q, K, V are iid N(0, 1) float32 draws from numpy's Philox generator keyed
+    by the seed, then rounded once to the working dtype (bf16: round to
+    nearest even); the float32 arrays returned hold those rounded values
+    exactly.
+  * For every kv-head h a unit vector u_h (a normalised N(0, I_d) draw) is
+    planted: alpha * u_h is added to every key of 128-token block 0 and of
+    ``n_hot`` distinct blocks drawn uniformly from [1, Lk/128), and to every
+    query of the q-heads that share kv-head h.  V is left unplanted.
+  * The planted values are rounded to the dtype after the addition.
+
+This gives the sink + needle + local-diagonal structure the long-context
+configurations describe (nano-vllm pages: RULER/needle workloads on
+Llama-3.1-8B, 32 q-heads, 8 kv-heads, head_dim 128).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+BLOCK = 128
+
+
+def round_to_bf16(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to the nearest bf16 (ties to even); return float32."""
+    x = np.ascontiguousarray(x, np.float32)
+    bits = x.view(np.uint32).astype(np.uint64)
+    lsb = (bits >> 16) & 1
+    rounded = ((bits + 0x7FFF + lsb) >> 16) << 16
+    out = (rounded & 0xFFFFFFFF).astype(np.uint32).view(np.float32)
+    # NaN/Inf never occur in these draws; keep them out explicitly
+    assert np.isfinite(out).all()
+    return out
+
+
+def bf16_bits(x: np.ndarray) -> np.ndarray:
+    """The upper 16 bits of bf16-exact float32 values, as uint16."""
+    x = np.ascontiguousarray(x, np.float32)
+    return (x.view(np.uint32) >> 16).astype(np.uint16)
+
+
+@dataclass
+class Workload:
+    q: np.ndarray        # [B, Lq, Hq, d] float32 (dtype-exact values)
+    k: np.ndarray        # [B, Lk, Hkv, d]
+    v: np.ndarray        # [B, Lk, Hkv, d]
+    q_start_pos: int
+    dtype: str           # "bf16" or "f32"
+    hot_blocks: np.ndarray  # [B, Hkv, n_hot] planted key blocks (besides block 0)
+
+
+def make_workload(seed: int, B: int, Hq: int, Hkv: int, d: int, Lk: int,
+                  q_start_pos: int, alpha: float = 3.0, n_hot: int = 0,
+                  dtype: str = "bf16", q_full: bool = False) -> Workload:
+    """Draw one workload.
+
+    Keys/values span positions [0, Lk).  Queries span [q_start_pos, Lk) unless
+    ``q_full`` is set, in which case they span [0, Lk) (a whole sequence to
+    be processed in chunks); q_start_pos is then recorded as 0.
+    """
+    assert dtype in ("bf16", "f32")
+    assert Lk % BLOCK == 0 and q_start_pos % BLOCK == 0 and Hq % Hkv == 0
+    rng = np.random.Generator(np.random.Philox(key=seed))
+    q0 = 0 if q_full else q_start_pos
+    Lq = Lk - q0
+    q = rng.standard_normal((B, Lq, Hq, d), dtype=np.float32)
+    k = rng.standard_normal((B, Lk, Hkv, d), dtype=np.float32)
+    v = rng.standard_normal((B, Lk, Hkv, d), dtype=np.float32)
+    nkb = Lk // BLOCK
+    n_hot = min(n_hot, nkb - 1)
+    hot = np.zeros((B, Hkv, n_hot), np.int64)
+    G = Hq // Hkv
+    if alpha != 0.0:
+        for b in range(B):
+            for h in range(Hkv):
+                u = rng.standard_normal(d).astype(np.float64)
+                u /= np.linalg.norm(u)
+                du = (alpha * u).astype(np.float32)
+                if n_hot > 0:
+                    hot[b, h] = 1 + rng.choice(nkb - 1, size=n_hot, replace=False)
+                for blk in [0] + sorted(hot[b, h].tolist()):
+                    k[b, blk * BLOCK:(blk + 1) * BLOCK, h, :] += du
+                q[b, :, h * G:(h + 1) * G, :] += du
+    if dtype == "bf16":
+        q, k, v = round_to_bf16(q), round_to_bf16(k), round_to_bf16(v)
+    return Workload(q, k, v, 0 if q_full else q_start_pos, dtype, hot)
+
+
+def random_block_mask(seed: int, B: int, Hq: int, nqb: int, nkb: int,
+                      q_start_pos: int, density: float) -> np.ndarray:
+    """A seeded random causal block mask with the sink and diagonal set.
+
+    Used to drive the block-sparse attention with masks that are independent
+    of any estimator.  Entries above the diagonal are left 0.
+    """
+    rng = np.random.Generator(np.random.Philox(key=seed + 0x5EED))
+    m = (rng.random((B, Hq, nqb, nkb)) < density).astype(np.uint8)
+    cur = q_start_pos // BLOCK
+    for qb in range(nqb):
+        m[:, :, qb, cur + qb + 1:] = 0
+        m[:, :, qb, cur + qb] = 1
+        m[:, :, qb, 0] = 1
+    return m
+
+
+# The workloads the benchmark and the parity tests use, by name.
+CONFIGS = {
+    # tiny single chunk: 2 q-heads, 1 kv-head, d 64, 1024 tokens, fp32
+    "tiny-1k-f32": dict(B=1, Hq=2, Hkv=1, d=64, Lk=1024, q_start_pos=0,
+                        alpha=3.0, n_hot=0, dtype="f32", stride=8, threshold=0.9),
+    # one 4096-token chunk at 28672 of a 32K context, Llama-3.1-8B heads
+    "llama8b-32k-chunk4096": dict(B=1, Hq=32, Hkv=8, d=128, Lk=32768,
+                                  q_start_pos=28672, alpha=3.0, n_hot=16,
+                                  dtype="bf16", stride=8, threshold=0.95),
+    # the last 4096-token chunk of a 128K context, stride 16
+    "llama8b-128k-chunk4096": dict(B=1, Hq=32, Hkv=8, d=128, Lk=131072,
+                                   q_start_pos=126976, alpha=3.0, n_hot=64,
+                                   dtype="bf16", stride=16, threshold=0.9),
+    # a whole 64K sequence processed as 16 chunks of 4096
+    "llama8b-64k-chunked": dict(B=1, Hq=32, Hkv=8, d=128, Lk=65536,
+                                q_start_pos=0, alpha=3.0, n_hot=32,
+                                dtype="bf16", stride=8, threshold=0.95,
+                                chunk=4096),
+}

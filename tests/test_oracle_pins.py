@@ -1,0 +1,339 @@
+"""Pins for the fp64 oracle: each check ties it to something other than itself.
+
+These tests run on the CPU.  They check the oracle against the pages' worked
+examples (``tests/golden/``), closed forms, invariants, brute force on tiny
+inputs and independent library routines (torch's fp64 attention), so that a
+dropped term, a wrong sign, scale or index, or a transposed operand in the
+oracle fails at least one of them.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import xattn_oracle as O
+from block_sparse_long_xattn_gb300.inputs import make_workload, random_block_mask
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# ----------------------------------------------------------------------------
+# a1: stride reshape and antidiagonal scores
+# ----------------------------------------------------------------------------
+def test_reshape_positions_match_guide_example():
+    g = _golden("stride_reshape_positions.json")
+    S = g["stride"]
+    pos = np.arange(4 * S, dtype=np.float64)[:, None]       # value = token position, d = 1
+    kr = O.stride_reshape_k(pos, S)
+    qr = O.stride_reshape_q(pos, S)
+    for row, expect in enumerate(g["k_r_row_positions"]):
+        assert kr[row].tolist() == expect
+    for row, expect in enumerate(g["q_r_row_positions"]):
+        assert qr[row].tolist() == expect
+
+
+@pytest.mark.parametrize("S,d,Lq,Lk", [(4, 3, 32, 48), (8, 2, 64, 64), (2, 5, 16, 40)])
+def test_scores_equal_token_pair_loop(S, d, Lq, Lk):
+    """s[i, j] = sum_t Q[i*S+S-1-t] . K[j*S+t] by an explicit loop over token pairs."""
+    rng = np.random.default_rng(S * 100 + d)
+    q = rng.standard_normal((Lq, d))
+    k = rng.standard_normal((Lk, d))
+    s = O.antidiagonal_scores(q, k, S)
+    assert s.shape == (Lq // S, Lk // S)
+    for i in range(Lq // S):
+        for j in range(Lk // S):
+            acc = 0.0
+            for t in range(S):
+                acc += float(np.dot(q[i * S + S - 1 - t], k[j * S + t]))
+            assert abs(s[i, j] - acc) <= 1e-12 * max(1.0, abs(acc))
+
+
+def test_scores_stride1_is_plain_qkt():
+    rng = np.random.default_rng(7)
+    q = rng.standard_normal((12, 6))
+    k = rng.standard_normal((20, 6))
+    ref = torch.from_numpy(q) @ torch.from_numpy(k).T
+    np.testing.assert_allclose(O.antidiagonal_scores(q, k, 1), ref.numpy(), rtol=1e-13, atol=1e-13)
+
+
+# ----------------------------------------------------------------------------
+# a2 + a3: softmax and block sums
+# ----------------------------------------------------------------------------
+def _block_sums_via_torch(q, k, P, S):
+    """Independent route: reshaped tensors built by token-pair indexing, softmax
+    and scale through torch's fp64 scaled_dot_product_attention (V = identity
+    extracts the probability matrix), block sums by explicit loops."""
+    B, Lq, Hq, d = q.shape
+    _, Lk, Hkv, _ = k.shape
+    G = Hq // Hkv
+    R, C, r = Lq // S, Lk // S, 128 // S
+    out = np.zeros((B, Hq, Lq // 128, Lk // 128))
+    for b in range(B):
+        for h in range(Hq):
+            qr = np.zeros((R, S * d))
+            kr = np.zeros((C, S * d))
+            for t in range(S):
+                qr[:, t * d:(t + 1) * d] = q[b, [i * S + S - 1 - t for i in range(R)], h, :]
+                kr[:, t * d:(t + 1) * d] = k[b, [j * S + t for j in range(C)], h // G, :]
+            allowed = torch.tensor([[J <= P // S + i for J in range(C)] for i in range(R)])
+            probs = torch.nn.functional.scaled_dot_product_attention(
+                torch.from_numpy(qr)[None, None], torch.from_numpy(kr)[None, None],
+                torch.eye(C, dtype=torch.float64)[None, None],
+                attn_mask=allowed[None, None], scale=1.0 / (math.sqrt(d) * S))[0, 0].numpy()
+            for qb in range(Lq // 128):
+                for kb in range(Lk // 128):
+                    out[b, h, qb, kb] = probs[qb * r:(qb + 1) * r, kb * r:(kb + 1) * r].sum()
+    return out
+
+
+@pytest.mark.parametrize("S,P", [(8, 0), (8, 256), (4, 128), (16, 384)])
+def test_block_sums_match_torch_attention(S, P):
+    w = make_workload(seed=11 + S, B=1, Hq=2, Hkv=1, d=16, Lk=P + 256, q_start_pos=P,
+                      alpha=2.0, n_hot=1, dtype="f32")
+    A = O.estimate_block_sums(w.q.astype(np.float64), w.k.astype(np.float64), P, S)
+    ref = _block_sums_via_torch(w.q.astype(np.float64), w.k.astype(np.float64), P, S)
+    np.testing.assert_allclose(A, ref, rtol=1e-10, atol=1e-12)
+
+
+def test_block_sums_row_invariant_and_causality():
+    w = make_workload(seed=3, B=2, Hq=4, Hkv=2, d=32, Lk=1024, q_start_pos=512,
+                      alpha=3.0, n_hot=2, dtype="bf16")
+    S = 8
+    A = O.estimate_block_sums(w.q, w.k, w.q_start_pos, S)
+    r = 128 // S
+    np.testing.assert_allclose(A.sum(axis=-1), r, rtol=0, atol=1e-11)
+    cur = w.q_start_pos // 128
+    for qb in range(A.shape[2]):
+        assert np.all(A[:, :, qb, cur + qb + 1:] == 0.0)
+        assert np.all(A[:, :, qb, :cur + qb + 1] > 0.0)
+
+
+def test_block_sums_uniform_keys_closed_form():
+    """Identical keys give equal scores per row, so row I spreads 1/(I+1) over J <= I."""
+    S, P, Lq, d = 8, 256, 256, 8
+    rng = np.random.default_rng(5)
+    q = rng.standard_normal((1, Lq, 1, d))
+    k = np.tile(rng.standard_normal((1, 1, 1, d)), (1, P + Lq, 1, 1))
+    A = O.estimate_block_sums(q, k, P, S)
+    r = 128 // S
+    expect = np.zeros_like(A)
+    for qb in range(Lq // 128):
+        for i in range(r):
+            I = P // S + qb * r + i
+            for J in range(I + 1):
+                expect[0, 0, qb, J // r] += 1.0 / (I + 1)
+    np.testing.assert_allclose(A, expect, rtol=1e-12, atol=1e-14)
+
+
+def test_chunked_rows_equal_full_sequence_estimate():
+    """A chunk's block sums equal the matching rows of the whole-sequence
+    estimate (the pages: chunked estimation gives identical density)."""
+    S = 8
+    w = make_workload(seed=21, B=1, Hq=2, Hkv=1, d=32, Lk=1024, q_start_pos=0,
+                      alpha=3.0, n_hot=2, dtype="bf16", q_full=True)
+    full = O.estimate_block_sums(w.q, w.k, 0, S)
+    for P in (256, 512, 768):
+        Lk = P + 256
+        part = O.estimate_block_sums(w.q[:, P:Lk], w.k[:, :Lk], P, S)
+        np.testing.assert_allclose(part, full[:, :, P // 128:Lk // 128, :Lk // 128],
+                                   rtol=1e-12, atol=1e-15)
+
+
+# ----------------------------------------------------------------------------
+# a4: selection
+# ----------------------------------------------------------------------------
+def test_selection_worked_example():
+    g = _golden("selection_worked_example.json")
+    row = np.array(g["row"])
+    rs = O.select_row(row, g["forced"], len(row), g["threshold"])
+    assert sorted(np.nonzero(rs.selected)[0].tolist()) == g["selected"]
+    order = np.argsort(-row, kind="stable")
+    np.testing.assert_allclose(np.cumsum(row[order]), g["sorted_cumsum"], atol=1e-12)
+
+
+def _brute_min_cover(vals, forced, tau):
+    n = len(vals)
+    total = vals.sum()
+    free = [i for i in range(n) if i not in forced]
+    for extra in range(len(free) + 1):
+        best = None
+        for comb in itertools.combinations(free, extra):
+            s = vals[list(forced)].sum() + vals[list(comb)].sum()
+            if s >= tau * total and (best is None or s > best[0]):
+                best = (s, set(forced) | set(comb))
+        if best is not None:
+            return len(best[1]), best[0]
+    return n, total
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_selection_is_minimal_cover(seed):
+    rng = np.random.default_rng(seed)
+    n = int(rng.integers(2, 12))
+    vals = rng.random(n) ** 3
+    diag = n - 1
+    forced = sorted({0, diag})
+    tau = float(rng.choice([0.5, 0.8, 0.9, 0.95, 0.99]))
+    rs = O.select_row(vals, forced, n, tau)
+    sel = np.nonzero(rs.selected)[0]
+    assert set(forced) <= set(sel.tolist())
+    size, best_mass = _brute_min_cover(vals, forced, tau)
+    assert len(sel) == size
+    assert abs(vals[sel].sum() - best_mass) <= 1e-12
+
+
+def test_selection_threshold_one_keeps_all_causal():
+    A = np.array([0.5, 0.0, 0.2, 0.3, 0.0, 0.0])
+    rs = O.select_row(A, [0, 3], 4, 1.0)
+    assert rs.selected.tolist() == [True, True, True, True, False, False]
+
+
+def test_selection_forced_mass_counts():
+    # forced sink+diag already hold 0.95 of the mass: nothing else is needed at 0.9
+    A = np.array([0.6, 0.02, 0.03, 0.35])
+    rs = O.select_row(A, [0, 3], 4, 0.9)
+    assert rs.selected.tolist() == [True, False, False, True]
+
+
+def test_estimate_mask_structure_and_tau1():
+    w = make_workload(seed=9, B=1, Hq=4, Hkv=2, d=32, Lk=1024, q_start_pos=512,
+                      alpha=3.0, n_hot=1, dtype="bf16")
+    cur = w.q_start_pos // 128
+    est = O.xattn_estimate(w.q, w.k, w.q_start_pos, 8, 0.9)
+    for qb in range(est.mask.shape[2]):
+        assert est.mask[:, :, qb, 0].all() and est.mask[:, :, qb, cur + qb].all()
+        assert not est.mask[:, :, qb, cur + qb + 1:].any()
+    full = O.xattn_estimate(w.q, w.k, w.q_start_pos, 8, 1.0)
+    for qb in range(full.mask.shape[2]):
+        assert full.mask[:, :, qb, :cur + qb + 1].all()
+
+
+# ----------------------------------------------------------------------------
+# a5: block-sparse attention
+# ----------------------------------------------------------------------------
+def _torch_attention(q, k, v, allowed):
+    """fp64 torch attention with a boolean [Lq, Lk] mask, plus logsumexp."""
+    d = q.shape[-1]
+    qt, kt, vt = (torch.from_numpy(np.asarray(x, np.float64)) for x in (q, k, v))
+    o = torch.nn.functional.scaled_dot_product_attention(
+        qt[None, None], kt[None, None], vt[None, None],
+        attn_mask=torch.from_numpy(allowed)[None, None], scale=1.0 / math.sqrt(d))[0, 0]
+    s = (qt @ kt.T) / math.sqrt(d)
+    lse = torch.logsumexp(s.masked_fill(~torch.from_numpy(allowed), -math.inf), dim=-1)
+    return o.numpy(), lse.numpy()
+
+
+@pytest.mark.parametrize("P,density", [(0, 1.0), (0, 0.5), (384, 0.4), (256, 1.0)])
+def test_bsa_matches_torch_attention(P, density):
+    w = make_workload(seed=31, B=1, Hq=4, Hkv=2, d=32, Lk=P + 384, q_start_pos=P,
+                      alpha=2.0, n_hot=1, dtype="bf16")
+    Lq, Lk = w.q.shape[1], w.k.shape[1]
+    mask = random_block_mask(4, 1, 4, Lq // 128, Lk // 128, P, density)
+    o, lse = O.bsa_prefill(w.q, w.k, w.v, mask, P, 0, Lk // 128)
+    for h in range(4):
+        allowed = np.zeros((Lq, Lk), bool)
+        for i in range(Lq):
+            for j in range(P + i + 1):
+                allowed[i, j] = bool(mask[0, h, i // 128, j // 128])
+        o_ref, lse_ref = _torch_attention(w.q[0, :, h], w.k[0, :, h // 2], w.v[0, :, h // 2], allowed)
+        np.testing.assert_allclose(o[0, :, h], o_ref, rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(lse[0, h], lse_ref, rtol=1e-12, atol=1e-12)
+
+
+def test_bsa_empty_range_and_tau1_is_dense_causal():
+    P = 256
+    w = make_workload(seed=8, B=1, Hq=2, Hkv=1, d=16, Lk=P + 256, q_start_pos=P,
+                      alpha=3.0, n_hot=1, dtype="f32")
+    Lq, Lk = 256, P + 256
+    est = O.xattn_estimate(w.q, w.k, P, 8, 1.0)
+    o, lse = O.bsa_prefill(w.q, w.k, w.v, est.mask, P, 0, Lk // 128)
+    allowed = np.tril(np.ones((Lq, Lk), bool), k=P)
+    for h in range(2):
+        o_ref, lse_ref = _torch_attention(w.q[0, :, h], w.k[0, :, 0], w.v[0, :, 0], allowed)
+        np.testing.assert_allclose(o[0, :, h], o_ref, rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(lse[0, h], lse_ref, rtol=1e-12, atol=1e-12)
+    o0, lse0 = O.bsa_prefill(w.q, w.k, w.v, est.mask, P, 1, 1)
+    assert np.all(o0 == 0.0) and np.all(np.isneginf(lse0))
+
+
+# ----------------------------------------------------------------------------
+# a6: merge
+# ----------------------------------------------------------------------------
+def test_merge_of_split_keys_equals_single_softmax():
+    P = 512
+    w = make_workload(seed=12, B=2, Hq=4, Hkv=1, d=32, Lk=P + 256, q_start_pos=P,
+                      alpha=3.0, n_hot=2, dtype="bf16")
+    Lk = w.k.shape[1]
+    mask = random_block_mask(6, 2, 4, 2, Lk // 128, P, 0.6)
+    cur = P // 128
+    oh, lh = O.bsa_prefill(w.q, w.k, w.v, mask, P, 0, cur)
+    oc, lc = O.bsa_prefill(w.q, w.k, w.v, mask, P, cur, Lk // 128)
+    oa, la = O.bsa_prefill(w.q, w.k, w.v, mask, P, 0, Lk // 128)
+    om, lm = O.merge_attn(oh, lh, oc, lc)
+    np.testing.assert_allclose(om, oa, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(lm, la, rtol=1e-12, atol=1e-12)
+    om2, lm2 = O.merge_attn(oc, lc, oh, lh)
+    np.testing.assert_allclose(om2, om, rtol=1e-13, atol=1e-14)
+
+
+def test_merge_identities():
+    rng = np.random.default_rng(2)
+    o1 = rng.standard_normal((1, 8, 2, 4))
+    l1 = rng.standard_normal((1, 2, 8))
+    o2 = rng.standard_normal((1, 8, 2, 4))
+    ninf = np.full((1, 2, 8), -np.inf)
+    o, l = O.merge_attn(o1, l1, o2, ninf)
+    np.testing.assert_array_equal(o, o1)
+    np.testing.assert_array_equal(l, l1)
+    o, l = O.merge_attn(o1, ninf, o2, ninf)
+    assert np.all(o == 0.0) and np.all(np.isneginf(l))
+    # equal LSEs: plain average, LSE + ln 2
+    o, l = O.merge_attn(o1, l1, o2, l1)
+    np.testing.assert_allclose(o, 0.5 * (o1 + o2), rtol=1e-14)
+    np.testing.assert_allclose(l, l1 + math.log(2.0), rtol=1e-14)
+
+
+# ----------------------------------------------------------------------------
+# a7: CPU-block map
+# ----------------------------------------------------------------------------
+def test_map_golden_example():
+    g = _golden("cpu_block_map_example.json")
+    mask = np.zeros((1, g["heads"], g["nqb"], g["nkb"]), bool)
+    for h, qb, kb in g["selected"]:
+        mask[0, h, qb, kb] = True
+    keep = O.map_mask_to_cpu_blocks(mask, g["q_start_pos"], g["cpu_block_tokens"])
+    assert keep[0].tolist() == g["keep_or_only"]
+    keep = O.map_mask_to_cpu_blocks(mask, g["q_start_pos"], g["cpu_block_tokens"], True)
+    assert keep[0].tolist() == g["keep_force_first_last"]
+
+
+@pytest.mark.parametrize("cpu_tokens", [1024, 4096])
+def test_map_by_scatter(cpu_tokens):
+    P = 8192
+    mask = random_block_mask(1, 2, 3, 4, P // 128 + 4, P, 0.02).astype(bool)
+    keep = O.map_mask_to_cpu_blocks(mask, P, cpu_tokens)
+    expect = np.zeros((2, P // cpu_tokens), np.uint8)
+    for b, h, qb, kb in zip(*np.nonzero(mask)):
+        if kb * 128 < P:
+            expect[b, (kb * 128) // cpu_tokens] = 1
+    np.testing.assert_array_equal(keep, expect)
+
+
+def test_chunk_step_runs_and_merges():
+    P = 256
+    w = make_workload(seed=4, B=1, Hq=2, Hkv=1, d=16, Lk=P + 256, q_start_pos=P,
+                      alpha=3.0, n_hot=1, dtype="bf16")
+    est, o, lse, keep = O.chunk_step(w.q, w.k, w.v, P, 8, 0.9, 128)
+    oa, la = O.bsa_prefill(w.q, w.k, w.v, est.mask, P, 0, w.k.shape[1] // 128)
+    np.testing.assert_allclose(o, oa, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(lse, la, rtol=1e-12, atol=1e-12)
+    assert keep.shape == (1, P // 128)
