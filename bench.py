@@ -1,0 +1,395 @@
+"""Benchmark: chunked-prefill tokens/s per layer for one 4096-token chunk.
+
+One step is the whole hot path for one chunk of one attention layer:
+  bsx_xattn_estimate (scores, softmax, block sums, selection)
+  -> bsx_bsa_prefill on the history key blocks
+  -> bsx_bsa_prefill on the current chunk's key blocks
+  -> bsx_merge_attn of the two (O, LSE) pairs
+  -> bsx_map_mask_to_cpu_blocks (1024-token CPU blocks)
+on the default workload "llama8b-32k-chunk4096" (32 q-heads, 8 kv-heads,
+head_dim 128, bf16, a 4096-token chunk at q_start_pos 28672 against 32768
+causal keys, stride 8, threshold 0.95, seeded planted-direction inputs).
+
+Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events
+on the launching stream; L2 is flushed (a 256 MiB write) between timed steps,
+outside the events.  value = tokens/s/layer over all ranks (each rank runs an
+independent replica; the path has no cross-GPU exchange).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference     # the fp64 CPU oracle, timed on a sample
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from block_sparse_long_xattn_gb300.inputs import CONFIGS, make_workload  # noqa: E402
+
+DEFAULT_WORKLOAD = "llama8b-32k-chunk4096"
+METRIC = "chunked-prefill tokens/s/layer at 32K ctx; % of bf16 TC / HBM roofline"
+UNIT = "tokens/s/layer"
+DOMINANT = "bsa_prefill"
+BSA_SOURCES = ("bsa_tc.cu", "bsa_simt.cu")
+
+
+def _env_rank():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p["hbm_gbs"], p["bf16_tflops"], "measured (MEASURED_PEAKS.json, burst)"
+    return 6800.0, 1900.0, "fallback"
+
+
+def _source_sha(names):
+    h = hashlib.sha256()
+    for n in names:
+        p = os.path.join(ROOT, "block_sparse_long_xattn_gb300", "csrc", n)
+        if os.path.exists(p):
+            h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_per_launch(kernel_key):
+    """DRAM bytes per launch of the dominant kernel from a committed ncu
+    summary, or None when it is absent or was taken on different source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        t = json.load(f)
+    e = t.get(kernel_key)
+    if not e or e.get("source_sha") != _source_sha(BSA_SOURCES):
+        return None
+    return e.get("bytes_per_launch_full")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[4:]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        pmax = max(r[2] for r in rows)
+        loaded = [r for r in rows if r[2] >= 0.5 * pmax] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3][1:5])
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded),
+                "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": pmax, "samples": len(rows), "reasons": reasons}
+
+
+def bsa_flops(mask: np.ndarray, q_start_pos: int, kb_begin: int, kb_end: int, d: int) -> float:
+    """4*d flops per (query, key) pair the block-sparse attention computes:
+    whole 128x128 tiles below the diagonal, the causal half on it."""
+    B, Hq, nqb, nkb = mask.shape
+    cur = q_start_pos // 128
+    m = mask[..., kb_begin:kb_end].astype(bool)
+    kb = np.arange(kb_begin, kb_end)[None, None, None, :]
+    diag = cur + np.arange(nqb)[None, None, :, None]
+    pairs = np.where(kb < diag, 128 * 128, np.where(kb == diag, 128 * 129 // 2, 0))
+    return float(4 * d * (m * pairs).sum())
+
+
+def estimate_flops(cfg, q_len, q_start_pos, stride):
+    """2*d*S flops per allowed reshaped (I, J) pair and q-head."""
+    R = q_len // stride
+    I = q_start_pos // stride + np.arange(R)
+    pairs = float((I + 1).sum())
+    return 2.0 * cfg["d"] * stride * pairs * cfg["Hq"] * cfg["B"]
+
+
+# ---------------------------------------------------------------------------
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import block_sparse_long_xattn_gb300 as bsx
+
+    rank, world, local = _env_rank()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = dict(CONFIGS[args.workload])
+    S, tau = cfg.pop("stride"), cfg.pop("threshold")
+    cfg.pop("chunk", None)
+    w = make_workload(seed=args.seed + rank, **cfg)
+    B, Lq, Hq, d = w.q.shape
+    P, Lk, Hkv = w.q_start_pos, w.k.shape[1], cfg["Hkv"]
+    cur, nkb = P // 128, Lk // 128
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+
+    host = {n: torch.from_numpy(x).to(tdt).pin_memory() for n, x in
+            (("q", w.q), ("k", w.k), ("v", w.v))}
+    dq, dk, dv = (host[n].to(dev) for n in ("q", "k", "v"))
+    mask = torch.empty((B, Hq, Lq // 128, nkb), dtype=torch.uint8, device=dev)
+    ws = torch.empty(bsx.bsx_estimate_workspace_bytes(bsx.shape_of(dq, dk), Lq, P, S),
+                     dtype=torch.uint8, device=dev)
+    oh = torch.empty_like(dq)
+    oc = torch.empty_like(dq)
+    lh = torch.empty((B, Hq, Lq), dtype=torch.float32, device=dev)
+    lc = torch.empty_like(lh)
+    keep = torch.empty((B, P // 1024), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    LAUNCHES_PER_STEP = 6  # estimate scores + selection, BSA x2, merge, map
+
+    def step(q, k, v, ev=None):
+        if ev:
+            ev[0].record(stream)
+        bsx.bsx_xattn_estimate(q, k, P, S, tau, mask=mask, workspace=ws, stream=stream)
+        if ev:
+            ev[1].record(stream)
+        bsx.bsx_bsa_prefill(q, k, v, mask, P, 0, cur, o=oh, lse=lh, stream=stream)
+        if ev:
+            ev[2].record(stream)
+        bsx.bsx_bsa_prefill(q, k, v, mask, P, cur, nkb, o=oc, lse=lc, stream=stream)
+        if ev:
+            ev[3].record(stream)
+        bsx.bsx_merge_attn(oh, lh, oc, lc, stream=stream)
+        bsx.bsx_map_mask_to_cpu_blocks(mask, P, 1024, keep=keep, stream=stream)
+        if ev:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        step(dq, dk, dv)
+    torch.cuda.synchronize()
+    mask_np = mask.cpu().numpy()
+    flops_hist = bsa_flops(mask_np, P, 0, cur, d)
+    flops_curr = bsa_flops(mask_np, P, cur, nkb, d)
+    causal_blocks = sum(cur + qb + 1 for qb in range(Lq // 128)) * B * Hq
+    density = float(mask_np.astype(bool).sum()) / causal_blocks
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            step(dq, dk, dv, evs[i])
+        torch.cuda.synchronize()
+    clocks = clk.summary()
+    t_step = [evs[i][0].elapsed_time(evs[i][4]) for i in range(args.steps)]
+    t_est = [evs[i][0].elapsed_time(evs[i][1]) for i in range(args.steps)]
+    t_bh = [evs[i][1].elapsed_time(evs[i][2]) for i in range(args.steps)]
+    t_bc = [evs[i][2].elapsed_time(evs[i][3]) for i in range(args.steps)]
+    t_tail = [evs[i][3].elapsed_time(evs[i][4]) for i in range(args.steps)]
+    ms_step = float(np.mean(t_step))
+
+    # end to end through the public API: pinned host inputs in, O/LSE/keep out
+    out_host = torch.empty(oh.shape, dtype=oh.dtype).pin_memory()
+    lse_host = torch.empty(lh.shape, dtype=torch.float32).pin_memory()
+    keep_host = torch.empty(keep.shape, dtype=torch.uint8).pin_memory()
+    e2e_ms = []
+    for i in range(max(3, args.steps // 2)):
+        flush.zero_()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        q2 = host["q"].to(dev, non_blocking=True)
+        k2 = host["k"].to(dev, non_blocking=True)
+        v2 = host["v"].to(dev, non_blocking=True)
+        step(q2, k2, v2)
+        out_host.copy_(oh, non_blocking=True)
+        lse_host.copy_(lh, non_blocking=True)
+        keep_host.copy_(keep, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms.append(e0.elapsed_time(e1))
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in (out_host, lse_host, keep_host))
+
+    times = torch.tensor([ms_step, float(np.mean(e2e_ms))], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    ms_step, ms_e2e = times.tolist()
+    tokens = B * Lq * world
+    value = tokens / (ms_step / 1e3)
+
+    hbm_peak, tc_peak, peak_src = _peaks()
+    bsa_ms = float(np.mean(t_bh) + np.mean(t_bc)) / 2.0        # average launch
+    bsa_flops_launch = (flops_hist + flops_curr) / 2.0
+    achieved = bsa_flops_launch / (bsa_ms / 1e3) / 1e12
+    traffic = _traffic_per_launch("bsa_prefill")
+    est_fl = estimate_flops(cfg, Lq, P, S)
+    est_bytes = (dq.numel() + dk.numel()) * dq.element_size() + mask.numel()
+    est_ms = float(np.mean(t_est))
+
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic (seeded planted-direction N(0,1) inputs)",
+        "config": {"workload": args.workload, "B": B, "Hq": Hq, "Hkv": Hkv, "d": d,
+                   "q_len": Lq, "q_start_pos": P, "Lk": Lk, "stride": S, "threshold": tau,
+                   "cpu_block_tokens": 1024, "parallelism": f"replicas{world}",
+                   "l2": "flushed (256 MiB write) between timed steps", "seed": args.seed},
+        "roofline": {"kernel": DOMINANT, "bound": "tensor", "achieved": achieved,
+                     "peak": tc_peak, "unit": "TFLOP/s", "frac": achieved / tc_peak,
+                     "traffic": traffic, "peak_source": peak_src,
+                     "flops_per_launch": bsa_flops_launch, "ms_per_launch": bsa_ms},
+        "kernels": {
+            "estimate_ms": est_ms, "bsa_hist_ms": float(np.mean(t_bh)),
+            "bsa_curr_ms": float(np.mean(t_bc)), "merge_map_ms": float(np.mean(t_tail)),
+            "estimate_tflops": est_fl / (est_ms / 1e3) / 1e12,
+            "estimate_tc_frac": est_fl / (est_ms / 1e3) / 1e12 / tc_peak,
+            "estimate_gbs": est_bytes / (est_ms / 1e3) / 1e9,
+            "estimate_hbm_frac": est_bytes / (est_ms / 1e3) / 1e9 / hbm_peak,
+            "bsa_hist_tflops": flops_hist / (np.mean(t_bh) / 1e3) / 1e12,
+            "bsa_curr_tflops": flops_curr / (np.mean(t_bc) / 1e3) / 1e12,
+        },
+        "density": density,
+        "e2e": {"value": tokens / (ms_e2e / 1e3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = oracle_baseline(w, S, tau, args.cpu_heads)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+def _oracle_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def oracle_baseline(w, stride, tau, n_heads):
+    """Time the fp64 oracle's chunk step on a sample of q-heads and scale it to
+    the whole chunk (heads are independent)."""
+    from oracle import xattn_oracle as O
+    G = w.q.shape[2] // w.k.shape[2]
+    heads = list(range(0, w.q.shape[2], G))[:n_heads]
+    t0 = time.perf_counter()
+    for h in heads:
+        kv = h // G
+        O.chunk_step(w.q[:, :, h:h + 1], w.k[:, :, kv:kv + 1], w.v[:, :, kv:kv + 1],
+                     w.q_start_pos, stride, tau, 1024)
+    dt = time.perf_counter() - t0
+    per_step = dt / len(heads) * w.q.shape[2]
+    return {"value": w.q.shape[0] * w.q.shape[1] / per_step, "unit": UNIT,
+            "cores": _oracle_threads(), "kind": "oracle",
+            "sample": f"chunk step for {len(heads)} of {w.q.shape[2]} q-heads "
+                      f"({dt:.1f} s), scaled by the head count"}
+
+
+def run_reference(args):
+    rank, world, _ = _env_rank()
+    if rank != 0:
+        return
+    cfg = dict(CONFIGS[args.workload])
+    S, tau = cfg.pop("stride"), cfg.pop("threshold")
+    cfg.pop("chunk", None)
+    w = make_workload(seed=args.seed, **cfg)
+    for _ in range(args.warmup):
+        oracle_baseline(w, S, tau, 1)
+    vals = [oracle_baseline(w, S, tau, args.cpu_heads) for _ in range(args.steps)]
+    ms = float(np.mean([w.q.shape[1] / v["value"] * 1e3 for v in vals]))
+    value = w.q.shape[0] * w.q.shape[1] / (ms / 1e3)
+    base = dict(vals[-1])
+    base["value"] = value
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded planted-direction N(0,1) inputs)",
+        "config": {"workload": args.workload, "parallelism": "cpu oracle, rank 0 only"},
+        "cpu_baseline": base,
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(CONFIGS))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-heads", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "gb300":
+        ap.error("at least 3 warm-up steps")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

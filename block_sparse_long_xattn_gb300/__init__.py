@@ -1,1 +1,22 @@
-"""XAttention block-sparse chunked prefill for GB300 (sm_103a)."""
+"""XAttention block-sparse chunked prefill for GB300 (sm_103a).
+
+The compute lives in libbsxattn.so (hand-written CUDA, C ABI declared in
+include/bsxattn.h).  This package holds the ctypes binding (same names as the
+C entry points), the in-tree build script and the seeded input generator.
+Importing the package does not load the library; the first call does, and it
+raises if the library has not been built.
+"""
+from ._lib import (  # noqa: F401
+    BSX_FORCE_FIRST_LAST,
+    BsxError,
+    BsxShape,
+    bsx_bsa_prefill,
+    bsx_estimate_workspace_bytes,
+    bsx_last_error,
+    bsx_map_mask_to_cpu_blocks,
+    bsx_merge_attn,
+    bsx_version,
+    bsx_xattn_estimate,
+    load,
+    shape_of,
+)

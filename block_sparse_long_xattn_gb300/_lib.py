@@ -1,0 +1,194 @@
+"""ctypes binding of libbsxattn.so: argument marshalling only.
+
+Every computation runs in the library's CUDA kernels; this module turns torch
+tensors into device pointers, sizes and the current CUDA stream, calls the C
+entry point of the same name and raises on a non-zero status.  There is no
+other implementation to fall back to: if the shared library is missing the
+first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libbsxattn.so")
+
+BSX_F32, BSX_BF16 = 0, 1
+BSX_FORCE_FIRST_LAST = 1
+STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported", -3: "CUDA error",
+          -4: "bounded device wait expired", -5: "workspace missing or too small"}
+
+EXPORTS = ("bsx_version", "bsx_status_string", "bsx_estimate_workspace_bytes",
+           "bsx_xattn_estimate", "bsx_bsa_prefill", "bsx_merge_attn",
+           "bsx_map_mask_to_cpu_blocks", "bsx_last_error")
+
+
+class BsxShape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int),
+                ("d", ctypes.c_int), ("dtype", ctypes.c_int)]
+
+
+class BsxError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)} ({status})")
+        self.status = status
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the library once and declare the C signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"libbsxattn.so not found at {path}: build it with "
+                "`python -m block_sparse_long_xattn_gb300.build` (no CPU fallback exists)")
+        lib = ctypes.CDLL(path)
+        vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.bsx_version.restype = i32
+        lib.bsx_version.argtypes = []
+        lib.bsx_status_string.restype = ctypes.c_char_p
+        lib.bsx_status_string.argtypes = [i32]
+        lib.bsx_estimate_workspace_bytes.restype = sz
+        lib.bsx_estimate_workspace_bytes.argtypes = [BsxShape, i32, i32, i32]
+        lib.bsx_xattn_estimate.restype = i32
+        lib.bsx_xattn_estimate.argtypes = [BsxShape, vp, vp, i32, i32, i32, f32, vp, vp,
+                                           vp, sz, vp]
+        lib.bsx_bsa_prefill.restype = i32
+        lib.bsx_bsa_prefill.argtypes = [BsxShape, vp, vp, vp, vp, i32, i32, i32, i32,
+                                        vp, vp, vp]
+        lib.bsx_merge_attn.restype = i32
+        lib.bsx_merge_attn.argtypes = [BsxShape, i32, vp, vp, vp, vp, vp]
+        lib.bsx_map_mask_to_cpu_blocks.restype = i32
+        lib.bsx_map_mask_to_cpu_blocks.argtypes = [BsxShape, vp, i32, i32, i32, i32, vp, vp]
+        lib.bsx_last_error.restype = i32
+        lib.bsx_last_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+        _lib = lib
+        return lib
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise BsxError(fn, status)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BSX_BF16
+    if t.dtype == torch.float32:
+        return BSX_F32
+    raise TypeError(f"unsupported dtype {t.dtype}; bsxattn takes bfloat16 or float32")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("bsxattn takes CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("bsxattn takes contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def shape_of(q: torch.Tensor, k: torch.Tensor) -> BsxShape:
+    B, _, Hq, d = q.shape
+    Hkv = k.shape[2]
+    return BsxShape(B, Hq, Hkv, d, _dtype_code(q))
+
+
+# --------------------------------------------------------------------------
+# entry points (same names as the C ABI)
+# --------------------------------------------------------------------------
+def bsx_version() -> int:
+    return load().bsx_version()
+
+
+def bsx_estimate_workspace_bytes(shape: BsxShape, q_len: int, q_start_pos: int,
+                                 stride: int) -> int:
+    return int(load().bsx_estimate_workspace_bytes(shape, q_len, q_start_pos, stride))
+
+
+def bsx_xattn_estimate(q, k, q_start_pos: int, stride: int, threshold: float, *,
+                       mask=None, block_sums=None, workspace=None, stream=None):
+    """uint8 block mask [B, Hq, q_len/128, Lk/128] for the chunk (see bsxattn.h)."""
+    lib = load()
+    B, q_len, Hq, _ = q.shape
+    Lk = k.shape[1]
+    shape = shape_of(q, k)
+    if mask is None:
+        mask = torch.empty((B, Hq, q_len // 128, Lk // 128), dtype=torch.uint8, device=q.device)
+    need = lib.bsx_estimate_workspace_bytes(shape, q_len, q_start_pos, stride)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("bsx_xattn_estimate", lib.bsx_xattn_estimate(
+        shape, _ptr(q), _ptr(k), q_len, q_start_pos, stride, float(threshold),
+        _ptr(mask), _ptr(block_sums), _ptr(workspace), ws_bytes, _stream(stream)))
+    return mask
+
+
+def bsx_bsa_prefill(q, k, v, mask, q_start_pos: int, kb_begin: int = 0,
+                    kb_end: int | None = None, *, o=None, lse=None, stream=None):
+    """Block-sparse causal attention over key blocks [kb_begin, kb_end) -> (o, lse)."""
+    lib = load()
+    B, q_len, Hq, d = q.shape
+    if kb_end is None:
+        kb_end = k.shape[1] // 128
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, q_len), dtype=torch.float32, device=q.device)
+    _check("bsx_bsa_prefill", lib.bsx_bsa_prefill(
+        shape_of(q, k), _ptr(q), _ptr(k), _ptr(v), _ptr(mask), q_len, q_start_pos,
+        kb_begin, kb_end, _ptr(o), _ptr(lse), _stream(stream)))
+    return o, lse
+
+
+def bsx_merge_attn(o1, lse1, o2, lse2, *, stream=None):
+    """In-place LSE merge of (o2, lse2) into (o1, lse1); returns (o1, lse1)."""
+    lib = load()
+    B, q_len, Hq, d = o1.shape
+    shape = BsxShape(B, Hq, Hq, d, _dtype_code(o1))
+    _check("bsx_merge_attn", lib.bsx_merge_attn(
+        shape, q_len, _ptr(o1), _ptr(lse1), _ptr(o2), _ptr(lse2), _stream(stream)))
+    return o1, lse1
+
+
+def bsx_map_mask_to_cpu_blocks(mask, q_start_pos: int, cpu_block_tokens: int = 1024,
+                               force_first_last: bool = False, *, keep=None, stream=None):
+    """uint8 keep flags [B, q_start_pos / cpu_block_tokens] from a block mask."""
+    lib = load()
+    B, Hq, nqb, nkb = mask.shape
+    n_cpu = q_start_pos // cpu_block_tokens
+    if keep is None:
+        keep = torch.empty((B, max(n_cpu, 0)), dtype=torch.uint8, device=mask.device)
+    shape = BsxShape(B, Hq, Hq, 128, BSX_BF16)
+    flags = BSX_FORCE_FIRST_LAST if force_first_last else 0
+    _check("bsx_map_mask_to_cpu_blocks", lib.bsx_map_mask_to_cpu_blocks(
+        shape, _ptr(mask), nqb * 128, q_start_pos, cpu_block_tokens, flags,
+        _ptr(keep) if keep.numel() else None, _stream(stream)))
+    return keep
+
+
+def bsx_last_error() -> int:
+    """Read and clear the device error word; returns the raw word (0 = none)."""
+    code = ctypes.c_uint(0)
+    status = load().bsx_last_error(ctypes.byref(code))
+    if status not in (0, -4):
+        raise BsxError("bsx_last_error", status)
+    return int(code.value)

@@ -1,0 +1,170 @@
+// C ABI of the library: argument validation, kernel choice, launches.
+// Declarations and the meaning of every argument: include/bsxattn.h.
+#include <math.h>
+#include <stdio.h>
+
+#include "../../include/bsxattn.h"
+#include "common.cuh"
+#include "launchers.h"
+
+namespace {
+
+// Device error word (one per device that loads the library).  Kernels that
+// run bounded waits record which wait gave up; bsx_last_error reads it.
+__device__ unsigned g_bsx_err_word = 0;
+
+constexpr int kMaxDevices = 64;
+unsigned* g_err_ptr[kMaxDevices] = {nullptr};
+
+// Device address of the error word for the current device (looked up once
+// per device; host code cannot use the symbol itself as an address).
+unsigned* err_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_bsx_err_word) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Common shape checks; fills the internal problem description.
+int make_problem(const bsx_shape& s, int q_len, int q_start_pos, bsx::Problem* p) {
+  if (s.B < 1 || s.Hq < 1 || s.Hkv < 1 || s.Hq % s.Hkv != 0) return BSX_ERR_INVALID_ARG;
+  if (s.dtype != BSX_F32 && s.dtype != BSX_BF16) return BSX_ERR_UNSUPPORTED;
+  if (s.d != 64 && s.d != 128) return BSX_ERR_UNSUPPORTED;
+  if (q_len < 128 || q_len % 128 != 0) return BSX_ERR_INVALID_ARG;
+  if (q_start_pos < 0 || q_start_pos % 128 != 0) return BSX_ERR_INVALID_ARG;
+  const long long Lk = (long long)q_start_pos + q_len;
+  if (Lk > (1LL << 24)) return BSX_ERR_UNSUPPORTED;
+  p->B = s.B;
+  p->Hq = s.Hq;
+  p->Hkv = s.Hkv;
+  p->d = s.d;
+  p->dtype = s.dtype;
+  p->q_len = q_len;
+  p->q_start_pos = q_start_pos;
+  p->Lk = (int)Lk;
+  p->nqb = q_len / 128;
+  p->nkb = (int)(Lk / 128);
+  return BSX_OK;
+}
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return BSX_OK;
+  fprintf(stderr, "bsxattn: CUDA error %s\n", cudaGetErrorString(e));
+  return BSX_ERR_CUDA;
+}
+
+constexpr int kMaxKeyBlocks = 8192;  // selection sorts up to this many blocks per row
+
+}  // namespace
+
+extern "C" {
+
+int bsx_version(void) { return (0 << 16) | 1; }
+
+const char* bsx_status_string(int status) {
+  switch (status) {
+    case BSX_OK: return "ok";
+    case BSX_ERR_INVALID_ARG: return "invalid argument";
+    case BSX_ERR_UNSUPPORTED: return "unsupported dtype, head dim or stride";
+    case BSX_ERR_CUDA: return "CUDA error";
+    case BSX_ERR_TIMEOUT: return "a bounded device wait expired";
+    case BSX_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+size_t bsx_estimate_workspace_bytes(bsx_shape s, int q_len, int q_start_pos, int stride) {
+  bsx::Problem p;
+  if (make_problem(s, q_len, q_start_pos, &p) != BSX_OK) return 0;
+  if (stride != 4 && stride != 8 && stride != 16) return 0;
+  return (size_t)p.B * p.Hq * p.nkb * (size_t)(q_len / stride) * sizeof(float);
+}
+
+int bsx_xattn_estimate(bsx_shape s, const void* q, const void* k, int q_len,
+                       int q_start_pos, int stride, float threshold, uint8_t* mask,
+                       float* block_sums, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  bsx::Problem p;
+  int rc = make_problem(s, q_len, q_start_pos, &p);
+  if (rc != BSX_OK) return rc;
+  if (stride != 4 && stride != 8 && stride != 16) return BSX_ERR_UNSUPPORTED;
+  if (!(threshold > 0.0f) || isnan(threshold)) return BSX_ERR_INVALID_ARG;
+  if (!q || !k || !mask || !aligned16(q) || !aligned16(k)) return BSX_ERR_INVALID_ARG;
+  if (block_sums && !aligned16(block_sums)) return BSX_ERR_INVALID_ARG;
+  if (p.nkb > kMaxKeyBlocks) return BSX_ERR_UNSUPPORTED;
+  const size_t need = bsx_estimate_workspace_bytes(s, q_len, q_start_pos, stride);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return BSX_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  float* lse_part = static_cast<float*>(workspace);
+  cudaError_t e = bsx::launch_estimate_simt(p, q, k, stride, lse_part, st);
+  if (e != cudaSuccess) return cuda_status(e);
+  e = bsx::launch_select(p, stride, threshold, lse_part, mask, block_sums, st);
+  return cuda_status(e);
+}
+
+int bsx_bsa_prefill(bsx_shape s, const void* q, const void* k, const void* v,
+                    const uint8_t* mask, int q_len, int q_start_pos, int kb_begin,
+                    int kb_end, void* o, float* lse, void* stream) {
+  bsx::Problem p;
+  int rc = make_problem(s, q_len, q_start_pos, &p);
+  if (rc != BSX_OK) return rc;
+  if (kb_begin < 0 || kb_begin > kb_end || kb_end > p.nkb) return BSX_ERR_INVALID_ARG;
+  if (!q || !k || !v || !mask || !o || !lse) return BSX_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return BSX_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = bsx::launch_bsa_simt(p, q, k, v, mask, kb_begin, kb_end, o, lse, st);
+  return cuda_status(e);
+}
+
+int bsx_merge_attn(bsx_shape s, int q_len, void* o1, float* lse1, const void* o2,
+                   const float* lse2, void* stream) {
+  bsx::Problem p;
+  int rc = make_problem(s, q_len, 0, &p);
+  if (rc != BSX_OK) return rc;
+  if (!o1 || !lse1 || !o2 || !lse2) return BSX_ERR_INVALID_ARG;
+  if (!aligned16(o1) || !aligned16(o2)) return BSX_ERR_INVALID_ARG;
+  return cuda_status(bsx::launch_merge(p, o1, lse1, o2, lse2, static_cast<cudaStream_t>(stream)));
+}
+
+int bsx_map_mask_to_cpu_blocks(bsx_shape s, const uint8_t* mask, int q_len,
+                               int q_start_pos, int cpu_block_tokens, int flags,
+                               uint8_t* keep, void* stream) {
+  bsx::Problem p;
+  int rc = make_problem(s, q_len, q_start_pos, &p);
+  if (rc != BSX_OK) return rc;
+  if (cpu_block_tokens < 128 || cpu_block_tokens % 128 != 0) return BSX_ERR_INVALID_ARG;
+  if (q_start_pos % cpu_block_tokens != 0) return BSX_ERR_INVALID_ARG;
+  if ((flags & ~BSX_FORCE_FIRST_LAST) != 0) return BSX_ERR_INVALID_ARG;
+  const int n_cpu = q_start_pos / cpu_block_tokens;
+  if (n_cpu > 0 && (!mask || !keep)) return BSX_ERR_INVALID_ARG;
+  return cuda_status(bsx::launch_map(p, mask, cpu_block_tokens, flags, keep,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+int bsx_last_error(unsigned int* code) {
+  if (!code) return BSX_ERR_INVALID_ARG;
+  *code = 0;
+  unsigned* w = err_word();
+  if (!w) return BSX_ERR_CUDA;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_status(e);
+  unsigned h = 0;
+  e = cudaMemcpy(&h, w, sizeof(h), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (h != 0) {
+    const unsigned zero = 0;
+    e = cudaMemcpy(w, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  *code = h;
+  return h ? BSX_ERR_TIMEOUT : BSX_OK;
+}
+
+}  // extern "C"

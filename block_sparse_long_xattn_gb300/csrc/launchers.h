@@ -1,0 +1,52 @@
+// Host-side launchers of the kernels (one translation unit each).  The C ABI
+// in abi.cu validates arguments and then calls these; they only enqueue work.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace bsx {
+
+struct Problem {
+  int B, Hq, Hkv, d;
+  int dtype;        // 0 = f32, 1 = bf16
+  int q_len, q_start_pos, Lk;
+  int nqb, nkb;     // q_len/128, Lk/128
+};
+
+// a6: in-place LSE merge.
+cudaError_t launch_merge(const Problem& p, void* o1, float* lse1, const void* o2,
+                         const float* lse2, cudaStream_t st);
+
+// a7: CPU-block keep flags.
+cudaError_t launch_map(const Problem& p, const uint8_t* mask, int cpu_block_tokens,
+                       int flags, uint8_t* keep, cudaStream_t st);
+
+// a1-a2 partial: per (b, h, key block, reshaped row) log-sum-exp of the scaled
+// scores of that row over that block's reshaped columns (CUDA cores).
+cudaError_t launch_estimate_simt(const Problem& p, const void* q, const void* k,
+                                 int stride, float* lse_part, cudaStream_t st);
+
+// a1-a2 partial, tensor-core version (bf16, tcgen05).
+cudaError_t launch_estimate_tc(const Problem& p, const void* q, const void* k,
+                               int stride, float* lse_part, unsigned* err,
+                               cudaStream_t st);
+
+// a2-a4: row normalisation, block sums and threshold selection.
+cudaError_t launch_select(const Problem& p, int stride, float threshold,
+                          const float* lse_part, uint8_t* mask, float* block_sums,
+                          cudaStream_t st);
+
+// a5: block-sparse attention on CUDA cores (any dtype, d in {64, 128}).
+cudaError_t launch_bsa_simt(const Problem& p, const void* q, const void* k,
+                            const void* v, const uint8_t* mask, int kb_begin,
+                            int kb_end, void* o, float* lse, cudaStream_t st);
+
+// a5: block-sparse attention on tcgen05 tensor cores (bf16).
+cudaError_t launch_bsa_tc(const Problem& p, const void* q, const void* k,
+                          const void* v, const uint8_t* mask, int kb_begin,
+                          int kb_end, void* o, float* lse, unsigned* err,
+                          cudaStream_t st);
+
+}  // namespace bsx

@@ -1,0 +1,46 @@
+// a7: BSA-block mask -> CPU-block keep flags.
+//
+// nano-vllm task_plan.md "核心设计理解" sections 1 and 3: one 1024-token CPU
+// block holds 8 BSA blocks and is kept if any of them is selected, OR over
+// heads and q-blocks; xattn_bsa.py select_blocks Step 6 aggregates only the
+// history blocks and then adds the first and last one.  One CTA per
+// (b, history CPU block) ORs the Hq * nqb * (cpu_block_tokens/128) bytes.
+#include "common.cuh"
+#include "launchers.h"
+
+namespace bsx {
+namespace {
+
+__global__ void __launch_bounds__(256) map_kernel(
+    const uint8_t* __restrict__ mask, int Hq, int nqb, int nkb, int per,
+    int n_cpu, int force_first_last, uint8_t* __restrict__ keep) {
+  const int c = blockIdx.x;
+  const int b = blockIdx.y;
+  const int pairs = Hq * nqb;
+  int any = 0;
+  for (int idx = threadIdx.x; idx < pairs * per; idx += blockDim.x) {
+    const int hq = idx / per;   // (h, qb) row
+    const int u = idx % per;
+    any |= mask[((long long)b * pairs + hq) * nkb + (long long)c * per + u];
+  }
+  any = __syncthreads_or(any);
+  if (threadIdx.x == 0) {
+    if (force_first_last && (c == 0 || c == n_cpu - 1)) any = 1;
+    keep[(long long)b * n_cpu + c] = any ? 1 : 0;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_map(const Problem& p, const uint8_t* mask, int cpu_block_tokens,
+                       int flags, uint8_t* keep, cudaStream_t st) {
+  const int n_cpu = p.q_start_pos / cpu_block_tokens;
+  if (n_cpu == 0 || p.B == 0) return cudaSuccess;
+  const int per = cpu_block_tokens / kBlock;
+  dim3 grid(n_cpu, p.B);
+  map_kernel<<<grid, 256, 0, st>>>(mask, p.Hq, p.nqb, p.nkb, per, n_cpu,
+                                    (flags & 1) ? 1 : 0, keep);
+  return cudaGetLastError();
+}
+
+}  // namespace bsx

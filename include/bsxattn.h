@@ -1,0 +1,186 @@
+/*
+ * bsxattn.h - C ABI of the XAttention block-sparse chunked-prefill library
+ * for GB300 (sm_103a).
+ *
+ * The library implements one chunk of XAttention chunked prefill as described
+ * by the nano-vllm pages (docs/xattention_algorithm_guide.md, "算法流程";
+ * nanovllm/kvcache/sparse/xattn_bsa.py, XAttentionBSAPolicy.select_blocks and
+ * compute_chunked_prefill):
+ *
+ *   bsx_xattn_estimate       stride-S antidiagonal scores, causal row softmax,
+ *                            128-token block sums and threshold selection
+ *                            -> uint8 block mask
+ *   bsx_bsa_prefill          causal GQA block-sparse attention over the
+ *                            selected 128-token blocks -> O and LSE
+ *   bsx_merge_attn           LSE merge of two partial (O, LSE) pairs
+ *   bsx_map_mask_to_cpu_blocks  1024-token CPU-block keep flags
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensors are caller-owned, contiguous, device-resident (CUDA global
+ *    memory) and 16-byte aligned.  The library never allocates, frees or
+ *    copies to the host on these calls, and never synchronises: work is
+ *    enqueued on `stream` (a cudaStream_t; NULL means the legacy default
+ *    stream) and the call returns.
+ *  - Layouts are token-major:
+ *        q     [B, q_len, Hq, d]            element type `dtype`
+ *        k, v  [B, Lk, Hkv, d]              Lk = q_start_pos + q_len
+ *        mask  [B, Hq, q_len/128, Lk/128]   uint8, 1 = block selected
+ *        o     [B, q_len, Hq, d]            element type `dtype`
+ *        lse   [B, Hq, q_len]               float32, natural log
+ *    GQA: q-head h reads kv-head h / (Hq/Hkv).
+ *  - q_start_pos is the absolute position of the chunk's first query; keys
+ *    are all earlier tokens plus the chunk.  q_start_pos and q_len must be
+ *    multiples of 128 (the BSA block size, fixed at 128 on the pages).
+ *  - Arguments are validated on the host before any launch; a bad argument
+ *    returns BSX_ERR_INVALID_ARG and an unsupported combination (dtype, d,
+ *    stride) returns BSX_ERR_UNSUPPORTED, with nothing enqueued.  There is no
+ *    fallback path.  A CUDA launch error returns BSX_ERR_CUDA.  Errors the
+ *    kernels detect asynchronously (a bounded wait that expired) are
+ *    recorded in a device error word read by bsx_last_error().
+ */
+#ifndef BSXATTN_H_
+#define BSXATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  BSX_OK = 0,
+  BSX_ERR_INVALID_ARG = -1,
+  BSX_ERR_UNSUPPORTED = -2,
+  BSX_ERR_CUDA = -3,
+  BSX_ERR_TIMEOUT = -4,
+  BSX_ERR_WORKSPACE = -5
+} bsx_status;
+
+typedef enum { BSX_F32 = 0, BSX_BF16 = 1 } bsx_dtype;
+
+/* Problem shape shared by all calls.  Hq % Hkv == 0; d in {64, 128}. */
+typedef struct {
+  int B;      /* batch (sequences of equal length and equal q_start_pos) */
+  int Hq;     /* query heads */
+  int Hkv;    /* key/value heads */
+  int d;      /* head dimension */
+  int dtype;  /* bsx_dtype of q, k, v and o */
+} bsx_shape;
+
+/* Flags for bsx_map_mask_to_cpu_blocks. */
+#define BSX_FORCE_FIRST_LAST 1
+
+/* Library version, (major << 16) | minor. */
+int bsx_version(void);
+
+/* Static description of a status code.  Never NULL. */
+const char* bsx_status_string(int status);
+
+/*
+ * Bytes of device scratch bsx_xattn_estimate needs for this problem: one
+ * float per (batch, q-head, key block, reshaped query row), i.e.
+ * B * Hq * (Lk/128) * (q_len/stride) * 4.  Returns 0 for invalid arguments.
+ */
+size_t bsx_estimate_workspace_bytes(bsx_shape s, int q_len, int q_start_pos,
+                                    int stride);
+
+/*
+ * XAttention estimate + block selection for one Q chunk.
+ *
+ * Defined by docs/xattention_algorithm_guide.md "算法流程" Phases 1-3 and
+ * "块选择算法 (find_blocks_chunked)", with the chunk offset of xattn_bsa.py
+ * select_blocks Steps 0-4:
+ *   reshaped row I = q_start_pos/S + i (i < q_len/S), reshaped key J < Lk/S;
+ *   s[I,J] = sum_{t<S} q[I*S+S-1-t] . k[J*S+t]                 (inverse mode)
+ *   p[I,:] = softmax over J <= I of s[I,J] / (sqrt(d) * S)
+ *   A[qb,kb] = sum of p over the (128/S) rows of q-block qb and the
+ *              (128/S) columns of key block kb
+ *   per (b, h, qb): blocks 0 and diag = q_start_pos/128 + qb are kept; the
+ *   others are taken by descending A (ties: lower kb first) while the
+ *   cumulative mass (forced blocks included) is below threshold * sum(A);
+ *   the block that crosses the threshold is kept; threshold >= 1 keeps every
+ *   causal block; blocks after the diagonal are never kept.
+ *
+ * q [B,q_len,Hq,d], k [B,Lk,Hkv,d] (device, `s.dtype`).
+ * mask (out, device) uint8 [B, Hq, q_len/128, Lk/128]; every byte written.
+ * block_sums (out, device, nullable) float32 [B, Hq, q_len/128, Lk/128]:
+ *   A for kb <= diag, 0 after it.
+ * workspace (device) of at least bsx_estimate_workspace_bytes() bytes,
+ *   overwritten; else BSX_ERR_WORKSPACE.
+ * stride in {4, 8, 16}; 0 < threshold.
+ */
+int bsx_xattn_estimate(bsx_shape s, const void* q, const void* k, int q_len,
+                       int q_start_pos, int stride, float threshold,
+                       uint8_t* mask, float* block_sums, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/*
+ * Block-sparse causal attention (BSA) over key blocks [kb_begin, kb_end).
+ *
+ * Defined by docs/xattention_algorithm_guide.md "BSA (Block Sparse
+ * Attention)" (block_sparse_attn_func with is_causal, 128-token blocks,
+ * per-head block mask) and xattn_bsa.py compute_chunked_prefill (history and
+ * current chunk computed separately, each returning O and LSE):
+ *   query row i (position q_start_pos + i) of head h sees key j iff
+ *   kb_begin*128 <= j < kb_end*128, j <= q_start_pos + i and
+ *   mask[b, h, i/128, j/128] != 0;
+ *   o[b,i,h,:] = sum_j softmax_j(q.k_j / sqrt(d)) v_j,
+ *   lse[b,h,i] = ln sum_j exp(q.k_j / sqrt(d)).
+ * A row that sees no key gets o = 0 and lse = -inf.
+ * 0 <= kb_begin <= kb_end <= Lk/128 (an empty range is allowed).
+ * o (out) [B,q_len,Hq,d] in `s.dtype`; lse (out) float32 [B,Hq,q_len].
+ */
+int bsx_bsa_prefill(bsx_shape s, const void* q, const void* k, const void* v,
+                    const uint8_t* mask, int q_len, int q_start_pos,
+                    int kb_begin, int kb_end, void* o, float* lse,
+                    void* stream);
+
+/*
+ * LSE merge of two partial attentions over disjoint key sets, in place into
+ * (o1, lse1).
+ *
+ * Defined by the nano-vllm optimization guide, "Online Softmax Merge -
+ * Triton Fused Kernel" (merge_attention_outputs):
+ *   m = max(lse1, lse2); w_i = exp(lse_i - m);
+ *   o1 <- (w1*o1 + w2*o2) / (w1 + w2); lse1 <- m + ln(w1 + w2).
+ * Rows whose two LSEs are both -inf get o1 = 0, lse1 = -inf.
+ * o1 (in/out), o2 (in) [B,q_len,Hq,d] in `s.dtype`; lse1 (in/out), lse2 (in)
+ * float32 [B,Hq,q_len].  o2/lse2 must not overlap o1/lse1.
+ */
+int bsx_merge_attn(bsx_shape s, int q_len, void* o1, float* lse1,
+                   const void* o2, const float* lse2, void* stream);
+
+/*
+ * CPU-block keep flags from a BSA block mask.
+ *
+ * Defined by nano-vllm task_plan.md "核心设计理解" section 1 (a 1024-token
+ * CPU block holds 8 BSA blocks) and section 3 (a CPU block is kept if any of
+ * its BSA blocks is selected, OR over heads and q-blocks), and xattn_bsa.py
+ * select_blocks Step 6 (history blocks only; first and last always added):
+ *   keep[b,c] = OR_{h, qb, u < cpu_block_tokens/128}
+ *               mask[b, h, qb, c*cpu_block_tokens/128 + u],
+ *   for the history blocks c < q_start_pos / cpu_block_tokens.
+ * flags & BSX_FORCE_FIRST_LAST also sets the first and last history block.
+ * cpu_block_tokens: a positive multiple of 128 dividing q_start_pos.
+ * keep (out, device) uint8 [B, q_start_pos / cpu_block_tokens].
+ */
+int bsx_map_mask_to_cpu_blocks(bsx_shape s, const uint8_t* mask, int q_len,
+                               int q_start_pos, int cpu_block_tokens,
+                               int flags, uint8_t* keep, void* stream);
+
+/*
+ * Read and clear the device error word of the current device.  Waits for
+ * the device to finish its work (this call is a diagnostic, not part of the
+ * hot path).  *code receives the raw word (0 = no error; otherwise the
+ * kernel and the wait that gave up).  Returns BSX_OK, BSX_ERR_TIMEOUT when
+ * the word was set, or BSX_ERR_CUDA.
+ */
+int bsx_last_error(unsigned int* code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSXATTN_H_ */

@@ -1,0 +1,98 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The shared library must load, export every entry point include/bsxattn.h
+declares, and reject bad arguments on the host before touching the device.
+None of these calls launches a kernel.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from block_sparse_long_xattn_gb300 import _lib as L
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "bsxattn.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(bsx_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(L.LIB_PATH):
+        from block_sparse_long_xattn_gb300 import build
+        build.build()
+    return L.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert names, "no entry points parsed from the header"
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in bsxattn.h but not exported"
+    assert set(L.EXPORTS) <= set(names)
+
+
+def test_version_and_status_strings(lib):
+    assert lib.bsx_version() >= 1
+    for code in (0, -1, -2, -3, -4, -5, 7):
+        assert lib.bsx_status_string(code)
+
+
+def test_workspace_formula(lib):
+    s = L.BsxShape(1, 32, 8, 128, L.BSX_BF16)
+    # one float per (b, q-head, key block, reshaped row)
+    assert lib.bsx_estimate_workspace_bytes(s, 4096, 28672, 8) == 32 * 256 * 512 * 4
+    assert lib.bsx_estimate_workspace_bytes(s, 4096, 126976, 16) == 32 * 1024 * 256 * 4
+    assert lib.bsx_estimate_workspace_bytes(s, 4000, 0, 8) == 0      # q_len not /128
+    assert lib.bsx_estimate_workspace_bytes(s, 4096, 0, 3) == 0      # bad stride
+
+
+NULL = None
+
+
+def _est(lib, shape, q_len=1024, P=0, stride=8, tau=0.9, ptr=16, ws=1 << 30):
+    p = ctypes.c_void_p(ptr) if ptr else None
+    return lib.bsx_xattn_estimate(shape, p, p, q_len, P, stride, tau, p, None, p, ws, None)
+
+
+def test_estimate_rejects_bad_arguments(lib):
+    good = L.BsxShape(1, 4, 2, 128, L.BSX_BF16)
+    assert _est(lib, L.BsxShape(1, 3, 2, 128, 1)) == -1          # Hq % Hkv
+    assert _est(lib, L.BsxShape(1, 4, 2, 96, 1)) == -2           # head dim
+    assert _est(lib, L.BsxShape(1, 4, 2, 128, 5)) == -2          # dtype
+    assert _est(lib, good, q_len=1000) == -1                     # q_len % 128
+    assert _est(lib, good, P=100) == -1                          # q_start_pos % 128
+    assert _est(lib, good, stride=3) == -2                       # stride
+    assert _est(lib, good, tau=0.0) == -1                        # threshold
+    assert _est(lib, good, tau=float("nan")) == -1
+    assert _est(lib, good, ptr=0) == -1                          # null pointers
+    assert _est(lib, good, ptr=8) == -1                          # misaligned
+    assert _est(lib, good, ws=16) == -5                          # workspace too small
+
+
+def test_bsa_merge_map_reject_bad_arguments(lib):
+    s = L.BsxShape(1, 4, 2, 128, L.BSX_BF16)
+    p = ctypes.c_void_p(16)
+    # kb range outside [0, Lk/128]
+    assert lib.bsx_bsa_prefill(s, p, p, p, p, 256, 256, 2, 1, p, p, None) == -1
+    assert lib.bsx_bsa_prefill(s, p, p, p, p, 256, 256, 0, 5, p, p, None) == -1
+    assert lib.bsx_bsa_prefill(s, p, None, p, p, 256, 256, 0, 4, p, p, None) == -1
+    assert lib.bsx_merge_attn(s, 100, p, p, p, p, None) == -1
+    assert lib.bsx_merge_attn(s, 128, p, None, p, p, None) == -1
+    # cpu block size must divide q_start_pos and be a multiple of 128
+    assert lib.bsx_map_mask_to_cpu_blocks(s, p, 128, 4096, 1000, 0, p, None) == -1
+    assert lib.bsx_map_mask_to_cpu_blocks(s, p, 128, 4096, 3072, 0, p, None) == -1
+    assert lib.bsx_map_mask_to_cpu_blocks(s, p, 128, 4096, 1024, 4, p, None) == -1
+
+
+def test_binding_requires_cuda_tensors():
+    import torch
+    q = torch.zeros(1, 128, 2, 64)
+    with pytest.raises((ValueError, RuntimeError)):
+        L.bsx_bsa_prefill(q, q[:, :, :1], q[:, :, :1], torch.ones(1, 2, 1, 1, dtype=torch.uint8), 0)

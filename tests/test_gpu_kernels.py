@@ -1,0 +1,154 @@
+"""GPU parity of every entry point against the fp64 oracle, at small sizes.
+
+Sizes here let the oracle finish in seconds while still spanning several
+128-token tiles, several key blocks per row, GQA groups, batch 2, every
+supported stride, fp32 and bf16, q_start_pos = 0 and > 0, and the degenerate
+cases (empty key range, a chunk of one block, threshold 1).
+"""
+import numpy as np
+import pytest
+import torch
+
+from block_sparse_long_xattn_gb300 import (
+    bsx_bsa_prefill, bsx_last_error, bsx_map_mask_to_cpu_blocks, bsx_merge_attn,
+    bsx_xattn_estimate)
+from block_sparse_long_xattn_gb300.inputs import make_workload, random_block_mask
+from oracle import xattn_oracle as O
+from tests.helpers import LSE_TOL, O_TOL, check_block_sums, check_mask, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _estimate(w, stride, tau):
+    q, k = to_dev(w.q, w.dtype), to_dev(w.k, w.dtype)
+    B, Lq, Hq, _ = w.q.shape
+    nkb = w.k.shape[1] // 128
+    A = torch.empty((B, Hq, Lq // 128, nkb), dtype=torch.float32, device="cuda")
+    mask = bsx_xattn_estimate(q, k, w.q_start_pos, stride, tau, block_sums=A)
+    torch.cuda.synchronize()
+    return mask.cpu().numpy(), A.cpu().numpy()
+
+
+ESTIMATE_CASES = [
+    # (B, Hq, Hkv, d, Lk, P, stride, tau, dtype, alpha, n_hot)
+    (1, 2, 1, 64, 1024, 0, 8, 0.9, "f32", 3.0, 0),     # the tiny single-chunk config
+    (1, 4, 2, 128, 1024, 512, 8, 0.95, "bf16", 3.0, 2),
+    (2, 4, 1, 64, 768, 256, 4, 0.9, "bf16", 2.0, 1),
+    (1, 8, 2, 128, 2048, 1536, 16, 0.9, "bf16", 4.0, 3),
+    (1, 2, 2, 128, 640, 0, 8, 0.8, "f32", 0.0, 0),
+    (1, 4, 1, 128, 1152, 1024, 8, 0.99, "bf16", 3.0, 2),  # chunk of one block
+    (1, 4, 2, 64, 896, 384, 16, 0.5, "bf16", 3.0, 1),
+]
+
+
+@pytest.mark.parametrize("case", ESTIMATE_CASES)
+def test_estimate_mask_and_block_sums(case):
+    B, Hq, Hkv, d, Lk, P, S, tau, dt, alpha, n_hot = case
+    w = make_workload(seed=100 + Lk + P, B=B, Hq=Hq, Hkv=Hkv, d=d, Lk=Lk, q_start_pos=P,
+                      alpha=alpha, n_hot=n_hot, dtype=dt)
+    mask, A = _estimate(w, S, tau)
+    est = O.xattn_estimate(w.q, w.k, P, S, tau)
+    check_block_sums(A, est.block_sums, S)
+    check_mask(mask, est, tau, P)
+    assert bsx_last_error() == 0
+
+
+def test_estimate_threshold_one_is_full_causal():
+    w = make_workload(seed=5, B=1, Hq=4, Hkv=2, d=128, Lk=1024, q_start_pos=512,
+                      alpha=3.0, n_hot=1, dtype="bf16")
+    mask, _ = _estimate(w, 8, 1.0)
+    cur = 512 // 128
+    for qb in range(4):
+        assert mask[:, :, qb, :cur + qb + 1].all()
+        assert not mask[:, :, qb, cur + qb + 1:].any()
+
+
+BSA_CASES = [
+    # (B, Hq, Hkv, d, Lk, P, dtype, density)
+    (1, 2, 1, 64, 1024, 0, "f32", 1.0),
+    (1, 4, 2, 128, 1024, 512, "bf16", 0.5),
+    (2, 4, 1, 64, 768, 256, "bf16", 0.3),
+    (1, 8, 2, 128, 1536, 1024, "f32", 0.6),
+    (1, 4, 4, 128, 512, 384, "bf16", 1.0),
+]
+
+
+@pytest.mark.parametrize("case", BSA_CASES)
+@pytest.mark.parametrize("cols", ["all", "hist", "curr"])
+def test_bsa_prefill(case, cols):
+    B, Hq, Hkv, d, Lk, P, dt, dens = case
+    w = make_workload(seed=7 + Lk, B=B, Hq=Hq, Hkv=Hkv, d=d, Lk=Lk, q_start_pos=P,
+                      alpha=3.0, n_hot=1, dtype=dt)
+    Lq, nkb, cur = Lk - P, Lk // 128, P // 128
+    mask = random_block_mask(17, B, Hq, Lq // 128, nkb, P, dens)
+    kb0, kb1 = {"all": (0, nkb), "hist": (0, cur), "curr": (cur, nkb)}[cols]
+    q, k, v = (to_dev(x, dt) for x in (w.q, w.k, w.v))
+    o, lse = bsx_bsa_prefill(q, k, v, torch.from_numpy(mask).cuda(), P, kb0, kb1)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = O.bsa_prefill(w.q, w.k, w.v, mask, P, kb0, kb1)
+    o_g = o.float().cpu().numpy()
+    lse_g = lse.cpu().numpy()
+    assert np.abs(o_g - o_ref).max() <= O_TOL[dt]
+    fin = np.isfinite(lse_ref)
+    assert np.array_equal(np.isfinite(lse_g), fin)
+    if fin.any():
+        assert np.abs(lse_g[fin] - lse_ref[fin]).max() <= LSE_TOL
+    assert np.all(o_g[np.transpose(~fin, (0, 2, 1))] == 0.0)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+@pytest.mark.parametrize("d", [64, 128])
+def test_merge(dt, d):
+    rng = np.random.default_rng(d)
+    B, Lq, Hq = 2, 384, 4
+    o1 = rng.standard_normal((B, Lq, Hq, d)).astype(np.float32)
+    o2 = rng.standard_normal((B, Lq, Hq, d)).astype(np.float32)
+    if dt == "bf16":
+        o1 = to_dev(o1, dt).float().cpu().numpy()
+        o2 = to_dev(o2, dt).float().cpu().numpy()
+    l1 = (rng.standard_normal((B, Hq, Lq)) * 4).astype(np.float32)
+    l2 = (rng.standard_normal((B, Hq, Lq)) * 4).astype(np.float32)
+    l1[0, 0, :7] = -np.inf                   # one side empty
+    l2[1, 1, 5:9] = -np.inf
+    l1[1, 2, 0] = l2[1, 2, 0] = -np.inf      # both empty
+    O1, L1 = to_dev(o1, dt), torch.from_numpy(l1).cuda()
+    bsx_merge_attn(O1, L1, to_dev(o2, dt), torch.from_numpy(l2).cuda())
+    torch.cuda.synchronize()
+    o_ref, l_ref = O.merge_attn(o1, l1, o2, l2)
+    assert np.abs(O1.float().cpu().numpy() - o_ref).max() <= O_TOL[dt]
+    lg = L1.cpu().numpy()
+    fin = np.isfinite(l_ref)
+    assert np.array_equal(np.isfinite(lg), fin)
+    assert np.abs(lg[fin] - l_ref[fin]).max() <= 1e-5
+
+
+@pytest.mark.parametrize("cpu_tokens,force", [(1024, False), (1024, True), (4096, False), (128, True)])
+def test_map(cpu_tokens, force):
+    P, Lq = 8192, 512
+    mask = random_block_mask(3, 2, 4, Lq // 128, (P + Lq) // 128, P, 0.01)
+    keep = bsx_map_mask_to_cpu_blocks(torch.from_numpy(mask).cuda(), P, cpu_tokens, force)
+    torch.cuda.synchronize()
+    ref = O.map_mask_to_cpu_blocks(mask.astype(bool), P, cpu_tokens, force)
+    np.testing.assert_array_equal(keep.cpu().numpy(), ref)
+
+
+def test_chunk_step_small():
+    """Estimate -> BSA(history) -> BSA(current) -> merge -> map, small chunk."""
+    P, S, tau = 768, 8, 0.9
+    w = make_workload(seed=77, B=1, Hq=8, Hkv=2, d=128, Lk=P + 512, q_start_pos=P,
+                      alpha=3.0, n_hot=2, dtype="bf16")
+    est, o_ref, lse_ref, keep_ref = O.chunk_step(w.q, w.k, w.v, P, S, tau, 256)
+    q, k, v = (to_dev(x, "bf16") for x in (w.q, w.k, w.v))
+    # BSA runs on the oracle's mask so that near-threshold rows cannot differ
+    mask_g = bsx_xattn_estimate(q, k, P, S, tau)
+    check_mask(mask_g.cpu().numpy(), est, tau, P)
+    mask = torch.from_numpy(est.mask.astype(np.uint8)).cuda()
+    cur, nkb = P // 128, (P + 512) // 128
+    oh, lh = bsx_bsa_prefill(q, k, v, mask, P, 0, cur)
+    oc, lc = bsx_bsa_prefill(q, k, v, mask, P, cur, nkb)
+    bsx_merge_attn(oh, lh, oc, lc)
+    keep = bsx_map_mask_to_cpu_blocks(mask, P, 256)
+    torch.cuda.synchronize()
+    assert np.abs(oh.float().cpu().numpy() - o_ref).max() <= O_TOL["bf16"]
+    assert np.abs(lh.cpu().numpy() - lse_ref).max() <= LSE_TOL
+    np.testing.assert_array_equal(keep.cpu().numpy(), keep_ref)
