@@ -17,6 +17,7 @@ from ._lib import (  # noqa: F401
     bsx_merge_attn,
     bsx_version,
     bsx_xattn_estimate,
+    bsx_xattn_estimate_noalloc,
     load,
     shape_of,
 )

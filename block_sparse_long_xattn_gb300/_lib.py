@@ -24,7 +24,7 @@ STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported", -3: "CUDA error",
 
 EXPORTS = ("bsx_version", "bsx_status_string", "bsx_estimate_workspace_bytes",
            "bsx_xattn_estimate", "bsx_bsa_prefill", "bsx_merge_attn",
-           "bsx_map_mask_to_cpu_blocks", "bsx_last_error")
+           "bsx_map_mask_to_cpu_blocks", "bsx_last_error", "bsx_xattn_estimate_noalloc")
 
 
 class BsxShape(ctypes.Structure):
@@ -63,6 +63,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.bsx_xattn_estimate.restype = i32
         lib.bsx_xattn_estimate.argtypes = [BsxShape, vp, vp, i32, i32, i32, f32, vp, vp,
                                            vp, sz, vp]
+        lib.bsx_xattn_estimate_noalloc.restype = i32
+        lib.bsx_xattn_estimate_noalloc.argtypes = [BsxShape, vp, vp, i32, i32, i32, f32,
+                                                   vp, vp, vp]
         lib.bsx_bsa_prefill.restype = i32
         lib.bsx_bsa_prefill.argtypes = [BsxShape, vp, vp, vp, vp, i32, i32, i32, i32,
                                         vp, vp, vp]
@@ -139,6 +142,18 @@ def bsx_xattn_estimate(q, k, q_start_pos: int, stride: int, threshold: float, *,
     _check("bsx_xattn_estimate", lib.bsx_xattn_estimate(
         shape, _ptr(q), _ptr(k), q_len, q_start_pos, stride, float(threshold),
         _ptr(mask), _ptr(block_sums), _ptr(workspace), ws_bytes, _stream(stream)))
+    return mask
+
+
+def bsx_xattn_estimate_noalloc(q, k, q_start_pos: int, stride: int, threshold: float,
+                               *, mask, block_sums=None, stream=None):
+    """bsx_xattn_estimate using the library's own scratch (no workspace, no
+    allocation by the library or by this wrapper: `mask` must be provided)."""
+    lib = load()
+    _, q_len, _, _ = q.shape
+    _check("bsx_xattn_estimate_noalloc", lib.bsx_xattn_estimate_noalloc(
+        shape_of(q, k), _ptr(q), _ptr(k), q_len, q_start_pos, stride, float(threshold),
+        _ptr(mask), _ptr(block_sums), _stream(stream)))
     return mask
 
 

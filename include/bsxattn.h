@@ -117,6 +117,29 @@ int bsx_xattn_estimate(bsx_shape s, const void* q, const void* k, int q_len,
                        size_t workspace_bytes, void* stream);
 
 /*
+ * bsx_xattn_estimate without a caller-provided workspace.  The pages have no
+ * counterpart to this call; it exists for callers that may not allocate
+ * device memory (a host engine that owns all device memory through its own
+ * pool and forbids its plugins to call cudaMalloc, or a loop that may not
+ * call an allocator) and have no buffer to lend as scratch.
+ *
+ * Same arguments, outputs and results as bsx_xattn_estimate, minus
+ * `workspace`/`workspace_bytes`.  The scratch is a 32 MiB array the library
+ * reserves in global memory of every device that loads it, kept until the
+ * process exits.  A problem whose bsx_estimate_workspace_bytes() exceeds
+ * 32 MiB (33554432 bytes) returns BSX_ERR_WORKSPACE with nothing enqueued.
+ * The first call on a device looks up the array's device address (with that
+ * device current) and caches it; make that first call before any stream
+ * capture.  All calls share the array: calls whose work overlaps on the GPU
+ * (other streams, other host threads) race on it and must be serialised by
+ * the caller.  This call allocates nothing.
+ */
+int bsx_xattn_estimate_noalloc(bsx_shape s, const void* q, const void* k,
+                               int q_len, int q_start_pos, int stride,
+                               float threshold, uint8_t* mask,
+                               float* block_sums, void* stream);
+
+/*
  * Block-sparse causal attention (BSA) over key blocks [kb_begin, kb_end).
  *
  * Defined by docs/xattention_algorithm_guide.md "BSA (Block Sparse
