@@ -119,7 +119,14 @@ int bsx_bsa_prefill(bsx_shape s, const void* q, const void* k, const void* v,
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return BSX_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = bsx::launch_bsa_simt(p, q, k, v, mask, kb_begin, kb_end, o, lse, st);
+  cudaError_t e;
+  if (p.dtype == BSX_BF16) {
+    // tcgen05 path: one 128-row q-tile per CTA, up to kMaxKeyBlocks per row
+    if (kb_end - kb_begin > kMaxKeyBlocks) return BSX_ERR_UNSUPPORTED;
+    e = bsx::launch_bsa_tc(p, q, k, v, mask, kb_begin, kb_end, o, lse, err_word(), st);
+  } else {
+    e = bsx::launch_bsa_simt(p, q, k, v, mask, kb_begin, kb_end, o, lse, st);
+  }
   return cuda_status(e);
 }
 

@@ -1,0 +1,414 @@
+// a5 on tcgen05 tensor cores: block-sparse causal attention with LSE (bf16).
+//
+// docs/xattention_algorithm_guide.md "BSA (Block Sparse Attention)": causal
+// FlashAttention restricted to the selected 128x128 tiles of a per-head block
+// mask (block size fixed at 128); xattn_bsa.py compute_chunked_prefill takes O
+// and LSE from the history part and the current-chunk part and merges them.
+//
+// One CTA per (128-row q-tile, q-head, batch); 6 warps with fixed roles:
+//   warp 0      TMA producer: Q once, then K and V tiles of every selected key
+//               block (a 2-stage ring), by block index from the mask row.
+//   warp 1      tcgen05 issuer: S = Q K^T into one of two TMEM buffers, and
+//               O += P V into a TMEM accumulator.
+//   warps 2..5  softmax, one query row per thread (TMEM lane = row): read S,
+//               mask the diagonal block causally, online max with lazy
+//               rescaling of O (only when the running max grows by > 8 in
+//               log2 units), P = exp2(x - m) as bf16 into shared memory in the
+//               128-byte-swizzled K-major layout the MMA reads, row sums, and
+//               at the end O / l and LSE to global memory.
+// The S MMA of block j+1 runs while the softmax of block j runs; the P V MMA
+// of block j runs while the softmax of block j+1 computes exponentials.
+// Every wait is bounded (2 s of wall time); on expiry the CTA records the wait
+// in the device error word, drains its in-flight copies and MMAs, frees TMEM
+// and exits.
+#include "launchers.h"
+#include "tc_common.cuh"
+
+namespace bsx {
+namespace {
+
+using namespace tc;
+
+constexpr int kThreads = 192;
+constexpr int kStages = 2;
+constexpr int kRegion = 128 * 128;  // bytes of one 128-row x 64-feature bf16 tile
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+enum Site : unsigned {
+  kSiteKvEmpty = 1, kSiteQFull, kSiteKvFull, kSiteSFree, kSitePFull, kSiteSFull,
+  kSiteODone, kSiteODoneFinal
+};
+
+template <int D>
+struct Layout {
+  static constexpr int kRegions = D / 64;
+  static constexpr int kTile = kRegions * kRegion;        // Q, K or V tile bytes
+  static constexpr int kQ = 0;
+  static constexpr int kKV = kQ + kTile;                  // stage s: K at kKV + 2*s*kTile, V after it
+  static constexpr int kP = kKV + 2 * kStages * kTile;    // 128 x 128 bf16, two regions
+  static constexpr int kBars = kP + 2 * kRegion;          // mbarriers (8 B each)
+  static constexpr int kNumBars = 16;
+  static constexpr int kMisc = kBars + 8 * kNumBars;      // tmem slot, n, abort, scan scratch
+  static constexpr int kList = kMisc + 64 + 4 * kThreads; // uint16 block list
+  static constexpr int kMaxList = 8192;
+  static constexpr int kBytes = kList + 2 * kMaxList;
+  static constexpr uint32_t kTmemCols = 512;              // S0, S1, O (128 each; O uses D)
+};
+
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  // Wait for work this CTA already issued (copies or MMAs) even when another
+  // thread aborted; bounded so that a broken phase cannot hang the CTA.
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > 2000000000ull) return;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
+    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    const __grid_constant__ CUtensorMap tm_v, const uint8_t* __restrict__ mask, int q_len,
+    int Lk, int Hq, int Hkv, int cur, int kb_begin, int kb_end, float scale_log2,
+    __nv_bfloat16* __restrict__ o, float* __restrict__ lse, unsigned* err) {
+  using L = Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  int* n_sm = reinterpret_cast<int*>(smem + L::kMisc + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 8);
+  int* scan = reinterpret_cast<int*>(smem + L::kMisc + 64);
+  uint16_t* list = reinterpret_cast<uint16_t*>(smem + L::kList);
+
+  // barrier addresses
+  const uint32_t bar0 = smem_u32(bars);
+  const uint32_t q_full = bar0 + 0;
+  auto kv_full = [&](int s) { return bar0 + 8 * (1 + s); };
+  auto kv_empty = [&](int s) { return bar0 + 8 * (3 + s); };
+  auto s_full = [&](int s) { return bar0 + 8 * (5 + s); };
+  auto s_free = [&](int s) { return bar0 + 8 * (7 + s); };
+  const uint32_t p_full = bar0 + 8 * 9;
+  const uint32_t o_done = bar0 + 8 * 10;
+  const uint32_t mma_final = bar0 + 8 * 11;
+
+  const int qb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int nqb = gridDim.x;
+  const int nkb = Lk / kBlock;
+  const int hk = h / (Hq / Hkv);
+  const int diag = cur + qb;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(kv_full(s), 1);
+      mbar_init(kv_empty(s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(s_full(s), 1);
+      mbar_init(s_free(s), 128);
+    }
+    mbar_init(p_full, 128);
+    mbar_init(o_done, 1);
+    mbar_init(mma_final, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
+    tmem_relinquish();
+  }
+
+  // ---- compact the selected key blocks of this row into `list` ----
+  const uint8_t* mrow = mask + (((long long)b * Hq + h) * nqb + qb) * nkb;
+  const int kb_last = min(kb_end, diag + 1);
+  const int span = max(0, kb_last - kb_begin);
+  const int seg = (span + kThreads - 1) / kThreads;
+  const int beg = tid * seg;
+  int cnt = 0;
+  for (int e = 0; e < seg; ++e) {
+    const int i = beg + e;
+    if (i < span && mrow[kb_begin + i]) ++cnt;
+  }
+  scan[tid] = cnt;
+  __syncthreads();
+  if (tid == 0) {
+    int run = 0;
+    for (int t = 0; t < kThreads; ++t) {
+      const int c = scan[t];
+      scan[t] = run;
+      run += c;
+    }
+    *n_sm = min(run, L::kMaxList);
+  }
+  __syncthreads();
+  {
+    int pos = scan[tid];
+    for (int e = 0; e < seg; ++e) {
+      const int i = beg + e;
+      if (i < span && mrow[kb_begin + i] && pos < L::kMaxList) list[pos++] = (uint16_t)(kb_begin + i);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int n = *n_sm;
+  const uint32_t tmem_s0 = tmem, tmem_o = tmem + 256;
+
+  if (n == 0) {
+    // no visible key: O = 0, LSE = -inf
+    for (int e = tid; e < 128 * D / 8; e += kThreads) {
+      const int r = e / (D / 8), c = e % (D / 8);
+      reinterpret_cast<uint4*>(o + (((long long)b * q_len + qb * 128 + r) * Hq + h) * D)[c] =
+          make_uint4(0, 0, 0, 0);
+    }
+    for (int r = tid; r < 128; r += kThreads)
+      lse[((long long)b * Hq + h) * q_len + qb * 128 + r] = -INFINITY;
+  } else if (warp == 0) {
+    // ------------------------------ producer ------------------------------
+    if (lane == 0) {
+      tma_prefetch_map(&tm_q);
+      tma_prefetch_map(&tm_k);
+      tma_prefetch_map(&tm_v);
+      mbar_arrive_expect_tx(q_full, L::kTile);
+      for (int r = 0; r < L::kRegions; ++r)
+        tma_load_4d(sb + L::kQ + r * kRegion, &tm_q, q_full, r * 64, h, qb * 128, b);
+      int issued = 0;
+      for (int j = 0; j < n; ++j) {
+        const int s = j % kStages;
+        if (j >= kStages &&
+            !mbar_wait(kv_empty(s), ((j / kStages) - 1) & 1, abort_flag, err, kErrBsaTc,
+                       kSiteKvEmpty))
+          break;
+        const int kb = list[j];
+        const uint32_t kdst = sb + L::kKV + 2 * s * L::kTile;
+        const uint32_t vdst = kdst + L::kTile;
+        mbar_arrive_expect_tx(kv_full(s), 2 * L::kTile);
+        for (int r = 0; r < L::kRegions; ++r) {
+          tma_load_4d(kdst + r * kRegion, &tm_k, kv_full(s), r * 64, hk, kb * 128, b);
+          tma_load_4d(vdst + r * kRegion, &tm_v, kv_full(s), r * 64, hk, kb * 128, b);
+        }
+        issued = j + 1;
+      }
+      // copies still in flight must land before the CTA may exit
+      drain_wait(q_full, 0);
+      for (int s = 0; s < kStages && s < issued; ++s)
+        drain_wait(kv_full(s), ((issued - 1 - s) / kStages) & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer ----------------------------
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0, 0);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);
+      bool ok = mbar_wait(q_full, 0, abort_flag, err, kErrBsaTc, kSiteQFull);
+      auto issue_pv = [&](int i) -> bool {
+        if (!mbar_wait(p_full, i & 1, abort_flag, err, kErrBsaTc, kSitePFull)) return false;
+        tc_fence_after();
+        const int s = i % kStages;
+        const uint32_t vbase = sb + L::kKV + 2 * s * L::kTile + L::kTile;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {  // 16 keys per MMA
+          const uint64_t a = smem_desc_sw128(sb + L::kP + (k >> 2) * kRegion + (k & 3) * 32, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(vbase + k * 2048, kRegion, 1024);
+          mma_bf16(tmem_o, a, bd, idesc_pv, (i > 0 || k > 0) ? 1u : 0u);
+        }
+        mma_commit(o_done);
+        mma_commit(kv_empty(s));
+        return true;
+      };
+      int j = 0;
+      for (; ok && j < n; ++j) {
+        const int s = j % kStages;
+        const int buf = j & 1;
+        if (!mbar_wait(kv_full(s), (j / kStages) & 1, abort_flag, err, kErrBsaTc, kSiteKvFull)) {
+          ok = false;
+          break;
+        }
+        if (j >= 2 &&
+            !mbar_wait(s_free(buf), ((j >> 1) - 1) & 1, abort_flag, err, kErrBsaTc, kSiteSFree)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t kbase = sb + L::kKV + 2 * s * L::kTile;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {  // 16 features per MMA
+          const uint32_t off = (k >> 2) * kRegion + (k & 3) * 32;
+          const uint64_t a = smem_desc_sw128(sb + L::kQ + off, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(kbase + off, 16, 1024);
+          mma_bf16(tmem_s0 + buf * 128, a, bd, idesc_qk, k > 0 ? 1u : 0u);
+        }
+        mma_commit(s_full(buf));
+        if (j >= 1 && !issue_pv(j - 1)) {
+          ok = false;
+          break;
+        }
+      }
+      if (ok) issue_pv(n - 1);
+      // every MMA issued above completes before TMEM is released
+      mma_commit(mma_final);
+      drain_wait(mma_final, 0);
+    }
+  } else {
+    // ------------------------------ softmax -------------------------------
+    const int quad = warp & 3;           // TMEM lane quadrant this warp may access
+    const int row = quad * 32 + lane;    // query row within the tile
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      const int buf = j & 1;
+      if (!mbar_wait(s_full(buf), (j >> 1) & 1, abort_flag, err, kErrBsaTc, kSiteSFull)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float x[128];
+      tmem_ld128(tmem_s0 + lane_base + buf * 128, x);
+      tc_fence_before();
+      mbar_arrive(s_free(buf));
+      const bool is_diag = list[j] == diag;
+      float mt = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        float v = x[c] * scale_log2;
+        if (is_diag && c > row) v = -INFINITY;
+        x[c] = v;
+        mt = fmaxf(mt, v);
+      }
+      const bool need = mt > m_run + kRescaleThreshold;
+      float alpha = 1.f;
+      if (need) {
+        alpha = fast_exp2(m_run - mt);  // 0 on the first block
+        m_run = mt;
+      }
+      l_run *= alpha;
+      if (j > 0) {
+        if (!mbar_wait(o_done, (j - 1) & 1, abort_flag, err, kErrBsaTc, kSiteODone)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            float t[32];
+            tmem_ld32(tmem_o + lane_base + cc * 32, t);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) t[e] *= alpha;
+            tmem_st32(tmem_o + lane_base + cc * 32, t);
+          }
+        }
+      }
+      // P = exp2(x - m) as bf16, 128-byte swizzled K-major rows
+      float rs = 0.f;
+      uint8_t* prow = smem + L::kP + row * 128;
+#pragma unroll
+      for (int c = 0; c < 128; c += 8) {
+        float p[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          p[e] = fast_exp2(x[c + e] - m_run);
+          rs += p[e];
+        }
+        uint4 pk;
+        __nv_bfloat162 t0 = __floats2bfloat162_rn(p[0], p[1]);
+        __nv_bfloat162 t1 = __floats2bfloat162_rn(p[2], p[3]);
+        __nv_bfloat162 t2 = __floats2bfloat162_rn(p[4], p[5]);
+        __nv_bfloat162 t3 = __floats2bfloat162_rn(p[6], p[7]);
+        pk.x = *reinterpret_cast<uint32_t*>(&t0);
+        pk.y = *reinterpret_cast<uint32_t*>(&t1);
+        pk.z = *reinterpret_cast<uint32_t*>(&t2);
+        pk.w = *reinterpret_cast<uint32_t*>(&t3);
+        const int region = c >> 6, chunk = (c & 63) >> 3;
+        *reinterpret_cast<uint4*>(prow + region * kRegion + ((chunk ^ (row & 7)) << 4)) = pk;
+      }
+      l_run += rs;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    if (ok && mbar_wait(o_done, (n - 1) & 1, abort_flag, err, kErrBsaTc, kSiteODoneFinal)) {
+      tc_fence_after();
+      const float inv = 1.f / l_run;
+      __nv_bfloat16* orow = o + (((long long)b * q_len + qb * 128 + row) * Hq + h) * D;
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        float t[32];
+        tmem_ld32(tmem_o + lane_base + cc * 32, t);
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          uint4 pk;
+          __nv_bfloat162 t0 = __floats2bfloat162_rn(t[e + 0] * inv, t[e + 1] * inv);
+          __nv_bfloat162 t1 = __floats2bfloat162_rn(t[e + 2] * inv, t[e + 3] * inv);
+          __nv_bfloat162 t2 = __floats2bfloat162_rn(t[e + 4] * inv, t[e + 5] * inv);
+          __nv_bfloat162 t3 = __floats2bfloat162_rn(t[e + 6] * inv, t[e + 7] * inv);
+          pk.x = *reinterpret_cast<uint32_t*>(&t0);
+          pk.y = *reinterpret_cast<uint32_t*>(&t1);
+          pk.z = *reinterpret_cast<uint32_t*>(&t2);
+          pk.w = *reinterpret_cast<uint32_t*>(&t3);
+          reinterpret_cast<uint4*>(orow + cc * 32 + e)[0] = pk;
+        }
+      }
+      lse[((long long)b * Hq + h) * q_len + qb * 128 + row] =
+          (m_run + __log2f(l_run)) * 0.69314718055994531f;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_d(const Problem& p, const void* q, const void* k, const void* v,
+                     const uint8_t* mask, int kb_begin, int kb_end, void* o, float* lse,
+                     unsigned* err, cudaStream_t st) {
+  using L = Layout<D>;
+  CUtensorMap mq, mk, mv;
+  const uint32_t box[4] = {64, 1, 128, 1};
+  {
+    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)p.Hq, (uint64_t)p.q_len, (uint64_t)p.B};
+    const uint64_t strides[3] = {(uint64_t)D * 2, (uint64_t)p.Hq * D * 2,
+                                 (uint64_t)p.q_len * p.Hq * D * 2};
+    if (!encode_tmap_bf16(&mq, q, 4, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)p.Hkv, (uint64_t)p.Lk, (uint64_t)p.B};
+    const uint64_t strides[3] = {(uint64_t)D * 2, (uint64_t)p.Hkv * D * 2,
+                                 (uint64_t)p.Lk * p.Hkv * D * 2};
+    if (!encode_tmap_bf16(&mk, k, 4, dims, strides, box)) return cudaErrorInvalidValue;
+    if (!encode_tmap_bf16(&mv, v, 4, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  const size_t smem = L::kBytes + 1024;
+  cudaError_t e = cudaFuncSetAttribute(bsa_tc_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
+  dim3 grid(p.nqb, p.Hq, p.B);
+  bsa_tc_kernel<D><<<grid, kThreads, smem, st>>>(
+      mq, mk, mv, mask, p.q_len, p.Lk, p.Hq, p.Hkv, p.q_start_pos / kBlock, kb_begin, kb_end,
+      scale_log2, static_cast<__nv_bfloat16*>(o), lse, err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bsa_tc(const Problem& p, const void* q, const void* k, const void* v,
+                          const uint8_t* mask, int kb_begin, int kb_end, void* o, float* lse,
+                          unsigned* err, cudaStream_t st) {
+  if (p.dtype != 1) return cudaErrorInvalidValue;
+  if (p.d == 64) return launch_d<64>(p, q, k, v, mask, kb_begin, kb_end, o, lse, err, st);
+  if (p.d == 128) return launch_d<128>(p, q, k, v, mask, kb_begin, kb_end, o, lse, err, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace bsx

@@ -5,6 +5,8 @@ Sizes here let the oracle finish in seconds while still spanning several
 supported stride, fp32 and bf16, q_start_pos = 0 and > 0, and the degenerate
 cases (empty key range, a chunk of one block, threshold 1).
 """
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -70,6 +72,8 @@ BSA_CASES = [
     (2, 4, 1, 64, 768, 256, "bf16", 0.3),
     (1, 8, 2, 128, 1536, 1024, "f32", 0.6),
     (1, 4, 4, 128, 512, 384, "bf16", 1.0),
+    (1, 4, 1, 128, 8192, 7168, "bf16", 0.7),   # ~45 blocks per row: many pipeline phases
+    (1, 2, 1, 64, 4096, 2048, "bf16", 0.9),
 ]
 
 
@@ -152,3 +156,28 @@ def test_chunk_step_small():
     assert np.abs(oh.float().cpu().numpy() - o_ref).max() <= O_TOL["bf16"]
     assert np.abs(lh.cpu().numpy() - lse_ref).max() <= LSE_TOL
     np.testing.assert_array_equal(keep.cpu().numpy(), keep_ref)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_bsa_running_max_grows_every_block(d):
+    """Scores rise by ~8 (natural log) from each key block to the next, so the
+    online softmax must rescale its accumulator at almost every block."""
+    rng = np.random.default_rng(d)
+    P, Lq, Hq = 1024, 256, 2
+    Lk = P + Lq
+    u = rng.standard_normal(d)
+    u /= np.linalg.norm(u)
+    q = (0.3 * rng.standard_normal((1, Lq, Hq, d)) + 4.0 * u).astype(np.float32)
+    k = 0.3 * rng.standard_normal((1, Lk, 1, d))
+    for kb in range(Lk // 128):
+        k[0, kb * 128:(kb + 1) * 128, 0, :] += (2.0 * kb * math.sqrt(d)) * u  # logit +8 per block
+    k = k.astype(np.float32)
+    v = rng.standard_normal((1, Lk, 1, d)).astype(np.float32)
+    qb_, kb_, vb_ = (to_dev(x, "bf16") for x in (q, k, v))
+    q32, k32, v32 = (x.float().cpu().numpy() for x in (qb_, kb_, vb_))
+    mask = np.ones((1, Hq, Lq // 128, Lk // 128), np.uint8)
+    o, lse = bsx_bsa_prefill(qb_, kb_, vb_, torch.from_numpy(mask).cuda(), P)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = O.bsa_prefill(q32, k32, v32, mask, P, 0, Lk // 128)
+    assert np.abs(o.float().cpu().numpy() - o_ref).max() <= O_TOL["bf16"]
+    assert np.abs(lse.cpu().numpy() - lse_ref).max() <= LSE_TOL * max(1.0, np.abs(lse_ref).max() / 100)
