@@ -102,7 +102,9 @@ int bsx_xattn_estimate(bsx_shape s, const void* q, const void* k, int q_len,
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return BSX_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float* lse_part = static_cast<float*>(workspace);
-  cudaError_t e = bsx::launch_estimate_simt(p, q, k, stride, lse_part, st);
+  cudaError_t e = p.dtype == BSX_BF16
+                      ? bsx::launch_estimate_tc(p, q, k, stride, lse_part, err_word(), st)
+                      : bsx::launch_estimate_simt(p, q, k, stride, lse_part, st);
   if (e != cudaSuccess) return cuda_status(e);
   e = bsx::launch_select(p, stride, threshold, lse_part, mask, block_sums, st);
   return cuda_status(e);

@@ -55,15 +55,6 @@ struct Layout {
   static constexpr uint32_t kTmemCols = 512;              // S0, S1, O (128 each; O uses D)
 };
 
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
-  // Wait for work this CTA already issued (copies or MMAs) even when another
-  // thread aborted; bounded so that a broken phase cannot hang the CTA.
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > 2000000000ull) return;
-  }
-}
-
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,

@@ -1,0 +1,309 @@
+// a1-a2 partial on tcgen05 tensor cores (bf16): per-(row, key block)
+// log-sum-exp of the scaled antidiagonal scores.
+//
+// docs/xattention_algorithm_guide.md "Stride Reshape 详解" and "Triton Kernels
+// 详解" (flat_group_gemm_fuse_reshape): the scores are Q_r K_r^T with
+//   Q_r[i] = [q[i*S+S-1], q[i*S+S-2], ..., q[i*S]],  K_r[j] = [k[j*S], ..., k[j*S+S-1]],
+// a GEMM with reduction length S*d.  Here the reshape is never materialised:
+// the reduction runs over S*d/64 chunks (phase t, 64 features), and for each
+// chunk a 5-D TMA view of Q (features, head, phase, reshaped row, batch)
+// fetches the rows q[i*S + S-1-t] and one of K fetches k[j*S + t], both
+// already in the 128-byte-swizzled K-major layout the MMA reads.
+//
+// Tile = 128 reshaped query rows x 256 reshaped keys, accumulated in TMEM
+// (two accumulators, so the epilogue of one tile overlaps the MMAs of the
+// next).  Epilogue, one row per thread: scale by log2(e)/(sqrt(d) S), apply
+// the causal rule J <= I (global reshaped indices, the chunk starting at row
+// q_start_pos/S; xattn_bsa.py select_blocks Step 0), and for every key block
+// (128/S consecutive keys) at or before the row's diagonal write
+//   lse_part[b][h][kb][i] = ln sum_{J in kb, J <= I} exp(s[I,J] / (sqrt(d) S)).
+// The selection kernel turns these into the softmax block sums.
+//
+// Persistent: one CTA per SM walks the tiles (b, h, row tile, key tile) in
+// order, so neighbouring CTAs share Q rows and K tiles through L2.
+// Warp 0: TMA producer (4-stage ring); warp 1: MMA issuer; warps 2..5:
+// epilogue.  Every wait is bounded and records the device error word.
+#include "launchers.h"
+#include "tc_common.cuh"
+
+namespace bsx {
+namespace {
+
+using namespace tc;
+
+constexpr int kThreads = 192;
+constexpr int kStages = 4;
+constexpr int kM = 128;                  // reshaped query rows per tile
+constexpr int kN = 256;                  // reshaped keys per tile
+constexpr int kABytes = kM * 128;        // 128 rows x 64 bf16 features
+constexpr int kBBytes = kN * 128;        // 256 rows x 64 bf16 features
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kBarOff = kStages * kStageBytes;
+constexpr int kMiscOff = kBarOff + 8 * 16;
+constexpr int kSmemBytes = kMiscOff + 64;
+constexpr uint32_t kTmemCols = 512;      // two 128 x 256 fp32 accumulators
+
+enum Site : unsigned { kSiteEmpty = 1, kSiteFull, kSiteAccEmpty, kSiteAccFull };
+
+struct Tiles {
+  int Hq, R, p_s, n_rt, per_bh, total;
+};
+
+// Key tiles needed by row tile rt: every 256-key tile holding a key J <= the
+// largest reshaped row of the tile.
+__device__ __host__ __forceinline__ int key_tiles(const Tiles& T, int rt) {
+  const int i_max = min(rt * kM + kM - 1, T.R - 1);
+  return (T.p_s + i_max) / kN + 1;
+}
+
+__device__ __forceinline__ void tile_coords(const Tiles& T, int t, int& b, int& h, int& rt,
+                                            int& kt) {
+  const int bh = t / T.per_bh;
+  int rem = t - bh * T.per_bh;
+  b = bh / T.Hq;
+  h = bh - b * T.Hq;
+  rt = 0;
+  while (rt < T.n_rt - 1) {
+    const int n = key_tiles(T, rt);
+    if (rem < n) break;
+    rem -= n;
+    ++rt;
+  }
+  kt = rem;
+}
+
+template <int S, int D>
+__global__ void __launch_bounds__(kThreads, 1) estimate_tc_kernel(
+    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    Tiles T, int Hkv, int nkb, float scale_log2, float* __restrict__ lse_part, unsigned* err) {
+  constexpr int RB = kBlock / S;          // reshaped keys (and rows) per 128-token block
+  constexpr int FCH = D / 64;             // 64-feature chunks per token
+  constexpr int NCH = S * FCH;            // reduction chunks per tile
+  constexpr int GPC = 32 / RB;            // key blocks per 32-column TMEM load
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(smem);
+  const uint32_t bar0 = sb + kBarOff;
+  auto full = [&](int s) { return bar0 + 8 * s; };
+  auto empty = [&](int s) { return bar0 + 8 * (kStages + s); };
+  auto acc_full = [&](int s) { return bar0 + 8 * (2 * kStages + s); };
+  auto acc_empty = [&](int s) { return bar0 + 8 * (2 * kStages + 2 + s); };
+  const uint32_t mma_final = bar0 + 8 * (2 * kStages + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 8);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = T.Hq / Hkv;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(acc_full(s), 1);
+      mbar_init(acc_empty(s), 128);
+    }
+    mbar_init(mma_final, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------ producer ------------------------------
+    if (lane == 0) {
+      tma_prefetch_map(&tm_q);
+      tma_prefetch_map(&tm_k);
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < T.total; t += gridDim.x) {
+        int b, h, rt, kt;
+        tile_coords(T, t, b, h, rt, kt);
+        const int hk = h / G;
+        for (int ch = 0; ch < NCH; ++ch, ++it) {
+          const int s = it % kStages;
+          if (it >= kStages &&
+              !mbar_wait(empty(s), ((it / kStages) - 1) & 1, abort_flag, err, kErrEstimateTc,
+                         kSiteEmpty)) {
+            ok = false;
+            break;
+          }
+          const int phase = ch / FCH, c0 = (ch % FCH) * 64;
+          const uint32_t a_dst = sb + s * kStageBytes;
+          mbar_arrive_expect_tx(full(s), kStageBytes);
+          tma_load_5d(a_dst, &tm_q, full(s), c0, h, S - 1 - phase, rt * kM, b);
+          tma_load_5d(a_dst + kABytes, &tm_k, full(s), c0, hk, phase, kt * kN, b);
+        }
+      }
+      for (int s = 0; s < kStages && s < it; ++s)
+        drain_wait(full(s), ((it - 1 - s) / kStages) & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer ----------------------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kM, kN, 0, 0);
+      int it = 0, ti = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < T.total; t += gridDim.x, ++ti) {
+        const int buf = ti & 1;
+        if (ti >= 2 && !mbar_wait(acc_empty(buf), ((ti >> 1) - 1) & 1, abort_flag, err,
+                                  kErrEstimateTc, kSiteAccEmpty)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t acc = tmem + buf * kN;
+        for (int ch = 0; ch < NCH; ++ch, ++it) {
+          const int s = it % kStages;
+          if (!mbar_wait(full(s), (it / kStages) & 1, abort_flag, err, kErrEstimateTc,
+                         kSiteFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = sb + s * kStageBytes;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {  // 16 features per MMA, 32 bytes along the row
+            const uint64_t a = smem_desc_sw128(a_base + k * 32, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(a_base + kABytes + k * 32, 16, 1024);
+            mma_bf16(acc, a, bd, idesc, (ch > 0 || k > 0) ? 1u : 0u);
+          }
+          mma_commit(empty(s));
+        }
+        if (ok) mma_commit(acc_full(buf));
+      }
+      mma_commit(mma_final);
+      drain_wait(mma_final, 0);
+    }
+  } else {
+    // ------------------------------ epilogue ------------------------------
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    int ti = 0;
+    for (int t = blockIdx.x; t < T.total; t += gridDim.x, ++ti) {
+      const int buf = ti & 1;
+      if (!mbar_wait(acc_full(buf), (ti >> 1) & 1, abort_flag, err, kErrEstimateTc,
+                     kSiteAccFull))
+        break;
+      tc_fence_after();
+      int b, h, rt, kt;
+      tile_coords(T, t, b, h, rt, kt);
+      const int i = rt * kM + row;              // reshaped row within the chunk
+      const int Ig = T.p_s + i;                 // global reshaped row
+      const bool valid = i < T.R;
+      float* out = lse_part + ((long long)(b * T.Hq + h) * nkb) * T.R + i;
+#pragma unroll 1
+      for (int cc = 0; cc < kN / 32; ++cc) {
+        float v[32];
+        tmem_ld32(tmem + lane_base + buf * kN + cc * 32, v);
+        const int J0 = kt * kN + cc * 32;
+#pragma unroll
+        for (int g = 0; g < GPC; ++g) {
+          const int Jg = J0 + g * RB;
+          if (valid && Jg <= Ig) {
+            float m = -INFINITY;
+#pragma unroll
+            for (int e = 0; e < RB; ++e) {
+              const float x = (Jg + e <= Ig) ? v[g * RB + e] * scale_log2 : -INFINITY;
+              v[g * RB + e] = x;
+              m = fmaxf(m, x);
+            }
+            float sum = 0.f;
+#pragma unroll
+            for (int e = 0; e < RB; ++e) sum += fast_exp2(v[g * RB + e] - m);
+            out[(long long)(Jg / RB) * T.R] = (m + __log2f(sum)) * 0.69314718055994531f;
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(acc_empty(buf));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int S, int D>
+cudaError_t launch_sd(const Problem& p, const void* q, const void* k, float* lse_part,
+                      unsigned* err, cudaStream_t st) {
+  const int R = p.q_len / S, Ck = p.Lk / S;
+  CUtensorMap mq, mk;
+  {
+    const uint64_t dims[5] = {(uint64_t)D, (uint64_t)p.Hq, (uint64_t)S, (uint64_t)R,
+                              (uint64_t)p.B};
+    const uint64_t strides[4] = {(uint64_t)D * 2, (uint64_t)p.Hq * D * 2,
+                                 (uint64_t)S * p.Hq * D * 2, (uint64_t)p.q_len * p.Hq * D * 2};
+    const uint32_t box[5] = {64, 1, 1, (uint32_t)kM, 1};
+    if (!encode_tmap_bf16(&mq, q, 5, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[5] = {(uint64_t)D, (uint64_t)p.Hkv, (uint64_t)S, (uint64_t)Ck,
+                              (uint64_t)p.B};
+    const uint64_t strides[4] = {(uint64_t)D * 2, (uint64_t)p.Hkv * D * 2,
+                                 (uint64_t)S * p.Hkv * D * 2, (uint64_t)p.Lk * p.Hkv * D * 2};
+    const uint32_t box[5] = {64, 1, 1, (uint32_t)kN, 1};
+    if (!encode_tmap_bf16(&mk, k, 5, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  Tiles T;
+  T.Hq = p.Hq;
+  T.R = R;
+  T.p_s = p.q_start_pos / S;
+  T.n_rt = (R + kM - 1) / kM;
+  T.per_bh = 0;
+  for (int rt = 0; rt < T.n_rt; ++rt) T.per_bh += key_tiles(T, rt);
+  T.total = p.B * p.Hq * T.per_bh;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const size_t smem = kSmemBytes + 1024;
+  e = cudaFuncSetAttribute(estimate_tc_kernel<S, D>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const float scale_log2 = 1.4426950408889634f / (sqrtf((float)D) * (float)S);
+  const int grid = T.total < sms ? T.total : sms;
+  estimate_tc_kernel<S, D><<<grid, kThreads, smem, st>>>(mq, mk, T, p.Hkv, p.nkb, scale_log2,
+                                                         lse_part, err);
+  return cudaGetLastError();
+}
+
+template <int S>
+cudaError_t launch_s(const Problem& p, const void* q, const void* k, float* lse_part,
+                     unsigned* err, cudaStream_t st) {
+  if (p.d == 64) return launch_sd<S, 64>(p, q, k, lse_part, err, st);
+  if (p.d == 128) return launch_sd<S, 128>(p, q, k, lse_part, err, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_estimate_tc(const Problem& p, const void* q, const void* k, int stride,
+                               float* lse_part, unsigned* err, cudaStream_t st) {
+  if (p.dtype != 1) return cudaErrorInvalidValue;
+  switch (stride) {
+    case 4: return launch_s<4>(p, q, k, lse_part, err, st);
+    case 8: return launch_s<8>(p, q, k, lse_part, err, st);
+    case 16: return launch_s<16>(p, q, k, lse_part, err, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace bsx
