@@ -6,8 +6,11 @@
 // and LSE from the history part and the current-chunk part and merges them.
 //
 // One CTA per (128-row q-tile, q-head, batch); 6 warps with fixed roles:
-//   warp 0      TMA producer: Q once, then K and V tiles of every selected key
-//               block (a 2-stage ring), by block index from the mask row.
+//   warp 0      TMA producer: Q once, then the K and V tiles of every selected
+//               key block, found by scanning the mask row, into a ring of
+//               tile-sized slots (K_0, V_0, K_1, V_1, ...).  A K slot is freed
+//               as soon as its S MMA completes and a V slot after its P V MMA,
+//               so loads run about two blocks ahead of the MMAs.
 //   warp 1      tcgen05 issuer: S = Q K^T into one of two TMEM buffers, and
 //               O += P V into a TMEM accumulator.
 //   warps 2..5  softmax, one query row per thread (TMEM lane = row): read S,
@@ -30,7 +33,6 @@ namespace {
 using namespace tc;
 
 constexpr int kThreads = 192;
-constexpr int kStages = 2;
 constexpr int kRegion = 128 * 128;  // bytes of one 128-row x 64-feature bf16 tile
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -43,15 +45,14 @@ template <int D>
 struct Layout {
   static constexpr int kRegions = D / 64;
   static constexpr int kTile = kRegions * kRegion;        // Q, K or V tile bytes
+  static constexpr int kSlots = D == 128 ? 5 : 8;         // K/V ring slots of kTile bytes
   static constexpr int kQ = 0;
-  static constexpr int kKV = kQ + kTile;                  // stage s: K at kKV + 2*s*kTile, V after it
-  static constexpr int kP = kKV + 2 * kStages * kTile;    // 128 x 128 bf16, two regions
-  static constexpr int kBars = kP + 2 * kRegion;          // mbarriers (8 B each)
-  static constexpr int kNumBars = 16;
-  static constexpr int kMisc = kBars + 8 * kNumBars;      // tmem slot, n, abort, scan scratch
-  static constexpr int kList = kMisc + 64 + 4 * kThreads; // uint16 block list
-  static constexpr int kMaxList = 8192;
-  static constexpr int kBytes = kList + 2 * kMaxList;
+  static constexpr int kP = kQ + kTile;                   // 128 x 128 bf16, two regions
+  static constexpr int kRing = kP + 2 * kRegion;
+  static constexpr int kBars = kRing + kSlots * kTile;    // mbarriers (8 B each)
+  static constexpr int kNumBars = 32;
+  static constexpr int kMisc = kBars + 8 * kNumBars;      // tmem slot, n, flags
+  static constexpr int kBytes = kMisc + 64;
   static constexpr uint32_t kTmemCols = 512;              // S0, S1, O (128 each; O uses D)
 };
 
@@ -70,19 +71,18 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   int* n_sm = reinterpret_cast<int*>(smem + L::kMisc + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 8);
-  int* scan = reinterpret_cast<int*>(smem + L::kMisc + 64);
-  uint16_t* list = reinterpret_cast<uint16_t*>(smem + L::kList);
 
   // barrier addresses
   const uint32_t bar0 = smem_u32(bars);
   const uint32_t q_full = bar0 + 0;
-  auto kv_full = [&](int s) { return bar0 + 8 * (1 + s); };
-  auto kv_empty = [&](int s) { return bar0 + 8 * (3 + s); };
-  auto s_full = [&](int s) { return bar0 + 8 * (5 + s); };
-  auto s_free = [&](int s) { return bar0 + 8 * (7 + s); };
-  const uint32_t p_full = bar0 + 8 * 9;
-  const uint32_t o_done = bar0 + 8 * 10;
-  const uint32_t mma_final = bar0 + 8 * 11;
+  auto slot_full = [&](int s) { return bar0 + 8 * (1 + s); };
+  auto slot_empty = [&](int s) { return bar0 + 8 * (1 + L::kSlots + s); };
+  constexpr int kB2 = 1 + 2 * L::kSlots;
+  auto s_full = [&](int s) { return bar0 + 8 * (kB2 + s); };
+  auto s_free = [&](int s) { return bar0 + 8 * (kB2 + 2 + s); };
+  const uint32_t p_full = bar0 + 8 * (kB2 + 4);
+  const uint32_t o_done = bar0 + 8 * (kB2 + 5);
+  const uint32_t mma_final = bar0 + 8 * (kB2 + 6);
 
   const int qb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int nqb = gridDim.x;
@@ -93,9 +93,9 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
 
   if (tid == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(kv_full(s), 1);
-      mbar_init(kv_empty(s), 1);
+    for (int s = 0; s < L::kSlots; ++s) {
+      mbar_init(slot_full(s), 1);
+      mbar_init(slot_empty(s), 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(s_full(s), 1);
@@ -105,6 +105,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
     mbar_init(o_done, 1);
     mbar_init(mma_final, 1);
     *abort_flag = 0;
+    *n_sm = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
   }
@@ -113,41 +114,21 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
     tmem_relinquish();
   }
 
-  // ---- compact the selected key blocks of this row into `list` ----
+  // ---- count the selected key blocks of this row ----
   const uint8_t* mrow = mask + (((long long)b * Hq + h) * nqb + qb) * nkb;
   const int kb_last = min(kb_end, diag + 1);
-  const int span = max(0, kb_last - kb_begin);
-  const int seg = (span + kThreads - 1) / kThreads;
-  const int beg = tid * seg;
   int cnt = 0;
-  for (int e = 0; e < seg; ++e) {
-    const int i = beg + e;
-    if (i < span && mrow[kb_begin + i]) ++cnt;
-  }
-  scan[tid] = cnt;
-  __syncthreads();
-  if (tid == 0) {
-    int run = 0;
-    for (int t = 0; t < kThreads; ++t) {
-      const int c = scan[t];
-      scan[t] = run;
-      run += c;
-    }
-    *n_sm = min(run, L::kMaxList);
-  }
-  __syncthreads();
-  {
-    int pos = scan[tid];
-    for (int e = 0; e < seg; ++e) {
-      const int i = beg + e;
-      if (i < span && mrow[kb_begin + i] && pos < L::kMaxList) list[pos++] = (uint16_t)(kb_begin + i);
-    }
-  }
+  for (int kb = kb_begin + tid; kb < kb_last; kb += kThreads) cnt += mrow[kb] ? 1 : 0;
+  cnt = __reduce_add_sync(0xffffffffu, cnt);
+  __syncthreads();  // n_sm initialised
+  if (lane == 0 && cnt) atomicAdd(n_sm, cnt);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int n = *n_sm;
+  // the diagonal block, when selected, is the last block of the row
+  const bool diag_last = diag >= kb_begin && diag < kb_end && mrow[diag] != 0;
   const uint32_t tmem_s0 = tmem, tmem_o = tmem + 256;
 
   if (n == 0) {
@@ -168,27 +149,36 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
       mbar_arrive_expect_tx(q_full, L::kTile);
       for (int r = 0; r < L::kRegions; ++r)
         tma_load_4d(sb + L::kQ + r * kRegion, &tm_q, q_full, r * 64, h, qb * 128, b);
+      // ring items in order K_0, V_0, K_1, V_1, ...; item i in slot i % kSlots
       int issued = 0;
-      for (int j = 0; j < n; ++j) {
-        const int s = j % kStages;
-        if (j >= kStages &&
-            !mbar_wait(kv_empty(s), ((j / kStages) - 1) & 1, abort_flag, err, kErrBsaTc,
-                       kSiteKvEmpty))
-          break;
-        const int kb = list[j];
-        const uint32_t kdst = sb + L::kKV + 2 * s * L::kTile;
-        const uint32_t vdst = kdst + L::kTile;
-        mbar_arrive_expect_tx(kv_full(s), 2 * L::kTile);
-        for (int r = 0; r < L::kRegions; ++r) {
-          tma_load_4d(kdst + r * kRegion, &tm_k, kv_full(s), r * 64, hk, kb * 128, b);
-          tma_load_4d(vdst + r * kRegion, &tm_v, kv_full(s), r * 64, hk, kb * 128, b);
+      int kb = kb_begin - 1;
+      bool ok = true;
+      for (int j = 0; ok && j < n; ++j) {
+        do {
+          ++kb;
+        } while (kb < kb_last && !__ldg(mrow + kb));
+        if (kb >= kb_last) break;  // cannot happen: n counts these blocks
+        for (int kind = 0; kind < 2; ++kind) {
+          const int i = 2 * j + kind;
+          const int s = i % L::kSlots;
+          if (i >= L::kSlots &&
+              !mbar_wait(slot_empty(s), ((i / L::kSlots) - 1) & 1, abort_flag, err, kErrBsaTc,
+                         kSiteKvEmpty)) {
+            ok = false;
+            break;
+          }
+          const uint32_t dst = sb + L::kRing + s * L::kTile;
+          mbar_arrive_expect_tx(slot_full(s), L::kTile);
+          const CUtensorMap* map = kind == 0 ? &tm_k : &tm_v;
+          for (int r = 0; r < L::kRegions; ++r)
+            tma_load_4d(dst + r * kRegion, map, slot_full(s), r * 64, hk, kb * 128, b);
+          issued = i + 1;
         }
-        issued = j + 1;
       }
       // copies still in flight must land before the CTA may exit
       drain_wait(q_full, 0);
-      for (int s = 0; s < kStages && s < issued; ++s)
-        drain_wait(kv_full(s), ((issued - 1 - s) / kStages) & 1);
+      for (int s = 0; s < L::kSlots && s < issued; ++s)
+        drain_wait(slot_full(s), ((issued - 1 - s) / L::kSlots) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ----------------------------
@@ -197,10 +187,14 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);
       bool ok = mbar_wait(q_full, 0, abort_flag, err, kErrBsaTc, kSiteQFull);
       auto issue_pv = [&](int i) -> bool {
+        const int item = 2 * i + 1;  // V_i
+        const int s = item % L::kSlots;
         if (!mbar_wait(p_full, i & 1, abort_flag, err, kErrBsaTc, kSitePFull)) return false;
+        if (!mbar_wait(slot_full(s), (item / L::kSlots) & 1, abort_flag, err, kErrBsaTc,
+                       kSiteKvFull))
+          return false;
         tc_fence_after();
-        const int s = i % kStages;
-        const uint32_t vbase = sb + L::kKV + 2 * s * L::kTile + L::kTile;
+        const uint32_t vbase = sb + L::kRing + s * L::kTile;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {  // 16 keys per MMA
           const uint64_t a = smem_desc_sw128(sb + L::kP + (k >> 2) * kRegion + (k & 3) * 32, 16, 1024);
@@ -208,14 +202,16 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
           mma_bf16(tmem_o, a, bd, idesc_pv, (i > 0 || k > 0) ? 1u : 0u);
         }
         mma_commit(o_done);
-        mma_commit(kv_empty(s));
+        mma_commit(slot_empty(s));
         return true;
       };
       int j = 0;
       for (; ok && j < n; ++j) {
-        const int s = j % kStages;
+        const int item = 2 * j;  // K_j
+        const int s = item % L::kSlots;
         const int buf = j & 1;
-        if (!mbar_wait(kv_full(s), (j / kStages) & 1, abort_flag, err, kErrBsaTc, kSiteKvFull)) {
+        if (!mbar_wait(slot_full(s), (item / L::kSlots) & 1, abort_flag, err, kErrBsaTc,
+                       kSiteKvFull)) {
           ok = false;
           break;
         }
@@ -225,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
           break;
         }
         tc_fence_after();
-        const uint32_t kbase = sb + L::kKV + 2 * s * L::kTile;
+        const uint32_t kbase = sb + L::kRing + s * L::kTile;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {  // 16 features per MMA
           const uint32_t off = (k >> 2) * kRegion + (k & 3) * 32;
@@ -234,6 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
           mma_bf16(tmem_s0 + buf * 128, a, bd, idesc_qk, k > 0 ? 1u : 0u);
         }
         mma_commit(s_full(buf));
+        mma_commit(slot_empty(s));
         if (j >= 1 && !issue_pv(j - 1)) {
           ok = false;
           break;
@@ -262,23 +259,43 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
       tmem_ld128(tmem_s0 + lane_base + buf * 128, x);
       tc_fence_before();
       mbar_arrive(s_free(buf));
-      const bool is_diag = list[j] == diag;
-      float mt = -INFINITY;
+      const bool is_diag = diag_last && j == n - 1;
+      // row max with 8 independent accumulators (no 128-long dependent chain)
+      float mx[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) mx[e] = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 128; ++c) {
         float v = x[c] * scale_log2;
         if (is_diag && c > row) v = -INFINITY;
         x[c] = v;
-        mt = fmaxf(mt, v);
+        mx[c & 7] = fmaxf(mx[c & 7], v);
       }
+      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       const bool need = mt > m_run + kRescaleThreshold;
       float alpha = 1.f;
       if (need) {
         alpha = fast_exp2(m_run - mt);  // 0 on the first block
         m_run = mt;
       }
-      l_run *= alpha;
+      // P = exp2(x - m) packed to bf16 pairs while PV(j-1) still runs
+      uint32_t pk[64];
+      float ps[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ps[e] = 0.f;
+#pragma unroll
+      for (int c = 0; c < 128; c += 2) {
+        const float p0 = fast_exp2(x[c] - m_run);
+        const float p1 = fast_exp2(x[c + 1] - m_run);
+        ps[(c >> 1) & 7] += p0 + p1;
+        __nv_bfloat162 t = __floats2bfloat162_rn(p0, p1);
+        pk[c >> 1] = *reinterpret_cast<uint32_t*>(&t);
+      }
+      const float rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      l_run = l_run * alpha + rs;
       if (j > 0) {
+        // PV(j-1) must be done before O is rescaled or P is overwritten
         if (!mbar_wait(o_done, (j - 1) & 1, abort_flag, err, kErrBsaTc, kSiteODone)) {
           ok = false;
           break;
@@ -295,30 +312,14 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
           }
         }
       }
-      // P = exp2(x - m) as bf16, 128-byte swizzled K-major rows
-      float rs = 0.f;
+      // store P: 128-byte swizzled K-major rows, 16-byte chunks
       uint8_t* prow = smem + L::kP + row * 128;
 #pragma unroll
-      for (int c = 0; c < 128; c += 8) {
-        float p[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          p[e] = fast_exp2(x[c + e] - m_run);
-          rs += p[e];
-        }
-        uint4 pk;
-        __nv_bfloat162 t0 = __floats2bfloat162_rn(p[0], p[1]);
-        __nv_bfloat162 t1 = __floats2bfloat162_rn(p[2], p[3]);
-        __nv_bfloat162 t2 = __floats2bfloat162_rn(p[4], p[5]);
-        __nv_bfloat162 t3 = __floats2bfloat162_rn(p[6], p[7]);
-        pk.x = *reinterpret_cast<uint32_t*>(&t0);
-        pk.y = *reinterpret_cast<uint32_t*>(&t1);
-        pk.z = *reinterpret_cast<uint32_t*>(&t2);
-        pk.w = *reinterpret_cast<uint32_t*>(&t3);
-        const int region = c >> 6, chunk = (c & 63) >> 3;
-        *reinterpret_cast<uint4*>(prow + region * kRegion + ((chunk ^ (row & 7)) << 4)) = pk;
+      for (int c8 = 0; c8 < 16; ++c8) {
+        const int region = c8 >> 3, chunk = c8 & 7;
+        *reinterpret_cast<uint4*>(prow + region * kRegion + ((chunk ^ (row & 7)) << 4)) =
+            make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
       }
-      l_run += rs;
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(p_full);

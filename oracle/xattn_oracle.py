@@ -218,16 +218,13 @@ class EstimateResult:
     gap: np.ndarray        # float64 [B, Hq, nqb]
 
 
-def xattn_estimate(q: np.ndarray, k: np.ndarray, q_start_pos: int,
-                   stride: int, threshold: float) -> EstimateResult:
-    """Estimator + selection + causal post-mask for one chunk.
+def select_blocks(A: np.ndarray, q_start_pos: int, threshold: float) -> EstimateResult:
+    """find_blocks_chunked over every (b, h, qb) row of A, then the causal post-mask.
 
-    [policy] select_blocks Steps 0-4: block sums over all Lk keys, then
-    find_blocks_chunked with current_index = q_start_pos/128, then the causal
-    post-mask (future blocks inside the chunk cleared).  The sink block 0 and
-    the diagonal block current_index + qb are forced ([guide] "块选择算法").
+    [policy] select_blocks Step 4: current_index = q_start_pos/128; the sink
+    block 0 and the diagonal block current_index + qb are forced ([guide]
+    "块选择算法"); blocks above the diagonal of the current chunk are cleared.
     """
-    A = estimate_block_sums(q, k, q_start_pos, stride)
     B, Hq, nqb, nkb = A.shape
     cur = q_start_pos // BSA_BLOCK
     mask = np.zeros(A.shape, bool)
@@ -241,11 +238,21 @@ def xattn_estimate(q: np.ndarray, k: np.ndarray, q_start_pos: int,
                 mask[b, h, qb] = rs.selected
                 margin[b, h, qb] = rs.margin
                 gap[b, h, qb] = rs.gap
-    # causal post-mask: [policy] Step 4 clears blocks above the diagonal of the
-    # current chunk; select_row never selects kb > diag, restated here.
+    # causal post-mask (select_row never selects kb > diag; restated here)
     for qb in range(nqb):
         mask[:, :, qb, cur + qb + 1:] = False
     return EstimateResult(mask, A, margin, gap)
+
+
+def xattn_estimate(q: np.ndarray, k: np.ndarray, q_start_pos: int,
+                   stride: int, threshold: float) -> EstimateResult:
+    """Estimator + selection + causal post-mask for one chunk.
+
+    [policy] select_blocks Steps 0-4: block sums over all Lk keys, then
+    find_blocks_chunked and the causal post-mask.
+    """
+    return select_blocks(estimate_block_sums(q, k, q_start_pos, stride),
+                         q_start_pos, threshold)
 
 
 # --------------------------------------------------------------------------- #

@@ -1,0 +1,179 @@
+"""GPU parity at the full workload sizes, in the launch sequence bench.py times.
+
+For each workload the chunk step runs exactly as the benchmark runs it:
+estimate -> BSA on history blocks -> BSA on the current chunk -> merge ->
+CPU-block map.  The block mask is compared with the oracle's for every
+(b, h, q-block) row (the near-threshold rule in tests/helpers.py); the
+attention then runs on the oracle's mask, so that an ambiguous row cannot
+change which keys a query sees, and O / LSE are compared on sampled rows
+(first, second, middle and last rows of the first, a middle and the last
+q-block of several heads), which the oracle computes one by one.  The
+CPU-block map is compared bit-exactly.
+"""
+from types import SimpleNamespace
+
+import numpy as np
+import pytest
+import torch
+
+from block_sparse_long_xattn_gb300 import (
+    bsx_bsa_prefill, bsx_last_error, bsx_map_mask_to_cpu_blocks, bsx_merge_attn,
+    bsx_xattn_estimate)
+from block_sparse_long_xattn_gb300.inputs import CONFIGS, make_workload
+from oracle import xattn_oracle as O
+from tests.helpers import LSE_TOL, O_TOL, check_block_sums, check_mask, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _cfg(name):
+    c = dict(CONFIGS[name])
+    return c, c.pop("stride"), c.pop("threshold"), c.pop("chunk", None)
+
+
+def gpu_chunk_step(q, k, v, P, S, tau, mask_for_bsa=None, cpu_tokens=1024):
+    """The benchmark's step; returns (mask, block sums, o, lse, keep)."""
+    B, Lq, Hq, _ = q.shape
+    nkb, cur = k.shape[1] // 128, P // 128
+    A = torch.empty((B, Hq, Lq // 128, nkb), dtype=torch.float32, device=q.device)
+    mask = bsx_xattn_estimate(q, k, P, S, tau, block_sums=A)
+    m = mask if mask_for_bsa is None else mask_for_bsa
+    oh, lh = bsx_bsa_prefill(q, k, v, m, P, 0, cur)
+    oc, lc = bsx_bsa_prefill(q, k, v, m, P, cur, nkb)
+    bsx_merge_attn(oh, lh, oc, lc)
+    keep = bsx_map_mask_to_cpu_blocks(m, P, cpu_tokens) if P >= cpu_tokens else None
+    torch.cuda.synchronize()
+    return mask, A, oh, lh, keep
+
+
+def _density(mask, P):
+    """Selected causal blocks / causal blocks."""
+    B, Hq, nqb, _ = mask.shape
+    causal = sum(P // 128 + qb + 1 for qb in range(nqb)) * B * Hq
+    return float(np.asarray(mask, bool).sum()) / causal
+
+
+def _sample_rows(Lq):
+    nqb = Lq // 128
+    rows = []
+    for qb in sorted({0, nqb // 2, nqb - 1}):
+        rows += [qb * 128 + r for r in (0, 1, 64, 126, 127)]
+    return np.array(sorted(set(rows)))
+
+
+def _check_rows(w, mask_np, o, lse, P, heads):
+    o_g = o.float().cpu().numpy()
+    l_g = lse.cpu().numpy()
+    rows = _sample_rows(w.q.shape[1])
+    nkb = w.k.shape[1] // 128
+    worst_o = worst_l = 0.0
+    for b in range(w.q.shape[0]):
+        for h in heads:
+            o_r, l_r = O.bsa_rows(w.q, w.k, w.v, mask_np, P, 0, nkb, b, h, rows)
+            worst_o = max(worst_o, float(np.abs(o_g[b, rows, h, :] - o_r).max()))
+            worst_l = max(worst_l, float(np.abs(l_g[b, h, rows] - l_r).max()))
+    assert worst_o <= O_TOL[w.dtype], worst_o
+    assert worst_l <= LSE_TOL, worst_l
+    return worst_o, worst_l
+
+
+def _run_single_chunk(name, heads):
+    c, S, tau, _ = _cfg(name)
+    w = make_workload(seed=0, **c)
+    P = w.q_start_pos
+    q, k, v = (to_dev(x, w.dtype) for x in (w.q, w.k, w.v))
+    est = O.xattn_estimate(w.q, w.k, P, S, tau)
+    mask_ref = torch.from_numpy(est.mask.astype(np.uint8)).cuda()
+    mask, A, o, lse, keep = gpu_chunk_step(q, k, v, P, S, tau, mask_for_bsa=mask_ref)
+    A_g = A.cpu().numpy()
+    err = check_block_sums(A_g, est.block_sums, S)
+    n_rows, n_near, n_tie = check_mask(mask.cpu().numpy(), est, tau, P, A_g)
+    print(f"{name}: {n_rows} mask rows, {n_near} near the threshold, {n_tie} near-tie "
+          f"swaps; block-sum max error {err:.2e}; density {_density(est.mask, P):.4f}")
+    _check_rows(w, est.mask, o, lse, P, heads)
+    if keep is not None:
+        np.testing.assert_array_equal(keep.cpu().numpy(),
+                                      O.map_mask_to_cpu_blocks(est.mask, P, 1024))
+    assert bsx_last_error() == 0
+
+
+def test_tiny_1k_f32_full_parity():
+    """The tiny single-chunk workload: every output compared, all rows."""
+    c, S, tau, _ = _cfg("tiny-1k-f32")
+    w = make_workload(seed=0, **c)
+    q, k, v = (to_dev(x, w.dtype) for x in (w.q, w.k, w.v))
+    est, o_ref, lse_ref, _ = O.chunk_step(w.q, w.k, w.v, 0, S, tau)
+    mask_ref = torch.from_numpy(est.mask.astype(np.uint8)).cuda()
+    mask, A, o, lse, _ = gpu_chunk_step(q, k, v, 0, S, tau, mask_for_bsa=mask_ref)
+    check_block_sums(A.cpu().numpy(), est.block_sums, S)
+    check_mask(mask.cpu().numpy(), est, tau, 0, A.cpu().numpy())
+    assert np.abs(o.cpu().numpy() - o_ref).max() <= O_TOL["f32"]
+    assert np.abs(lse.cpu().numpy() - lse_ref).max() <= LSE_TOL
+
+
+def test_llama8b_32k_chunk4096():
+    _run_single_chunk("llama8b-32k-chunk4096", heads=[0, 13, 31])
+
+
+def test_llama8b_128k_chunk4096():
+    _run_single_chunk("llama8b-128k-chunk4096", heads=[0, 22, 31])
+
+
+def test_llama8b_64k_chunked_sequence():
+    """A 64K sequence in 16 chunks of 4096; chunks 0, 1, 8 and 15 are checked."""
+    c, S, tau, chunk = _cfg("llama8b-64k-chunked")
+    w = make_workload(seed=0, q_full=True, **c)
+    Lk_full = w.k.shape[1]
+    qf, kf, vf = (to_dev(x, w.dtype) for x in (w.q, w.k, w.v))
+    for ci in range(Lk_full // chunk):
+        P = ci * chunk
+        Lk = P + chunk
+        q, k, v = qf[:, P:Lk].contiguous(), kf[:, :Lk].contiguous(), vf[:, :Lk].contiguous()
+        if ci not in (0, 1, 8, 15):
+            gpu_chunk_step(q, k, v, P, S, tau)   # run in order, as a prefill would
+            continue
+        wq = w.q[:, P:Lk]
+        wk, wv = w.k[:, :Lk], w.v[:, :Lk]
+        est = O.xattn_estimate(wq, wk, P, S, tau)
+        mask_ref = torch.from_numpy(est.mask.astype(np.uint8)).cuda()
+        mask, A, o, lse, keep = gpu_chunk_step(q, k, v, P, S, tau, mask_for_bsa=mask_ref)
+        check_block_sums(A.cpu().numpy(), est.block_sums, S)
+        _, n_near, n_tie = check_mask(mask.cpu().numpy(), est, tau, P, A.cpu().numpy())
+        print(f"64k chunk {ci}: {n_near} near-threshold rows, {n_tie} near-tie swaps, "
+              f"density {_density(est.mask, P):.4f}")
+
+        ch = SimpleNamespace(q=wq, k=wk, v=wv, dtype=w.dtype)
+        _check_rows(ch, est.mask, o, lse, P, heads=[0, 31])
+        if keep is not None:
+            np.testing.assert_array_equal(keep.cpu().numpy(),
+                                          O.map_mask_to_cpu_blocks(est.mask, P, 1024))
+    assert bsx_last_error() == 0
+
+
+@pytest.mark.parametrize("alpha", [0.0, 2.0, 4.0])
+def test_density_sweep_32k(alpha):
+    """Thresholds 0.8 .. 1.0 on the 32K / 4096-chunk shapes; threshold 1 must
+    select every causal block and then equal dense causal attention."""
+    c, S, _, _ = _cfg("llama8b-32k-chunk4096")
+    c["alpha"] = alpha
+    c["n_hot"] = 16 if alpha > 0 else 0
+    w = make_workload(seed=1, **c)
+    P = w.q_start_pos
+    q, k, v = (to_dev(x, w.dtype) for x in (w.q, w.k, w.v))
+    A_ref = O.estimate_block_sums(w.q, w.k, P, S)
+    for tau in (0.8, 0.9, 0.95, 0.99, 1.0):
+        est = O.select_blocks(A_ref, P, tau)
+        mask_ref = torch.from_numpy(est.mask.astype(np.uint8)).cuda()
+        mask, A, o, lse, _ = gpu_chunk_step(q, k, v, P, S, tau, mask_for_bsa=mask_ref)
+        A_g = A.cpu().numpy()
+        if tau == 0.8:
+            check_block_sums(A_g, A_ref, S)
+        n_rows, n_near, n_tie = check_mask(mask.cpu().numpy(), est, tau, P, A_g)
+        print(f"alpha {alpha} tau {tau}: density {_density(est.mask, P):.4f}, "
+              f"{n_near}/{n_rows} near-threshold rows, {n_tie} near-tie swaps")
+        if tau == 1.0:
+            cur = P // 128
+            m = mask.cpu().numpy().astype(bool)
+            for qb in range(m.shape[2]):
+                assert m[:, :, qb, :cur + qb + 1].all() and not m[:, :, qb, cur + qb + 1:].any()
+            _check_rows(w, np.ones_like(est.mask), o, lse, P, heads=[5])

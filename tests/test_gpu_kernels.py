@@ -51,7 +51,7 @@ def test_estimate_mask_and_block_sums(case):
     mask, A = _estimate(w, S, tau)
     est = O.xattn_estimate(w.q, w.k, P, S, tau)
     check_block_sums(A, est.block_sums, S)
-    check_mask(mask, est, tau, P)
+    check_mask(mask, est, tau, P, A)
     assert bsx_last_error() == 0
 
 
@@ -144,8 +144,9 @@ def test_chunk_step_small():
     est, o_ref, lse_ref, keep_ref = O.chunk_step(w.q, w.k, w.v, P, S, tau, 256)
     q, k, v = (to_dev(x, "bf16") for x in (w.q, w.k, w.v))
     # BSA runs on the oracle's mask so that near-threshold rows cannot differ
-    mask_g = bsx_xattn_estimate(q, k, P, S, tau)
-    check_mask(mask_g.cpu().numpy(), est, tau, P)
+    A = torch.empty(est.block_sums.shape, dtype=torch.float32, device="cuda")
+    mask_g = bsx_xattn_estimate(q, k, P, S, tau, block_sums=A)
+    check_mask(mask_g.cpu().numpy(), est, tau, P, A.cpu().numpy())
     mask = torch.from_numpy(est.mask.astype(np.uint8)).cuda()
     cur, nkb = P // 128, (P + 512) // 128
     oh, lh = bsx_bsa_prefill(q, k, v, mask, P, 0, cur)
