@@ -5,7 +5,7 @@
 // mask (block size fixed at 128); xattn_bsa.py compute_chunked_prefill takes O
 // and LSE from the history part and the current-chunk part and merges them.
 //
-// One CTA per (128-row q-tile, q-head, batch); 6 warps with fixed roles:
+// One CTA per (128-row q-tile, q-head, batch); 10 warps with fixed roles:
 //   warp 0      TMA producer: Q once, then the K and V tiles of every selected
 //               key block, found by scanning the mask row, into a ring of
 //               tile-sized slots (K_0, V_0, K_1, V_1, ...).  A K slot is freed
@@ -13,7 +13,8 @@
 //               so loads run about two blocks ahead of the MMAs.
 //   warp 1      tcgen05 issuer: S = Q K^T into one of two TMEM buffers, and
 //               O += P V into a TMEM accumulator.
-//   warps 2..5  softmax, one query row per thread (TMEM lane = row): read S,
+//   warps 2..9  softmax, two threads per query row (TMEM lane = row, each
+//               thread 64 of the 128 key columns): read S,
 //               mask the diagonal block causally, online max with lazy
 //               rescaling of O (only when the running max grows by > 8 in
 //               log2 units), P = exp2(x - m) as bf16 into shared memory in the
@@ -32,13 +33,13 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;   // producer, MMA issuer, 8 softmax warps
 constexpr int kRegion = 128 * 128;  // bytes of one 128-row x 64-feature bf16 tile
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 enum Site : unsigned {
   kSiteKvEmpty = 1, kSiteQFull, kSiteKvFull, kSiteSFree, kSitePFull, kSiteSFull,
-  kSiteODone, kSiteODoneFinal
+  kSiteODone, kSiteODoneFinal, kSiteXchg
 };
 
 template <int D>
@@ -52,7 +53,8 @@ struct Layout {
   static constexpr int kBars = kRing + kSlots * kTile;    // mbarriers (8 B each)
   static constexpr int kNumBars = 32;
   static constexpr int kMisc = kBars + 8 * kNumBars;      // tmem slot, n, flags
-  static constexpr int kBytes = kMisc + 64;
+  static constexpr int kXchg = kMisc + 64;                // [2 halves][128 rows] fp32
+  static constexpr int kBytes = kXchg + 2 * 128 * 4;
   static constexpr uint32_t kTmemCols = 512;              // S0, S1, O (128 each; O uses D)
 };
 
@@ -83,6 +85,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
   const uint32_t p_full = bar0 + 8 * (kB2 + 4);
   const uint32_t o_done = bar0 + 8 * (kB2 + 5);
   const uint32_t mma_final = bar0 + 8 * (kB2 + 6);
+  auto xbar = [&](int q) { return bar0 + 8 * (kB2 + 7 + q); };  // softmax warp pairs
 
   const int qb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int nqb = gridDim.x;
@@ -99,9 +102,10 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(s_full(s), 1);
-      mbar_init(s_free(s), 128);
+      mbar_init(s_free(s), 256);
     }
-    mbar_init(p_full, 128);
+    for (int q = 0; q < 4; ++q) mbar_init(xbar(q), 64);
+    mbar_init(p_full, 256);
     mbar_init(o_done, 1);
     mbar_init(mma_final, 1);
     *abort_flag = 0;
@@ -243,9 +247,24 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
     }
   } else {
     // ------------------------------ softmax -------------------------------
-    const int quad = warp & 3;           // TMEM lane quadrant this warp may access
+    // 8 warps: two per TMEM lane quadrant (a warp may only touch the lanes
+    // 32 * (warp % 4) .. + 31), each owning 64 of the 128 columns of S, P
+    // and O for the 32 query rows of that quadrant.  The two halves of a row
+    // exchange their partial maxima (and at the end their row sums) through
+    // shared memory, synchronised by a 64-thread mbarrier per quadrant.
+    const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int row = quad * 32 + lane;    // query row within the tile
+    const int c0 = half * 64;            // first column this thread owns
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    float* xchg = reinterpret_cast<float*>(smem + L::kXchg);
+    int xphase = 0;
+    auto pair_sync = [&]() -> bool {
+      mbar_arrive(xbar(quad));
+      const bool r = mbar_wait(xbar(quad), xphase & 1, abort_flag, err, kErrBsaTc, kSiteXchg);
+      ++xphase;
+      return r;
+    };
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
@@ -255,45 +274,52 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
         break;
       }
       tc_fence_after();
-      float x[128];
-      tmem_ld128(tmem_s0 + lane_base + buf * 128, x);
+      float x[64];
+      tmem_ld64(tmem_s0 + lane_base + buf * 128 + c0, x);
       tc_fence_before();
       mbar_arrive(s_free(buf));
-      const bool is_diag = diag_last && j == n - 1;
-      // row max with 8 independent accumulators (no 128-long dependent chain)
+      if (diag_last && j == n - 1) {
+        // diagonal block: key column c is visible to row r iff c <= r
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (c0 + c > row) x[c] = -INFINITY;
+      }
       float mx[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) mx[e] = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        float v = x[c] * scale_log2;
-        if (is_diag && c > row) v = -INFINITY;
-        x[c] = v;
-        mx[c & 7] = fmaxf(mx[c & 7], v);
-      }
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+      for (int c = 0; c < 64; ++c) mx[c & 7] = fmaxf(mx[c & 7], x[c]);
+      const float pm = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                              fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      xchg[half * 128 + row] = pm;
+      if (!pair_sync()) {
+        ok = false;
+        break;
+      }
+      const float mt = fmaxf(pm, xchg[(1 - half) * 128 + row]) * scale_log2;
+      if (!pair_sync()) {  // the partner has read before the next write
+        ok = false;
+        break;
+      }
       const bool need = mt > m_run + kRescaleThreshold;
       float alpha = 1.f;
       if (need) {
         alpha = fast_exp2(m_run - mt);  // 0 on the first block
         m_run = mt;
       }
-      // P = exp2(x - m) packed to bf16 pairs while PV(j-1) still runs
-      uint32_t pk[64];
-      float ps[8];
+      // P = exp2(x * scale - m), packed to bf16 pairs while PV(j-1) still runs
+      uint32_t pk[32];
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+      const float neg_m = -m_run;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) ps[e] = 0.f;
-#pragma unroll
-      for (int c = 0; c < 128; c += 2) {
-        const float p0 = fast_exp2(x[c] - m_run);
-        const float p1 = fast_exp2(x[c + 1] - m_run);
-        ps[(c >> 1) & 7] += p0 + p1;
+      for (int c = 0; c < 64; c += 2) {
+        const float p0 = fast_exp2(fmaf(x[c], scale_log2, neg_m));
+        const float p1 = fast_exp2(fmaf(x[c + 1], scale_log2, neg_m));
+        ps[(c >> 1) & 3] += p0 + p1;
         __nv_bfloat162 t = __floats2bfloat162_rn(p0, p1);
         pk[c >> 1] = *reinterpret_cast<uint32_t*>(&t);
       }
-      const float rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-      l_run = l_run * alpha + rs;
+      l_run = l_run * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
       if (j > 0) {
         // PV(j-1) must be done before O is rescaled or P is overwritten
         if (!mbar_wait(o_done, (j - 1) & 1, abort_flag, err, kErrBsaTc, kSiteODone)) {
@@ -303,51 +329,60 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
         tc_fence_after();
         if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) {
+          for (int cc = 0; cc < D / 64; ++cc) {  // this half's O columns
             float t[32];
-            tmem_ld32(tmem_o + lane_base + cc * 32, t);
+            const uint32_t oc = tmem_o + lane_base + half * (D / 2) + cc * 32;
+            tmem_ld32(oc, t);
 #pragma unroll
             for (int e = 0; e < 32; ++e) t[e] *= alpha;
-            tmem_st32(tmem_o + lane_base + cc * 32, t);
+            tmem_st32(oc, t);
           }
         }
       }
-      // store P: 128-byte swizzled K-major rows, 16-byte chunks
-      uint8_t* prow = smem + L::kP + row * 128;
+      // store this half of P: region `half` (keys c0 .. c0+63), 128-byte
+      // swizzled K-major rows of 16-byte chunks
+      uint8_t* prow = smem + L::kP + half * kRegion + row * 128;
 #pragma unroll
-      for (int c8 = 0; c8 < 16; ++c8) {
-        const int region = c8 >> 3, chunk = c8 & 7;
-        *reinterpret_cast<uint4*>(prow + region * kRegion + ((chunk ^ (row & 7)) << 4)) =
-            make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
-      }
+      for (int chunk = 0; chunk < 8; ++chunk)
+        *reinterpret_cast<uint4*>(prow + ((chunk ^ (row & 7)) << 4)) =
+            make_uint4(pk[4 * chunk], pk[4 * chunk + 1], pk[4 * chunk + 2], pk[4 * chunk + 3]);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(p_full);
     }
+    // row sum = both halves
+    float l_tot = 0.f;
+    if (ok) {
+      xchg[half * 128 + row] = l_run;
+      ok = pair_sync();
+      if (ok) l_tot = l_run + xchg[(1 - half) * 128 + row];
+    }
     if (ok && mbar_wait(o_done, (n - 1) & 1, abort_flag, err, kErrBsaTc, kSiteODoneFinal)) {
       tc_fence_after();
-      const float inv = 1.f / l_run;
+      const float inv = 1.f / l_tot;
       __nv_bfloat16* orow = o + (((long long)b * q_len + qb * 128 + row) * Hq + h) * D;
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
+      for (int cc = 0; cc < D / 64; ++cc) {
         float t[32];
-        tmem_ld32(tmem_o + lane_base + cc * 32, t);
+        const int col = half * (D / 2) + cc * 32;
+        tmem_ld32(tmem_o + lane_base + col, t);
 #pragma unroll
         for (int e = 0; e < 32; e += 8) {
-          uint4 pk;
+          uint4 pk4;
           __nv_bfloat162 t0 = __floats2bfloat162_rn(t[e + 0] * inv, t[e + 1] * inv);
           __nv_bfloat162 t1 = __floats2bfloat162_rn(t[e + 2] * inv, t[e + 3] * inv);
           __nv_bfloat162 t2 = __floats2bfloat162_rn(t[e + 4] * inv, t[e + 5] * inv);
           __nv_bfloat162 t3 = __floats2bfloat162_rn(t[e + 6] * inv, t[e + 7] * inv);
-          pk.x = *reinterpret_cast<uint32_t*>(&t0);
-          pk.y = *reinterpret_cast<uint32_t*>(&t1);
-          pk.z = *reinterpret_cast<uint32_t*>(&t2);
-          pk.w = *reinterpret_cast<uint32_t*>(&t3);
-          reinterpret_cast<uint4*>(orow + cc * 32 + e)[0] = pk;
+          pk4.x = *reinterpret_cast<uint32_t*>(&t0);
+          pk4.y = *reinterpret_cast<uint32_t*>(&t1);
+          pk4.z = *reinterpret_cast<uint32_t*>(&t2);
+          pk4.w = *reinterpret_cast<uint32_t*>(&t3);
+          reinterpret_cast<uint4*>(orow + col + e)[0] = pk4;
         }
       }
-      lse[((long long)b * Hq + h) * q_len + qb * 128 + row] =
-          (m_run + __log2f(l_run)) * 0.69314718055994531f;
+      if (half == 0)
+        lse[((long long)b * Hq + h) * q_len + qb * 128 + row] =
+            (m_run + __log2f(l_tot)) * 0.69314718055994531f;
     }
   }
 
