@@ -354,9 +354,11 @@ def run_reference(args):
     S, tau = cfg.pop("stride"), cfg.pop("threshold")
     cfg.pop("chunk", None)
     w = make_workload(seed=args.seed, **cfg)
+    # each step: the oracle's chunk step on one q-head (a bounded sample),
+    # scaled to the whole chunk by the head count
     for _ in range(args.warmup):
         oracle_baseline(w, S, tau, 1)
-    vals = [oracle_baseline(w, S, tau, args.cpu_heads) for _ in range(args.steps)]
+    vals = [oracle_baseline(w, S, tau, 1) for _ in range(args.steps)]
     ms = float(np.mean([w.q.shape[1] / v["value"] * 1e3 for v in vals]))
     value = w.q.shape[0] * w.q.shape[1] / (ms / 1e3)
     base = dict(vals[-1])
@@ -380,7 +382,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(CONFIGS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--cpu-heads", type=int, default=2)
+    ap.add_argument("--cpu-heads", type=int, default=4,
+                    help="q-heads in the oracle sample of the cpu_baseline leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "gb300":

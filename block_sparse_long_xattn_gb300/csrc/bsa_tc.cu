@@ -11,17 +11,19 @@
 //               tile-sized slots (K_0, V_0, K_1, V_1, ...).  A K slot is freed
 //               as soon as its S MMA completes and a V slot after its P V MMA,
 //               so loads run about two blocks ahead of the MMAs.
-//   warp 1      tcgen05 issuer: S = Q K^T into one of two TMEM buffers, and
-//               O += P V into a TMEM accumulator.
-//   warps 2..9  softmax, two threads per query row (TMEM lane = row, each
-//               thread 64 of the 128 key columns): read S,
-//               mask the diagonal block causally, online max with lazy
-//               rescaling of O (only when the running max grows by > 8 in
-//               log2 units), P = exp2(x - m) as bf16 into shared memory in the
-//               128-byte-swizzled K-major layout the MMA reads, row sums, and
-//               at the end O / l and LSE to global memory.
-// The S MMA of block j+1 runs while the softmax of block j runs; the P V MMA
-// of block j runs while the softmax of block j+1 computes exponentials.
+//   warp 1      tcgen05 issuer: S(j) = Q K_j^T into TMEM buffer j % 2, and
+//               O_{j%2} += P(j) V_j with P(j) read from that same buffer.
+//   warps 2..9  two softmax groups of four warps; group g takes the blocks
+//               j = g, g + 2, ... with one query row per thread (TMEM lane =
+//               row): read S, mask the diagonal block causally, online max
+//               with lazy rescaling of O_g (only when the running max grows
+//               by more than 8 in log2 units), P = exp2(x - m) as bf16 pairs
+//               written back over the consumed S columns, row sums.  At the
+//               end the two partial results (O_g, m_g, l_g) are merged per
+//               row and O and LSE go to global memory.
+// Each group's chain S(j) -> softmax -> P V(j) -> S(j + 2) interleaves with
+// the other group's on the tensor pipe, and no per-block exchange between
+// warps is needed.  TMEM: S/P buffers in columns 0-255, O_0 and O_1 after.
 // Every wait is bounded (2 s of wall time); on expiry the CTA records the wait
 // in the device error word, drains its in-flight copies and MMAs, frees TMEM
 // and exits.
@@ -38,8 +40,8 @@ constexpr int kRegion = 128 * 128;  // bytes of one 128-row x 64-feature bf16 ti
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 enum Site : unsigned {
-  kSiteKvEmpty = 1, kSiteQFull, kSiteKvFull, kSiteSFree, kSitePFull, kSiteSFull,
-  kSiteODone, kSiteODoneFinal, kSiteXchg
+  kSiteKvEmpty = 1, kSiteQFull, kSiteKvFull, kSitePFull, kSiteSFull, kSiteODoneFinal,
+  kSiteXchg
 };
 
 template <int D>
@@ -48,14 +50,13 @@ struct Layout {
   static constexpr int kTile = kRegions * kRegion;        // Q, K or V tile bytes
   static constexpr int kSlots = D == 128 ? 5 : 8;         // K/V ring slots of kTile bytes
   static constexpr int kQ = 0;
-  static constexpr int kP = kQ + kTile;                   // 128 x 128 bf16, two regions
-  static constexpr int kRing = kP + 2 * kRegion;
+  static constexpr int kRing = kQ + kTile;
   static constexpr int kBars = kRing + kSlots * kTile;    // mbarriers (8 B each)
   static constexpr int kNumBars = 32;
   static constexpr int kMisc = kBars + 8 * kNumBars;      // tmem slot, n, flags
-  static constexpr int kXchg = kMisc + 64;                // [2 halves][128 rows] fp32
-  static constexpr int kBytes = kXchg + 2 * 128 * 4;
-  static constexpr uint32_t kTmemCols = 512;              // S0, S1, O (128 each; O uses D)
+  static constexpr int kXchg = kMisc + 64;                // [2 groups][m, l][128 rows] fp32
+  static constexpr int kBytes = kXchg + 2 * 2 * 128 * 4;
+  static constexpr uint32_t kTmemCols = 512;              // S/P 0, S/P 1, O_0, O_1
 };
 
 template <int D>
@@ -80,12 +81,11 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
   auto slot_full = [&](int s) { return bar0 + 8 * (1 + s); };
   auto slot_empty = [&](int s) { return bar0 + 8 * (1 + L::kSlots + s); };
   constexpr int kB2 = 1 + 2 * L::kSlots;
-  auto s_full = [&](int s) { return bar0 + 8 * (kB2 + s); };
-  auto s_free = [&](int s) { return bar0 + 8 * (kB2 + 2 + s); };
-  const uint32_t p_full = bar0 + 8 * (kB2 + 4);
-  const uint32_t o_done = bar0 + 8 * (kB2 + 5);
+  auto s_full = [&](int g) { return bar0 + 8 * (kB2 + g); };    // S(j) ready, g = j % 2
+  auto p_full = [&](int g) { return bar0 + 8 * (kB2 + 2 + g); };  // P(j) written
+  auto o_done = [&](int g) { return bar0 + 8 * (kB2 + 4 + g); };  // P V(j) complete
   const uint32_t mma_final = bar0 + 8 * (kB2 + 6);
-  auto xbar = [&](int q) { return bar0 + 8 * (kB2 + 7 + q); };  // softmax warp pairs
+  const uint32_t xbar = bar0 + 8 * (kB2 + 7);                    // end-of-row merge
 
   const int qb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int nqb = gridDim.x;
@@ -100,13 +100,12 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
       mbar_init(slot_full(s), 1);
       mbar_init(slot_empty(s), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(s_full(s), 1);
-      mbar_init(s_free(s), 256);
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(s_full(g), 1);
+      mbar_init(p_full(g), 128);
+      mbar_init(o_done(g), 1);
     }
-    for (int q = 0; q < 4; ++q) mbar_init(xbar(q), 64);
-    mbar_init(p_full, 256);
-    mbar_init(o_done, 1);
+    mbar_init(xbar, 256);
     mbar_init(mma_final, 1);
     *abort_flag = 0;
     *n_sm = 0;
@@ -133,7 +132,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
   const int n = *n_sm;
   // the diagonal block, when selected, is the last block of the row
   const bool diag_last = diag >= kb_begin && diag < kb_end && mrow[diag] != 0;
-  const uint32_t tmem_s0 = tmem, tmem_o = tmem + 256;
+  const uint32_t tmem_s0 = tmem, tmem_o0 = tmem + 256;
 
   if (n == 0) {
     // no visible key: O = 0, LSE = -inf
@@ -191,21 +190,24 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);
       bool ok = mbar_wait(q_full, 0, abort_flag, err, kErrBsaTc, kSiteQFull);
       auto issue_pv = [&](int i) -> bool {
+        const int g = i & 1;
         const int item = 2 * i + 1;  // V_i
         const int s = item % L::kSlots;
-        if (!mbar_wait(p_full, i & 1, abort_flag, err, kErrBsaTc, kSitePFull)) return false;
+        if (!mbar_wait(p_full(g), (i >> 1) & 1, abort_flag, err, kErrBsaTc, kSitePFull))
+          return false;
         if (!mbar_wait(slot_full(s), (item / L::kSlots) & 1, abort_flag, err, kErrBsaTc,
                        kSiteKvFull))
           return false;
         tc_fence_after();
         const uint32_t vbase = sb + L::kRing + s * L::kTile;
+        const uint32_t p_tmem = tmem_s0 + g * 128;  // P(i) overwrote S(i)
+        const uint32_t o_tmem = tmem_o0 + g * D;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {  // 16 keys per MMA
-          const uint64_t a = smem_desc_sw128(sb + L::kP + (k >> 2) * kRegion + (k & 3) * 32, 16, 1024);
+        for (int k = 0; k < 8; ++k) {  // 16 keys per MMA: 8 TMEM columns of bf16 pairs
           const uint64_t bd = smem_desc_sw128(vbase + k * 2048, kRegion, 1024);
-          mma_bf16(tmem_o, a, bd, idesc_pv, (i > 0 || k > 0) ? 1u : 0u);
+          mma_bf16_tmem_a(o_tmem, p_tmem + k * 8, bd, idesc_pv, (i >= 2 || k > 0) ? 1u : 0u);
         }
-        mma_commit(o_done);
+        mma_commit(o_done(g));
         mma_commit(slot_empty(s));
         return true;
       };
@@ -213,14 +215,11 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
       for (; ok && j < n; ++j) {
         const int item = 2 * j;  // K_j
         const int s = item % L::kSlots;
-        const int buf = j & 1;
+        const int g = j & 1;
+        // S(j) overwrites P(j-2) in buffer g: P V(j-2) was issued in the
+        // previous iteration and the tensor pipe runs the MMAs in order
         if (!mbar_wait(slot_full(s), (item / L::kSlots) & 1, abort_flag, err, kErrBsaTc,
                        kSiteKvFull)) {
-          ok = false;
-          break;
-        }
-        if (j >= 2 &&
-            !mbar_wait(s_free(buf), ((j >> 1) - 1) & 1, abort_flag, err, kErrBsaTc, kSiteSFree)) {
           ok = false;
           break;
         }
@@ -231,9 +230,9 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
           const uint32_t off = (k >> 2) * kRegion + (k & 3) * 32;
           const uint64_t a = smem_desc_sw128(sb + L::kQ + off, 16, 1024);
           const uint64_t bd = smem_desc_sw128(kbase + off, 16, 1024);
-          mma_bf16(tmem_s0 + buf * 128, a, bd, idesc_qk, k > 0 ? 1u : 0u);
+          mma_bf16(tmem_s0 + g * 128, a, bd, idesc_qk, k > 0 ? 1u : 0u);
         }
-        mma_commit(s_full(buf));
+        mma_commit(s_full(g));
         mma_commit(slot_empty(s));
         if (j >= 1 && !issue_pv(j - 1)) {
           ok = false;
@@ -247,72 +246,47 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
     }
   } else {
     // ------------------------------ softmax -------------------------------
-    // 8 warps: two per TMEM lane quadrant (a warp may only touch the lanes
-    // 32 * (warp % 4) .. + 31), each owning 64 of the 128 columns of S, P
-    // and O for the 32 query rows of that quadrant.  The two halves of a row
-    // exchange their partial maxima (and at the end their row sums) through
-    // shared memory, synchronised by a 64-thread mbarrier per quadrant.
-    const int quad = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int quad = warp & 3;           // TMEM lane quadrant this warp may access
+    const int grp = (warp - 2) >> 2;     // takes blocks j = grp, grp + 2, ...
     const int row = quad * 32 + lane;    // query row within the tile
-    const int c0 = half * 64;            // first column this thread owns
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    float* xchg = reinterpret_cast<float*>(smem + L::kXchg);
-    int xphase = 0;
-    auto pair_sync = [&]() -> bool {
-      mbar_arrive(xbar(quad));
-      const bool r = mbar_wait(xbar(quad), xphase & 1, abort_flag, err, kErrBsaTc, kSiteXchg);
-      ++xphase;
-      return r;
-    };
+    const uint32_t sbuf = tmem_s0 + lane_base + grp * 128;
+    const uint32_t obuf = tmem_o0 + lane_base + grp * D;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    for (int j = 0; j < n; ++j) {
-      const int buf = j & 1;
-      if (!mbar_wait(s_full(buf), (j >> 1) & 1, abort_flag, err, kErrBsaTc, kSiteSFull)) {
+    for (int j = grp; j < n; j += 2) {
+      if (!mbar_wait(s_full(grp), (j >> 1) & 1, abort_flag, err, kErrBsaTc, kSiteSFull)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float x[64];
-      tmem_ld64(tmem_s0 + lane_base + buf * 128 + c0, x);
-      tc_fence_before();
-      mbar_arrive(s_free(buf));
+      float x[128];
+      tmem_ld128(sbuf, x);
       if (diag_last && j == n - 1) {
         // diagonal block: key column c is visible to row r iff c <= r
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (c0 + c > row) x[c] = -INFINITY;
+        for (int c = 0; c < 128; ++c)
+          if (c > row) x[c] = -INFINITY;
       }
       float mx[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) mx[e] = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 64; ++c) mx[c & 7] = fmaxf(mx[c & 7], x[c]);
-      const float pm = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      xchg[half * 128 + row] = pm;
-      if (!pair_sync()) {
-        ok = false;
-        break;
-      }
-      const float mt = fmaxf(pm, xchg[(1 - half) * 128 + row]) * scale_log2;
-      if (!pair_sync()) {  // the partner has read before the next write
-        ok = false;
-        break;
-      }
+      for (int c = 0; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], x[c]);
+      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * scale_log2;
       const bool need = mt > m_run + kRescaleThreshold;
       float alpha = 1.f;
       if (need) {
-        alpha = fast_exp2(m_run - mt);  // 0 on the first block
+        alpha = fast_exp2(m_run - mt);  // 0 on the group's first block
         m_run = mt;
       }
-      // P = exp2(x * scale - m), packed to bf16 pairs while PV(j-1) still runs
-      uint32_t pk[32];
+      // P = exp2(x * scale - m) as bf16 pairs
+      uint32_t pk[64];
       float ps[4] = {0.f, 0.f, 0.f, 0.f};
       const float neg_m = -m_run;
 #pragma unroll
-      for (int c = 0; c < 64; c += 2) {
+      for (int c = 0; c < 128; c += 2) {
         const float p0 = fast_exp2(fmaf(x[c], scale_log2, neg_m));
         const float p1 = fast_exp2(fmaf(x[c + 1], scale_log2, neg_m));
         ps[(c >> 1) & 3] += p0 + p1;
@@ -320,69 +294,77 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
         pk[c >> 1] = *reinterpret_cast<uint32_t*>(&t);
       }
       l_run = l_run * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
-      if (j > 0) {
-        // PV(j-1) must be done before O is rescaled or P is overwritten
-        if (!mbar_wait(o_done, (j - 1) & 1, abort_flag, err, kErrBsaTc, kSiteODone)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, need)) {
+      // O_g is rescaled between P V(j-2) and P V(j).  P V(j-2) is complete:
+      // the tensor pipe ran it before S(j), which we have read.
+      if (j >= 2 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
-          for (int cc = 0; cc < D / 64; ++cc) {  // this half's O columns
-            float t[32];
-            const uint32_t oc = tmem_o + lane_base + half * (D / 2) + cc * 32;
-            tmem_ld32(oc, t);
+        for (int cc = 0; cc < D / 32; ++cc) {
+          float t[32];
+          tmem_ld32(obuf + cc * 32, t);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) t[e] *= alpha;
-            tmem_st32(oc, t);
-          }
+          for (int e = 0; e < 32; ++e) t[e] *= alpha;
+          tmem_st32(obuf + cc * 32, t);
         }
       }
-      // store this half of P: region `half` (keys c0 .. c0+63), 128-byte
-      // swizzled K-major rows of 16-byte chunks
-      uint8_t* prow = smem + L::kP + half * kRegion + row * 128;
-#pragma unroll
-      for (int chunk = 0; chunk < 8; ++chunk)
-        *reinterpret_cast<uint4*>(prow + ((chunk ^ (row & 7)) << 4)) =
-            make_uint4(pk[4 * chunk], pk[4 * chunk + 1], pk[4 * chunk + 2], pk[4 * chunk + 3]);
-      fence_proxy_async_smem();
+      tmem_st64(sbuf, reinterpret_cast<const float*>(pk));  // P(j) over S(j)
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(p_full(grp));
     }
-    // row sum = both halves
-    float l_tot = 0.f;
+    // ---- merge the two groups' partial results per row ----
+    float* xm = reinterpret_cast<float*>(smem + L::kXchg);   // [group][m, l][row]
+    xm[(grp * 2 + 0) * 128 + row] = m_run;
+    xm[(grp * 2 + 1) * 128 + row] = l_run;
+    const int j_last = ((n - 1 - grp) >= 0) ? n - 1 - ((n - 1 - grp) & 1) : -1;
+    if (ok && j_last >= 0 &&
+        !mbar_wait(o_done(grp), (j_last >> 1) & 1, abort_flag, err, kErrBsaTc, kSiteODoneFinal))
+      ok = false;
+    mbar_arrive(xbar);
+    if (!mbar_wait(xbar, 0, abort_flag, err, kErrBsaTc, kSiteXchg)) ok = false;
     if (ok) {
-      xchg[half * 128 + row] = l_run;
-      ok = pair_sync();
-      if (ok) l_tot = l_run + xchg[(1 - half) * 128 + row];
-    }
-    if (ok && mbar_wait(o_done, (n - 1) & 1, abort_flag, err, kErrBsaTc, kSiteODoneFinal)) {
       tc_fence_after();
-      const float inv = 1.f / l_tot;
+      const float m0 = xm[0 * 128 + row], l0 = xm[1 * 128 + row];
+      const float m1 = xm[2 * 128 + row], l1 = xm[3 * 128 + row];
+      const float m = fmaxf(m0, m1);
+      // group 1 has no block when n == 1 (uniform over the CTA, so the
+      // warp-collective TMEM loads below stay convergent)
+      const bool has1 = n >= 2;
+      const float w0 = fast_exp2(m0 - m);
+      const float w1 = has1 ? fast_exp2(m1 - m) : 0.f;
+      const float l = l0 * w0 + l1 * w1;
+      const float inv = 1.f / l;
+      const float f0 = w0 * inv, f1 = w1 * inv;
+      // this group writes output columns [grp * D/2, grp * D/2 + D/2)
       __nv_bfloat16* orow = o + (((long long)b * q_len + qb * 128 + row) * Hq + h) * D;
 #pragma unroll
       for (int cc = 0; cc < D / 64; ++cc) {
-        float t[32];
-        const int col = half * (D / 2) + cc * 32;
-        tmem_ld32(tmem_o + lane_base + col, t);
+        const int col = grp * (D / 2) + cc * 32;
+        float t0[32], t1[32];
+        tmem_ld32(tmem_o0 + lane_base + col, t0);
+        if (has1) {
+          tmem_ld32(tmem_o0 + lane_base + D + col, t1);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) t0[e] = t0[e] * f0 + t1[e] * f1;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) t0[e] *= f0;
+        }
 #pragma unroll
         for (int e = 0; e < 32; e += 8) {
           uint4 pk4;
-          __nv_bfloat162 t0 = __floats2bfloat162_rn(t[e + 0] * inv, t[e + 1] * inv);
-          __nv_bfloat162 t1 = __floats2bfloat162_rn(t[e + 2] * inv, t[e + 3] * inv);
-          __nv_bfloat162 t2 = __floats2bfloat162_rn(t[e + 4] * inv, t[e + 5] * inv);
-          __nv_bfloat162 t3 = __floats2bfloat162_rn(t[e + 6] * inv, t[e + 7] * inv);
-          pk4.x = *reinterpret_cast<uint32_t*>(&t0);
-          pk4.y = *reinterpret_cast<uint32_t*>(&t1);
-          pk4.z = *reinterpret_cast<uint32_t*>(&t2);
-          pk4.w = *reinterpret_cast<uint32_t*>(&t3);
+          __nv_bfloat162 a0 = __floats2bfloat162_rn(t0[e + 0], t0[e + 1]);
+          __nv_bfloat162 a1 = __floats2bfloat162_rn(t0[e + 2], t0[e + 3]);
+          __nv_bfloat162 a2 = __floats2bfloat162_rn(t0[e + 4], t0[e + 5]);
+          __nv_bfloat162 a3 = __floats2bfloat162_rn(t0[e + 6], t0[e + 7]);
+          pk4.x = *reinterpret_cast<uint32_t*>(&a0);
+          pk4.y = *reinterpret_cast<uint32_t*>(&a1);
+          pk4.z = *reinterpret_cast<uint32_t*>(&a2);
+          pk4.w = *reinterpret_cast<uint32_t*>(&a3);
           reinterpret_cast<uint4*>(orow + col + e)[0] = pk4;
         }
       }
-      if (half == 0)
+      if (grp == 0)
         lse[((long long)b * Hq + h) * q_len + qb * 128 + row] =
-            (m_run + __log2f(l_tot)) * 0.69314718055994531f;
+            (m + __log2f(l)) * 0.69314718055994531f;
     }
   }
 
