@@ -159,6 +159,21 @@ def estimate_flops(cfg, q_len, q_start_pos, stride):
     return 2.0 * cfg["d"] * stride * pairs * cfg["Hq"] * cfg["B"]
 
 
+def aggregate_ranks(local_ms, tokens_per_rank, world, device):
+    """Whole-job throughput: every rank runs its own replica, so the job
+    takes the slowest rank's time (max over ranks) and processes
+    tokens_per_rank on each rank.  Returns (max times, total tokens,
+    tokens/s from the first time)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(local_ms, dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    times = t.tolist()
+    tokens = tokens_per_rank * world
+    return times, tokens, tokens / (times[0] / 1e3)
+
+
 # ---------------------------------------------------------------------------
 def run_gpu(args):
     import torch
@@ -261,12 +276,8 @@ def run_gpu(args):
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in (out_host, lse_host, keep_host))
 
-    times = torch.tensor([ms_step, float(np.mean(e2e_ms))], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    ms_step, ms_e2e = times.tolist()
-    tokens = B * Lq * world
-    value = tokens / (ms_step / 1e3)
+    (ms_step, ms_e2e), tokens, value = aggregate_ranks(
+        [ms_step, float(np.mean(e2e_ms))], B * Lq, world, dev)
 
     hbm_peak, tc_peak, peak_src = _peaks()
     bsa_ms = float(np.mean(t_bh) + np.mean(t_bc)) / 2.0        # average launch
