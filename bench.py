@@ -16,6 +16,7 @@ outside the events.  value = tokens/s/layer over all ranks (each rank runs an
 independent replica; the path has no cross-GPU exchange).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--step chunk|fused|offload|prefill]
     python bench.py --impl reference     # the fp64 CPU oracle, timed on a sample
 """
 from __future__ import annotations
@@ -193,50 +194,80 @@ def run_gpu(args):
     B, Lq, Hq, d = w.q.shape
     P, Lk, Hkv = w.q_start_pos, w.k.shape[1], cfg["Hkv"]
     cur, nkb = P // 128, Lk // 128
+    cpu_tokens = 1024
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
 
     host = {n: torch.from_numpy(x).to(tdt).pin_memory() for n, x in
             (("q", w.q), ("k", w.k), ("v", w.v))}
     dq, dk, dv = (host[n].to(dev) for n in ("q", "k", "v"))
     mask = torch.empty((B, Hq, Lq // 128, nkb), dtype=torch.uint8, device=dev)
+    omask = torch.empty_like(mask)
     ws = torch.empty(bsx.bsx_estimate_workspace_bytes(bsx.shape_of(dq, dk), Lq, P, S),
                      dtype=torch.uint8, device=dev)
     oh = torch.empty_like(dq)
     oc = torch.empty_like(dq)
     lh = torch.empty((B, Hq, Lq), dtype=torch.float32, device=dev)
     lc = torch.empty_like(lh)
-    keep = torch.empty((B, P // 1024), dtype=torch.uint8, device=dev)
+    keep = torch.empty((B, P // cpu_tokens), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-    LAUNCHES_PER_STEP = 6  # estimate scores + selection, BSA x2, merge, map
+
+    def est(q, k, v):
+        bsx.bsx_xattn_estimate(q, k, P, S, tau, mask=mask, workspace=ws, stream=stream)
+
+    def bsa(m, kb0, kb1, o, lse):
+        return lambda q, k, v: bsx.bsx_bsa_prefill(q, k, v, m, P, kb0, kb1, o=o, lse=lse,
+                                                   stream=stream)
+
+    def merge_map(q, k, v):
+        bsx.bsx_merge_attn(oh, lh, oc, lc, stream=stream)
+        if P >= cpu_tokens:
+            bsx.bsx_map_mask_to_cpu_blocks(mask, P, cpu_tokens, keep=keep, stream=stream)
+
+    def offload_mask(q, k, v):
+        bsx.bsx_map_mask_to_cpu_blocks(mask, P, cpu_tokens, True, keep=keep, stream=stream)
+        bsx.bsx_cpu_block_mask(keep, Lq, P, Hq, cpu_tokens, mask=omask, stream=stream)
+
+    def merge_only(q, k, v):
+        bsx.bsx_merge_attn(oh, lh, oc, lc, stream=stream)
+
+    # phases of one step, timed separately; the BSA phases give the roofline
+    if args.step == "chunk":
+        phases = [("estimate", est), ("bsa_hist", bsa(mask, 0, cur, oh, lh)),
+                  ("bsa_curr", bsa(mask, cur, nkb, oc, lc)), ("merge_map", merge_map)]
+        launches = 6
+    elif args.step in ("fused", "prefill"):
+        # the launches bsx_chunk_prefill enqueues, timed one by one
+        phases = [("estimate", est), ("bsa_all", bsa(mask, 0, nkb, oh, lh))]
+        launches = 3
+    elif args.step == "offload":
+        phases = [("estimate", est), ("cpu_blocks", offload_mask),
+                  ("bsa_hist", bsa(omask, 0, cur, oh, lh)),
+                  ("bsa_curr", bsa(omask, cur, nkb, oc, lc)), ("merge", merge_only)]
+        launches = 7
+    else:
+        raise ValueError(args.step)
 
     def step(q, k, v, ev=None):
         if ev:
             ev[0].record(stream)
-        bsx.bsx_xattn_estimate(q, k, P, S, tau, mask=mask, workspace=ws, stream=stream)
-        if ev:
-            ev[1].record(stream)
-        bsx.bsx_bsa_prefill(q, k, v, mask, P, 0, cur, o=oh, lse=lh, stream=stream)
-        if ev:
-            ev[2].record(stream)
-        bsx.bsx_bsa_prefill(q, k, v, mask, P, cur, nkb, o=oc, lse=lc, stream=stream)
-        if ev:
-            ev[3].record(stream)
-        bsx.bsx_merge_attn(oh, lh, oc, lc, stream=stream)
-        bsx.bsx_map_mask_to_cpu_blocks(mask, P, 1024, keep=keep, stream=stream)
-        if ev:
-            ev[4].record(stream)
+        for i, (_, fn) in enumerate(phases):
+            fn(q, k, v)
+            if ev:
+                ev[i + 1].record(stream)
 
     for _ in range(args.warmup):
         step(dq, dk, dv)
     torch.cuda.synchronize()
-    mask_np = mask.cpu().numpy()
-    flops_hist = bsa_flops(mask_np, P, 0, cur, d)
-    flops_curr = bsa_flops(mask_np, P, cur, nkb, d)
+    bsa_mask = (omask if args.step == "offload" else mask).cpu().numpy()
     causal_blocks = sum(cur + qb + 1 for qb in range(Lq // 128)) * B * Hq
-    density = float(mask_np.astype(bool).sum()) / causal_blocks
+    density = float(mask.cpu().numpy().astype(bool).sum()) / causal_blocks
+    ranges = {"bsa_hist": (0, cur), "bsa_curr": (cur, nkb), "bsa_all": (0, nkb)}
+    flops = {n: bsa_flops(bsa_mask, P, *ranges[n], d) for n, _ in phases if n in ranges}
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    np_ = len(phases)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(np_ + 1)]
+           for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -246,14 +277,13 @@ def run_gpu(args):
             step(dq, dk, dv, evs[i])
         torch.cuda.synchronize()
     clocks = clk.summary()
-    t_step = [evs[i][0].elapsed_time(evs[i][4]) for i in range(args.steps)]
-    t_est = [evs[i][0].elapsed_time(evs[i][1]) for i in range(args.steps)]
-    t_bh = [evs[i][1].elapsed_time(evs[i][2]) for i in range(args.steps)]
-    t_bc = [evs[i][2].elapsed_time(evs[i][3]) for i in range(args.steps)]
-    t_tail = [evs[i][3].elapsed_time(evs[i][4]) for i in range(args.steps)]
+    t_step = [evs[i][0].elapsed_time(evs[i][np_]) for i in range(args.steps)]
+    t_phase = {n: float(np.mean([evs[i][j].elapsed_time(evs[i][j + 1])
+                                 for i in range(args.steps)]))
+               for j, (n, _) in enumerate(phases)}
     ms_step = float(np.mean(t_step))
 
-    # end to end through the public API: pinned host inputs in, O/LSE/keep out
+    # end to end through the public API: pinned host inputs in, O/LSE(/flags) out
     out_host = torch.empty(oh.shape, dtype=oh.dtype).pin_memory()
     lse_host = torch.empty(lh.shape, dtype=torch.float32).pin_memory()
     keep_host = torch.empty(keep.shape, dtype=torch.uint8).pin_memory()
@@ -266,58 +296,69 @@ def run_gpu(args):
         q2 = host["q"].to(dev, non_blocking=True)
         k2 = host["k"].to(dev, non_blocking=True)
         v2 = host["v"].to(dev, non_blocking=True)
-        step(q2, k2, v2)
+        if args.step in ("fused", "prefill"):
+            bsx.bsx_chunk_prefill(q2, k2, v2, P, S, tau, mask=mask, o=oh, lse=lh,
+                                  workspace=ws, stream=stream)
+        else:
+            step(q2, k2, v2)
         out_host.copy_(oh, non_blocking=True)
         lse_host.copy_(lh, non_blocking=True)
-        keep_host.copy_(keep, non_blocking=True)
+        if keep.numel() and args.step in ("chunk", "offload"):
+            keep_host.copy_(keep, non_blocking=True)
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = sum(t.numel() * t.element_size() for t in (out_host, lse_host, keep_host))
+    d2h = sum(t.numel() * t.element_size() for t in (out_host, lse_host))
+    if keep.numel() and args.step in ("chunk", "offload"):
+        d2h += keep_host.numel()
 
     (ms_step, ms_e2e), tokens, value = aggregate_ranks(
         [ms_step, float(np.mean(e2e_ms))], B * Lq, world, dev)
 
     hbm_peak, tc_peak, peak_src = _peaks()
-    bsa_ms = float(np.mean(t_bh) + np.mean(t_bc)) / 2.0        # average launch
-    bsa_flops_launch = (flops_hist + flops_curr) / 2.0
+    bsa_names = [n for n, _ in phases if n in ranges]
+    bsa_ms = float(np.mean([t_phase[n] for n in bsa_names]))        # mean launch
+    bsa_flops_launch = float(np.mean([flops[n] for n in bsa_names]))
     achieved = bsa_flops_launch / (bsa_ms / 1e3) / 1e12
-    traffic = _traffic_per_launch("bsa_prefill")
+    traffic = _traffic_per_launch("bsa_prefill") if args.step == "chunk" and \
+        args.workload == DEFAULT_WORKLOAD else None
     est_fl = estimate_flops(cfg, Lq, P, S)
     est_bytes = (dq.numel() + dk.numel()) * dq.element_size() + mask.numel()
-    est_ms = float(np.mean(t_est))
+    est_ms = t_phase["estimate"]
+
+    kernels = {f"{n}_ms": t for n, t in t_phase.items()}
+    kernels.update({
+        "estimate_tflops": est_fl / (est_ms / 1e3) / 1e12,
+        "estimate_tc_frac": est_fl / (est_ms / 1e3) / 1e12 / tc_peak,
+        "estimate_gbs": est_bytes / (est_ms / 1e3) / 1e9,
+        "estimate_hbm_frac": est_bytes / (est_ms / 1e3) / 1e9 / hbm_peak,
+    })
+    for n in bsa_names:
+        kernels[f"{n}_tflops"] = flops[n] / (t_phase[n] / 1e3) / 1e12
 
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic (seeded planted-direction N(0,1) inputs)",
-        "config": {"workload": args.workload, "B": B, "Hq": Hq, "Hkv": Hkv, "d": d,
-                   "q_len": Lq, "q_start_pos": P, "Lk": Lk, "stride": S, "threshold": tau,
-                   "cpu_block_tokens": 1024, "parallelism": f"replicas{world}",
+        "config": {"workload": args.workload, "step": args.step, "B": B, "Hq": Hq,
+                   "Hkv": Hkv, "d": d, "q_len": Lq, "q_start_pos": P, "Lk": Lk, "stride": S,
+                   "threshold": tau, "cpu_block_tokens": cpu_tokens,
+                   "parallelism": f"replicas{world}",
                    "l2": "flushed (256 MiB write) between timed steps", "seed": args.seed},
         "roofline": {"kernel": DOMINANT, "bound": "tensor", "achieved": achieved,
                      "peak": tc_peak, "unit": "TFLOP/s", "frac": achieved / tc_peak,
                      "traffic": traffic, "peak_source": peak_src,
                      "flops_per_launch": bsa_flops_launch, "ms_per_launch": bsa_ms},
-        "kernels": {
-            "estimate_ms": est_ms, "bsa_hist_ms": float(np.mean(t_bh)),
-            "bsa_curr_ms": float(np.mean(t_bc)), "merge_map_ms": float(np.mean(t_tail)),
-            "estimate_tflops": est_fl / (est_ms / 1e3) / 1e12,
-            "estimate_tc_frac": est_fl / (est_ms / 1e3) / 1e12 / tc_peak,
-            "estimate_gbs": est_bytes / (est_ms / 1e3) / 1e9,
-            "estimate_hbm_frac": est_bytes / (est_ms / 1e3) / 1e9 / hbm_peak,
-            "bsa_hist_tflops": flops_hist / (np.mean(t_bh) / 1e3) / 1e12,
-            "bsa_curr_tflops": flops_curr / (np.mean(t_bc) / 1e3) / 1e12,
-        },
+        "kernels": kernels,
         "density": density,
         "e2e": {"value": tokens / (ms_e2e / 1e3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
-        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "gpu_launches": launches * args.steps,
         "clocks": clocks,
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and args.step == "chunk":
         result["cpu_baseline"] = oracle_baseline(w, S, tau, args.cpu_heads)
     if rank == 0:
         print(json.dumps(result), flush=True)
@@ -392,6 +433,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(CONFIGS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--step", default="chunk", choices=["chunk", "fused", "offload", "prefill"],
+                    help="chunk: estimate, BSA on history and current chunk, merge, map "
+                         "(the default); fused: estimate + one BSA launch over all key "
+                         "blocks; offload: the pages' CPU-block-dense history; prefill: "
+                         "fused on a whole-sequence workload")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-heads", type=int, default=4,
                     help="q-heads in the oracle sample of the cpu_baseline leg")
@@ -399,6 +445,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "gb300":
         ap.error("at least 3 warm-up steps")
+    if args.step == "prefill" and args.workload == DEFAULT_WORKLOAD:
+        args.workload = "llama8b-32k-prefill"
     if args.impl == "reference":
         run_reference(args)
     else:

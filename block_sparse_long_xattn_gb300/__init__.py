@@ -11,6 +11,8 @@ from ._lib import (  # noqa: F401
     BsxError,
     BsxShape,
     bsx_bsa_prefill,
+    bsx_chunk_prefill,
+    bsx_cpu_block_mask,
     bsx_estimate_workspace_bytes,
     bsx_last_error,
     bsx_map_mask_to_cpu_blocks,

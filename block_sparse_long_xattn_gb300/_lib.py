@@ -24,7 +24,8 @@ STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported", -3: "CUDA error",
 
 EXPORTS = ("bsx_version", "bsx_status_string", "bsx_estimate_workspace_bytes",
            "bsx_xattn_estimate", "bsx_bsa_prefill", "bsx_merge_attn",
-           "bsx_map_mask_to_cpu_blocks", "bsx_last_error", "bsx_xattn_estimate_noalloc")
+           "bsx_map_mask_to_cpu_blocks", "bsx_last_error", "bsx_xattn_estimate_noalloc",
+           "bsx_cpu_block_mask", "bsx_chunk_prefill")
 
 
 class BsxShape(ctypes.Structure):
@@ -73,6 +74,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.bsx_merge_attn.argtypes = [BsxShape, i32, vp, vp, vp, vp, vp]
         lib.bsx_map_mask_to_cpu_blocks.restype = i32
         lib.bsx_map_mask_to_cpu_blocks.argtypes = [BsxShape, vp, i32, i32, i32, i32, vp, vp]
+        lib.bsx_chunk_prefill.restype = i32
+        lib.bsx_chunk_prefill.argtypes = [BsxShape, vp, vp, vp, i32, i32, i32, f32, vp, vp,
+                                          vp, vp, sz, vp]
+        lib.bsx_cpu_block_mask.restype = i32
+        lib.bsx_cpu_block_mask.argtypes = [BsxShape, vp, i32, i32, i32, vp, vp]
         lib.bsx_last_error.restype = i32
         lib.bsx_last_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
         _lib = lib
@@ -174,6 +180,29 @@ def bsx_bsa_prefill(q, k, v, mask, q_start_pos: int, kb_begin: int = 0,
     return o, lse
 
 
+def bsx_chunk_prefill(q, k, v, q_start_pos: int, stride: int, threshold: float, *,
+                      mask=None, o=None, lse=None, workspace=None, stream=None):
+    """Estimate + block-sparse attention over all key blocks -> (mask, o, lse)."""
+    lib = load()
+    B, q_len, Hq, _ = q.shape
+    Lk = k.shape[1]
+    shape = shape_of(q, k)
+    if mask is None:
+        mask = torch.empty((B, Hq, q_len // 128, Lk // 128), dtype=torch.uint8, device=q.device)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, q_len), dtype=torch.float32, device=q.device)
+    need = lib.bsx_estimate_workspace_bytes(shape, q_len, q_start_pos, stride)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check("bsx_chunk_prefill", lib.bsx_chunk_prefill(
+        shape, _ptr(q), _ptr(k), _ptr(v), q_len, q_start_pos, stride, float(threshold),
+        _ptr(mask), _ptr(o), _ptr(lse), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return mask, o, lse
+
+
 def bsx_merge_attn(o1, lse1, o2, lse2, *, stream=None):
     """In-place LSE merge of (o2, lse2) into (o1, lse1); returns (o1, lse1)."""
     lib = load()
@@ -198,6 +227,21 @@ def bsx_map_mask_to_cpu_blocks(mask, q_start_pos: int, cpu_block_tokens: int = 1
         shape, _ptr(mask), nqb * 128, q_start_pos, cpu_block_tokens, flags,
         _ptr(keep) if keep.numel() else None, _stream(stream)))
     return keep
+
+
+def bsx_cpu_block_mask(keep, q_len: int, q_start_pos: int, Hq: int,
+                       cpu_block_tokens: int = 1024, *, mask=None, stream=None):
+    """Offload-mode BSA block mask [B, Hq, q_len/128, Lk/128] from keep flags."""
+    lib = load()
+    B = keep.shape[0]
+    nkb = (q_start_pos + q_len) // 128
+    if mask is None:
+        mask = torch.empty((B, Hq, q_len // 128, nkb), dtype=torch.uint8, device=keep.device)
+    shape = BsxShape(B, Hq, Hq, 128, BSX_BF16)
+    _check("bsx_cpu_block_mask", lib.bsx_cpu_block_mask(
+        shape, _ptr(keep) if keep.numel() else None, q_len, q_start_pos, cpu_block_tokens,
+        _ptr(mask), _stream(stream)))
+    return mask
 
 
 def bsx_last_error() -> int:

@@ -157,6 +157,34 @@ int bsx_map_mask_to_cpu_blocks(bsx_shape s, const uint8_t* mask, int q_len,
                                      static_cast<cudaStream_t>(stream)));
 }
 
+int bsx_chunk_prefill(bsx_shape s, const void* q, const void* k, const void* v, int q_len,
+                      int q_start_pos, int stride, float threshold, uint8_t* mask, void* o,
+                      float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  // validate everything before the first launch, so nothing is enqueued on error
+  bsx::Problem p;
+  int rc = make_problem(s, q_len, q_start_pos, &p);
+  if (rc != BSX_OK) return rc;
+  if (!v || !o || !lse || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return BSX_ERR_INVALID_ARG;
+  if (p.nkb > kMaxKeyBlocks) return BSX_ERR_UNSUPPORTED;
+  rc = bsx_xattn_estimate(s, q, k, q_len, q_start_pos, stride, threshold, mask, nullptr,
+                          workspace, workspace_bytes, stream);
+  if (rc != BSX_OK) return rc;
+  return bsx_bsa_prefill(s, q, k, v, mask, q_len, q_start_pos, 0, p.nkb, o, lse, stream);
+}
+
+int bsx_cpu_block_mask(bsx_shape s, const uint8_t* keep, int q_len, int q_start_pos,
+                       int cpu_block_tokens, uint8_t* mask, void* stream) {
+  bsx::Problem p;
+  int rc = make_problem(s, q_len, q_start_pos, &p);
+  if (rc != BSX_OK) return rc;
+  if (cpu_block_tokens < 128 || cpu_block_tokens % 128 != 0) return BSX_ERR_INVALID_ARG;
+  if (q_start_pos % cpu_block_tokens != 0) return BSX_ERR_INVALID_ARG;
+  if (!mask || (q_start_pos > 0 && !keep)) return BSX_ERR_INVALID_ARG;
+  return cuda_status(bsx::launch_cpu_block_mask(p, keep, cpu_block_tokens, mask,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
 int bsx_last_error(unsigned int* code) {
   if (!code) return BSX_ERR_INVALID_ARG;
   *code = 0;

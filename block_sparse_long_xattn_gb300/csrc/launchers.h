@@ -23,6 +23,10 @@ cudaError_t launch_merge(const Problem& p, void* o1, float* lse1, const void* o2
 cudaError_t launch_map(const Problem& p, const uint8_t* mask, int cpu_block_tokens,
                        int flags, uint8_t* keep, cudaStream_t st);
 
+// Offload-mode block mask from CPU-block keep flags.
+cudaError_t launch_cpu_block_mask(const Problem& p, const uint8_t* keep, int cpu_block_tokens,
+                                  uint8_t* mask, cudaStream_t st);
+
 // a1-a2 partial: per (b, h, key block, reshaped row) log-sum-exp of the scaled
 // scores of that row over that block's reshaped columns (CUDA cores).
 cudaError_t launch_estimate_simt(const Problem& p, const void* q, const void* k,

@@ -5,6 +5,9 @@
 // heads and q-blocks; xattn_bsa.py select_blocks Step 6 aggregates only the
 // history blocks and then adds the first and last one.  One CTA per
 // (b, history CPU block) ORs the Hq * nqb * (cpu_block_tokens/128) bytes.
+// cpu_block_mask_kernel expands kept CPU blocks back into the BSA block mask
+// of the pages' offload attention (xattn_bsa.py compute_chunked_prefill:
+// history dense over the selected CPU blocks, current chunk dense causal).
 #include "common.cuh"
 #include "launchers.h"
 
@@ -30,7 +33,34 @@ __global__ void __launch_bounds__(256) map_kernel(
   }
 }
 
+// Block mask of the pages' offload attention: key block kb of the history is
+// visible to every head and q-block iff its CPU block is kept; the current
+// chunk's blocks are visible causally (kb <= diagonal).
+__global__ void __launch_bounds__(256) cpu_block_mask_kernel(
+    const uint8_t* __restrict__ keep, int Hq, int nqb, int nkb, int cur, int per, int n_cpu,
+    uint8_t* __restrict__ mask) {
+  const int qb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int diag = cur + qb;
+  uint8_t* row = mask + (((long long)b * Hq + h) * nqb + qb) * nkb;
+  for (int kb = threadIdx.x; kb < nkb; kb += blockDim.x) {
+    uint8_t m;
+    if (kb < cur) m = keep[(long long)b * n_cpu + kb / per] ? 1 : 0;
+    else m = kb <= diag ? 1 : 0;
+    row[kb] = m;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_cpu_block_mask(const Problem& p, const uint8_t* keep, int cpu_block_tokens,
+                                  uint8_t* mask, cudaStream_t st) {
+  const int per = cpu_block_tokens / kBlock;
+  const int n_cpu = p.q_start_pos / cpu_block_tokens;
+  dim3 grid(p.nqb, p.Hq, p.B);
+  cpu_block_mask_kernel<<<grid, 256, 0, st>>>(keep, p.Hq, p.nqb, p.nkb, p.q_start_pos / kBlock,
+                                               per, n_cpu, mask);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_map(const Problem& p, const uint8_t* mask, int cpu_block_tokens,
                        int flags, uint8_t* keep, cudaStream_t st) {

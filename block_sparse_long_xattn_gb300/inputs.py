@@ -124,6 +124,10 @@ CONFIGS = {
     "llama8b-128k-chunk4096": dict(B=1, Hq=32, Hkv=8, d=128, Lk=131072,
                                    q_start_pos=126976, alpha=3.0, n_hot=64,
                                    dtype="bf16", stride=16, threshold=0.9),
+    # GPU-only prefill of a whole 32K sequence (q_start_pos 0, one chunk)
+    "llama8b-32k-prefill": dict(B=1, Hq=32, Hkv=8, d=128, Lk=32768, q_start_pos=0,
+                                alpha=3.0, n_hot=16, dtype="bf16", stride=8,
+                                threshold=0.9),
     # a whole 64K sequence processed as 16 chunks of 4096
     "llama8b-64k-chunked": dict(B=1, Hq=32, Hkv=8, d=128, Lk=65536,
                                 q_start_pos=0, alpha=3.0, n_hot=32,

@@ -161,6 +161,21 @@ int bsx_bsa_prefill(bsx_shape s, const void* q, const void* k, const void* v,
                     void* stream);
 
 /*
+ * One chunk of XAttention prefill with the KV resident on the device:
+ * bsx_xattn_estimate followed by bsx_bsa_prefill over every key block
+ * [0, Lk/128) in one launch.  By the merge identity this equals attending to
+ * the history and the current chunk separately and merging them by LSE (the
+ * structure of xattn_bsa.py compute_chunked_prefill), without the second
+ * launch and the merge.  Outputs: mask (as bsx_xattn_estimate), o, lse (as
+ * bsx_bsa_prefill).  Arguments are validated before anything is enqueued;
+ * workspace as for bsx_xattn_estimate.
+ */
+int bsx_chunk_prefill(bsx_shape s, const void* q, const void* k, const void* v,
+                      int q_len, int q_start_pos, int stride, float threshold,
+                      uint8_t* mask, void* o, float* lse, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/*
  * LSE merge of two partial attentions over disjoint key sets, in place into
  * (o1, lse1).
  *
@@ -192,6 +207,25 @@ int bsx_merge_attn(bsx_shape s, int q_len, void* o1, float* lse1,
 int bsx_map_mask_to_cpu_blocks(bsx_shape s, const uint8_t* mask, int q_len,
                                int q_start_pos, int cpu_block_tokens,
                                int flags, uint8_t* keep, void* stream);
+
+/*
+ * Block mask of the pages' CPU-offload attention, from CPU-block keep flags.
+ *
+ * nano-vllm xattn_bsa.py compute_chunked_prefill attends, for every head and
+ * query, densely to all keys of the selected CPU blocks of the history (each
+ * through flash_attn_with_lse without causal masking, merged by LSE) and
+ * causally to the current chunk; select_blocks Step 6 picks the CPU blocks
+ * (bsx_map_mask_to_cpu_blocks with BSX_FORCE_FIRST_LAST).  This call writes
+ * the BSA block mask that makes bsx_bsa_prefill compute exactly that:
+ *   mask[b,h,qb,kb] = keep[b, kb*128 / cpu_block_tokens]   kb < q_start_pos/128
+ *                   = (kb <= q_start_pos/128 + qb)          otherwise.
+ * keep (in, device) uint8 [B, q_start_pos / cpu_block_tokens] (may be NULL
+ * when q_start_pos is 0); mask (out, device) uint8 [B, Hq, q_len/128,
+ * Lk/128], every byte written.
+ */
+int bsx_cpu_block_mask(bsx_shape s, const uint8_t* keep, int q_len,
+                       int q_start_pos, int cpu_block_tokens, uint8_t* mask,
+                       void* stream);
 
 /*
  * Read and clear the device error word of the current device.  Waits for

@@ -393,3 +393,104 @@ def chunk_step(q: np.ndarray, k: np.ndarray, v: np.ndarray, q_start_pos: int,
     o, lse = merge_attn(o_h, lse_h, o_c, lse_c)
     keep = map_mask_to_cpu_blocks(est.mask, q_start_pos, cpu_block_tokens)
     return est, o, lse, keep
+
+
+# --------------------------------------------------------------------------- #
+# The pages' CPU-offload attention (history dense over selected CPU blocks)    #
+# --------------------------------------------------------------------------- #
+def _dense_attention(qh: np.ndarray, kh: np.ndarray, vh: np.ndarray,
+                     allowed: np.ndarray):
+    """softmax(q k^T / sqrt(d)) v over the allowed (query, key) pairs, with
+    the natural-log LSE; rows without an allowed key get O = 0, LSE = -inf."""
+    d = qh.shape[-1]
+    s = np.where(allowed, (qh @ kh.T) / math.sqrt(d), -np.inf)
+    m = s.max(axis=1, keepdims=True)
+    has = np.isfinite(m[:, 0])
+    m_safe = np.where(has[:, None], m, 0.0)
+    e = np.where(allowed, np.exp(s - m_safe), 0.0)
+    l = e.sum(axis=1)
+    o = np.zeros((qh.shape[0], vh.shape[1]))
+    o[has] = (e[has] @ vh) / l[has, None]
+    lse = np.where(has, m_safe[:, 0] + np.log(np.where(has, l, 1.0)), -np.inf)
+    return o, lse
+
+
+def offload_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, keep: np.ndarray,
+                      q_start_pos: int, cpu_block_tokens: int = 1024):
+    """Attention as nano-vllm's offload path computes it.
+
+    [policy] compute_chunked_prefill: for every selected CPU block, in order,
+    flash_attn_with_lse(q, k_block, v_block, causal=False) merged into the
+    running (O, LSE) with merge_attention_outputs; then the current chunk with
+    causal=True, merged last.  keep: uint8 [B, q_start_pos/cpu_block_tokens].
+    Returns o [B, Lq, Hq, d], lse [B, Hq, Lq].
+    """
+    B, Lq, Hq, d = q.shape
+    _, Lk, Hkv, _ = k.shape
+    G = Hq // Hkv
+    o_all = np.zeros((B, Lq, Hq, d))
+    lse_all = np.full((B, Hq, Lq), -np.inf)
+    for b in range(B):
+        blocks = [c for c in range(keep.shape[1]) if keep[b, c]]
+        for h in range(Hq):
+            qh = np.asarray(q[b, :, h, :], np.float64)
+            kh = np.asarray(k[b, :, h // G, :], np.float64)
+            vh = np.asarray(v[b, :, h // G, :], np.float64)
+            o_acc = None
+            lse_acc = None
+            for c in blocks:
+                keys = slice(c * cpu_block_tokens, (c + 1) * cpu_block_tokens)
+                allowed = np.ones((Lq, cpu_block_tokens), bool)
+                o_c, lse_c = _dense_attention(qh, kh[keys], vh[keys], allowed)
+                if o_acc is None:
+                    o_acc, lse_acc = o_c, lse_c
+                else:
+                    o_m, lse_m = merge_attn(o_acc[None, :, None, :], lse_acc[None, None, :],
+                                            o_c[None, :, None, :], lse_c[None, None, :])
+                    o_acc, lse_acc = o_m[0, :, 0, :], lse_m[0, 0]
+            cur = slice(q_start_pos, Lk)
+            rows = np.arange(Lq)[:, None]
+            allowed = np.arange(Lq)[None, :] <= rows        # j - P <= i
+            o_c, lse_c = _dense_attention(qh, kh[cur], vh[cur], allowed)
+            if o_acc is not None:
+                o_m, lse_m = merge_attn(o_acc[None, :, None, :], lse_acc[None, None, :],
+                                        o_c[None, :, None, :], lse_c[None, None, :])
+                o_c, lse_c = o_m[0, :, 0, :], lse_m[0, 0]
+            o_all[b, :, h, :] = o_c
+            lse_all[b, h] = lse_c
+    return o_all, lse_all
+
+
+def offload_block_mask(keep: np.ndarray, Hq: int, q_len: int, q_start_pos: int,
+                       cpu_block_tokens: int = 1024) -> np.ndarray:
+    """The 128-token block mask under which block-sparse attention equals
+    offload_attention: history block kb visible iff its CPU block is kept
+    (every head, every q-block); current-chunk block kb visible iff it is at
+    or before the q-block's diagonal.  Returns bool [B, Hq, q_len/128, Lk/128].
+    """
+    B = keep.shape[0]
+    nqb = q_len // BSA_BLOCK
+    cur = q_start_pos // BSA_BLOCK
+    nkb = cur + nqb
+    per = cpu_block_tokens // BSA_BLOCK
+    mask = np.zeros((B, Hq, nqb, nkb), bool)
+    for b in range(B):
+        for qb in range(nqb):
+            for kb in range(nkb):
+                if kb < cur:
+                    mask[b, :, qb, kb] = bool(keep[b, kb // per])
+                else:
+                    mask[b, :, qb, kb] = kb <= cur + qb
+    return mask
+
+
+def chunk_step_offload(q: np.ndarray, k: np.ndarray, v: np.ndarray, q_start_pos: int,
+                       stride: int, threshold: float, cpu_block_tokens: int = 1024):
+    """[policy] select_blocks (estimate, then CPU blocks kept if any of their
+    BSA blocks is selected, first and last always added) followed by
+    compute_chunked_prefill (offload_attention)."""
+    est = xattn_estimate(q, k, q_start_pos, stride, threshold)
+    keep = map_mask_to_cpu_blocks(est.mask, q_start_pos, cpu_block_tokens,
+                                  force_first_last=True)
+    o, lse = offload_attention(q, k, v, keep, q_start_pos, cpu_block_tokens)
+    return est, keep, o, lse

@@ -177,3 +177,29 @@ def test_density_sweep_32k(alpha):
             for qb in range(m.shape[2]):
                 assert m[:, :, qb, :cur + qb + 1].all() and not m[:, :, qb, cur + qb + 1:].any()
             _check_rows(w, np.ones_like(est.mask), o, lse, P, heads=[5])
+
+
+def test_llama8b_32k_whole_sequence_prefill():
+    """GPU-only prefill of a whole 32K sequence (q_start_pos 0): all 32 heads
+    run on the GPU; the oracle checks the mask of one GQA group (heads 0-3,
+    kv-head 0) in full and O / LSE on sampled rows of heads 0 and 3."""
+    c, S, tau, _ = _cfg("llama8b-32k-prefill")
+    w = make_workload(seed=0, **c)
+    q, k, v = (to_dev(x, w.dtype) for x in (w.q, w.k, w.v))
+    Lk = w.k.shape[1]
+    A = torch.empty((1, 32, Lk // 128, Lk // 128), dtype=torch.float32, device="cuda")
+    mask = bsx_xattn_estimate(q, k, 0, S, tau, block_sums=A)
+    wq, wk, wv = w.q[:, :, :4], w.k[:, :, :1], w.v[:, :, :1]
+    est = O.xattn_estimate(wq, wk, 0, S, tau)
+    A_g = A[:, :4].cpu().numpy()
+    check_block_sums(A_g, est.block_sums, S)
+    _, n_near, n_tie = check_mask(mask[:, :4].cpu().numpy(), est, tau, 0, A_g)
+    print(f"32k prefill: {n_near} near-threshold rows, {n_tie} near-tie swaps of 1024; "
+          f"density {_density(est.mask, 0):.4f}")
+    m = mask.clone()
+    m[:, :4] = torch.from_numpy(est.mask.astype(np.uint8)).cuda()
+    o, lse = bsx_bsa_prefill(q, k, v, m, 0)
+    torch.cuda.synchronize()
+    ch = SimpleNamespace(q=wq, k=wk, v=wv, dtype=w.dtype)
+    _check_rows(ch, est.mask, o[:, :, :4].contiguous(), lse[:, :4].contiguous(), 0, heads=[0, 3])
+    assert bsx_last_error() == 0

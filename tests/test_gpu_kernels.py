@@ -12,8 +12,8 @@ import pytest
 import torch
 
 from block_sparse_long_xattn_gb300 import (
-    bsx_bsa_prefill, bsx_last_error, bsx_map_mask_to_cpu_blocks, bsx_merge_attn,
-    bsx_xattn_estimate)
+    bsx_bsa_prefill, bsx_chunk_prefill, bsx_cpu_block_mask, bsx_last_error,
+    bsx_map_mask_to_cpu_blocks, bsx_merge_attn, bsx_xattn_estimate)
 from block_sparse_long_xattn_gb300.inputs import make_workload, random_block_mask
 from oracle import xattn_oracle as O
 from tests.helpers import LSE_TOL, O_TOL, check_block_sums, check_mask, to_dev
@@ -182,3 +182,69 @@ def test_bsa_running_max_grows_every_block(d):
     o_ref, lse_ref = O.bsa_prefill(q32, k32, v32, mask, P, 0, Lk // 128)
     assert np.abs(o.float().cpu().numpy() - o_ref).max() <= O_TOL["bf16"]
     assert np.abs(lse.cpu().numpy() - lse_ref).max() <= LSE_TOL * max(1.0, np.abs(lse_ref).max() / 100)
+
+
+def test_fused_chunk_prefill_equals_split_and_oracle():
+    """bsx_chunk_prefill (estimate + BSA over every key block, no merge) equals
+    the oracle's estimate + attention over all columns (rows of near-threshold
+    masks excepted: there BSA runs on the oracle's mask in a second call)."""
+    P, S, tau = 768, 8, 0.9
+    w = make_workload(seed=91, B=1, Hq=8, Hkv=2, d=128, Lk=P + 512, q_start_pos=P,
+                      alpha=3.0, n_hot=2, dtype="bf16")
+    q, k, v = (to_dev(x, "bf16") for x in (w.q, w.k, w.v))
+    mask, o, lse = bsx_chunk_prefill(q, k, v, P, S, tau)
+    torch.cuda.synchronize()
+    est = O.xattn_estimate(w.q, w.k, P, S, tau)
+    m_g = mask.cpu().numpy()
+    if np.array_equal(m_g.astype(bool), est.mask):
+        o_ref, lse_ref = O.bsa_prefill(w.q, w.k, w.v, est.mask, P, 0, (P + 512) // 128)
+    else:   # a near-threshold row differs: compare attention on the GPU's own mask
+        o_ref, lse_ref = O.bsa_prefill(w.q, w.k, w.v, m_g, P, 0, (P + 512) // 128)
+    assert np.abs(o.float().cpu().numpy() - o_ref).max() <= O_TOL["bf16"]
+    assert np.abs(lse.cpu().numpy() - lse_ref).max() <= LSE_TOL
+
+
+def test_offload_semantics_chunk_step():
+    """The pages' offload attention: CPU blocks kept if any of their BSA blocks
+    is selected (first and last forced), history dense over the kept CPU
+    blocks, current chunk dense causal, merged by LSE."""
+    P, S, tau, cpu = 1024, 8, 0.9, 256
+    Lq = 512
+    w = make_workload(seed=88, B=1, Hq=8, Hkv=2, d=128, Lk=P + Lq, q_start_pos=P,
+                      alpha=3.0, n_hot=2, dtype="bf16")
+    est, keep_ref, o_ref, lse_ref = O.chunk_step_offload(w.q, w.k, w.v, P, S, tau, cpu)
+    q, k, v = (to_dev(x, "bf16") for x in (w.q, w.k, w.v))
+    mask_o = torch.from_numpy(est.mask.astype(np.uint8)).cuda()
+    keep = bsx_map_mask_to_cpu_blocks(mask_o, P, cpu, True)
+    om = bsx_cpu_block_mask(keep, Lq, P, 8, cpu)
+    cur, nkb = P // 128, (P + Lq) // 128
+    oh, lh = bsx_bsa_prefill(q, k, v, om, P, 0, cur)
+    oc, lc = bsx_bsa_prefill(q, k, v, om, P, cur, nkb)
+    bsx_merge_attn(oh, lh, oc, lc)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(keep.cpu().numpy(), keep_ref)
+    np.testing.assert_array_equal(om.cpu().numpy().astype(bool),
+                                  O.offload_block_mask(keep_ref, 8, Lq, P, cpu))
+    assert np.abs(oh.float().cpu().numpy() - o_ref).max() <= O_TOL["bf16"]
+    assert np.abs(lh.cpu().numpy() - lse_ref).max() <= LSE_TOL
+
+
+@pytest.mark.parametrize("S,dt", [(8, "bf16"), (16, "bf16"), (8, "f32")])
+def test_whole_sequence_prefill(S, dt):
+    """GPU-only XAttention prefill of a whole sequence (q_start_pos 0): the
+    estimate over all rows and one BSA launch over every key block."""
+    Lk = 2048
+    w = make_workload(seed=7 + S, B=1, Hq=4, Hkv=2, d=128 if dt == "bf16" else 64, Lk=Lk,
+                      q_start_pos=0, alpha=3.0, n_hot=2, dtype=dt)
+    q, k, v = (to_dev(x, dt) for x in (w.q, w.k, w.v))
+    A = torch.empty((1, 4, Lk // 128, Lk // 128), dtype=torch.float32, device="cuda")
+    mask = bsx_xattn_estimate(q, k, 0, S, 0.9, block_sums=A)
+    est = O.xattn_estimate(w.q, w.k, 0, S, 0.9)
+    check_block_sums(A.cpu().numpy(), est.block_sums, S)
+    check_mask(mask.cpu().numpy(), est, 0.9, 0, A.cpu().numpy())
+    m = torch.from_numpy(est.mask.astype(np.uint8)).cuda()
+    o, lse = bsx_bsa_prefill(q, k, v, m, 0)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = O.bsa_prefill(w.q, w.k, w.v, est.mask, 0, 0, Lk // 128)
+    assert np.abs(o.float().cpu().numpy() - o_ref).max() <= O_TOL[dt]
+    assert np.abs(lse.cpu().numpy() - lse_ref).max() <= LSE_TOL

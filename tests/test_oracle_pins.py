@@ -337,3 +337,52 @@ def test_chunk_step_runs_and_merges():
     np.testing.assert_allclose(o, oa, rtol=1e-11, atol=1e-12)
     np.testing.assert_allclose(lse, la, rtol=1e-12, atol=1e-12)
     assert keep.shape == (1, P // 128)
+
+
+# ----------------------------------------------------------------------------
+# the pages' offload attention
+# ----------------------------------------------------------------------------
+def test_offload_attention_all_kept_is_dense_causal():
+    P, cpu = 512, 256
+    w = make_workload(seed=14, B=1, Hq=2, Hkv=1, d=16, Lk=P + 256, q_start_pos=P,
+                      alpha=2.0, n_hot=1, dtype="bf16")
+    keep = np.ones((1, P // cpu), np.uint8)
+    o, lse = O.offload_attention(w.q, w.k, w.v, keep, P, cpu)
+    Lq, Lk = 256, P + 256
+    allowed = np.tril(np.ones((Lq, Lk), bool), k=P)
+    for h in range(2):
+        o_ref, lse_ref = _torch_attention(w.q[0, :, h], w.k[0, :, 0], w.v[0, :, 0], allowed)
+        np.testing.assert_allclose(o[0, :, h], o_ref, rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(lse[0, h], lse_ref, rtol=1e-12, atol=1e-12)
+
+
+def test_offload_attention_equals_torch_on_kept_keys_and_bsa_with_its_mask():
+    P, cpu = 1024, 256
+    w = make_workload(seed=15, B=2, Hq=4, Hkv=2, d=16, Lk=P + 256, q_start_pos=P,
+                      alpha=2.0, n_hot=2, dtype="bf16")
+    keep = np.array([[1, 0, 0, 1], [0, 1, 1, 0]], np.uint8)
+    o, lse = O.offload_attention(w.q, w.k, w.v, keep, P, cpu)
+    Lq, Lk = 256, P + 256
+    for b in range(2):
+        allowed = np.zeros((Lq, Lk), bool)
+        for c in range(4):
+            if keep[b, c]:
+                allowed[:, c * cpu:(c + 1) * cpu] = True
+        allowed[:, P:] = np.tril(np.ones((Lq, Lq), bool))
+        for h in range(4):
+            o_ref, lse_ref = _torch_attention(w.q[b, :, h], w.k[b, :, h // 2], w.v[b, :, h // 2],
+                                              allowed)
+            np.testing.assert_allclose(o[b, :, h], o_ref, rtol=1e-10, atol=1e-12)
+            np.testing.assert_allclose(lse[b, h], lse_ref, rtol=1e-12, atol=1e-12)
+    mask = O.offload_block_mask(keep, 4, Lq, P, cpu)
+    o2, lse2 = O.bsa_prefill(w.q, w.k, w.v, mask, P, 0, Lk // 128)
+    np.testing.assert_allclose(o2, o, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(lse2, lse, rtol=1e-12, atol=1e-12)
+
+
+def test_offload_mask_small_example():
+    keep = np.array([[0, 1]], np.uint8)          # CPU blocks of 256 tokens: 2 BSA blocks each
+    m = O.offload_block_mask(keep, 1, 256, 512, 256)
+    # history blocks 0,1 (CPU block 0, dropped), 2,3 (kept); current blocks 4, 5 causal
+    assert m[0, 0, 0].tolist() == [False, False, True, True, True, False]
+    assert m[0, 0, 1].tolist() == [False, False, True, True, True, True]
