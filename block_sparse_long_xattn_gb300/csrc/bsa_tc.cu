@@ -8,11 +8,12 @@
 // One CTA per (128-row q-tile, q-head, batch); 10 warps with fixed roles:
 //   warp 0      TMA producer: Q once, then the K and V tiles of every selected
 //               key block, found by scanning the mask row, into a ring of
-//               tile-sized slots (K_0, V_0, K_1, V_1, ...).  A K slot is freed
-//               as soon as its S MMA completes and a V slot after its P V MMA,
-//               so loads run about two blocks ahead of the MMAs.
-//   warp 1      tcgen05 issuer: S(j) = Q K_j^T into TMEM buffer j % 2, and
-//               O_{j%2} += P(j) V_j with P(j) read from that same buffer.
+//               tile-sized slots in the order the MMAs consume them (K_0, K_1,
+//               V_0, K_2, V_1, ...).  A K slot is freed as soon as its S MMA
+//               completes and a V slot after its P V MMA.
+//   warp 1      tcgen05 issuer (one elected lane): S(j) = Q K_j^T into TMEM
+//               buffer j % 2, and O_{j%2} += P(j) V_j with P(j) read from that
+//               same buffer.
 //   warps 2..9  two softmax groups of four warps; group g takes the blocks
 //               j = g, g + 2, ... with one query row per thread (TMEM lane =
 //               row): read S, mask the diagonal block causally, online max
@@ -152,31 +153,40 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
       mbar_arrive_expect_tx(q_full, L::kTile);
       for (int r = 0; r < L::kRegions; ++r)
         tma_load_4d(sb + L::kQ + r * kRegion, &tm_q, q_full, r * 64, h, qb * 128, b);
-      // ring items in order K_0, V_0, K_1, V_1, ...; item i in slot i % kSlots
+      // Ring items in the order the tensor pipe consumes them,
+      //   K_0, K_1, V_0, K_2, V_1, ..., K_{n-1}, V_{n-2}, V_{n-1},
+      // item i in slot i % kSlots, so that the ring is a plain FIFO.
       int issued = 0;
       int kb = kb_begin - 1;
+      int kb_even = 0, kb_odd = 0;  // key blocks of the two most recent K items
       bool ok = true;
-      for (int j = 0; ok && j < n; ++j) {
-        do {
-          ++kb;
-        } while (kb < kb_last && !__ldg(mrow + kb));
-        if (kb >= kb_last) break;  // cannot happen: n counts these blocks
-        for (int kind = 0; kind < 2; ++kind) {
-          const int i = 2 * j + kind;
-          const int s = i % L::kSlots;
-          if (i >= L::kSlots &&
-              !mbar_wait(slot_empty(s), ((i / L::kSlots) - 1) & 1, abort_flag, err, kErrBsaTc,
-                         kSiteKvEmpty)) {
-            ok = false;
-            break;
-          }
-          const uint32_t dst = sb + L::kRing + s * L::kTile;
-          mbar_arrive_expect_tx(slot_full(s), L::kTile);
-          const CUtensorMap* map = kind == 0 ? &tm_k : &tm_v;
-          for (int r = 0; r < L::kRegions; ++r)
-            tma_load_4d(dst + r * kRegion, map, slot_full(s), r * 64, hk, kb * 128, b);
-          issued = i + 1;
+      for (int i = 0; ok && i < 2 * n; ++i) {
+        const bool is_k = i == 0 || ((i & 1) && (i + 1) / 2 < n);
+        int blk;
+        if (is_k) {
+          blk = (i + 1) / 2;
+          do {
+            ++kb;
+          } while (kb < kb_last && !__ldg(mrow + kb));
+          if (kb >= kb_last) break;  // cannot happen: n counts these blocks
+          if (blk & 1) kb_odd = kb; else kb_even = kb;
+        } else {
+          blk = i == 2 * n - 1 ? n - 1 : (i - 2) / 2;
         }
+        const int s = i % L::kSlots;
+        if (i >= L::kSlots &&
+            !mbar_wait(slot_empty(s), ((i / L::kSlots) - 1) & 1, abort_flag, err, kErrBsaTc,
+                       kSiteKvEmpty)) {
+          ok = false;
+          break;
+        }
+        const uint32_t dst = sb + L::kRing + s * L::kTile;
+        mbar_arrive_expect_tx(slot_full(s), L::kTile);
+        const CUtensorMap* map = is_k ? &tm_k : &tm_v;
+        for (int r = 0; r < L::kRegions; ++r)
+          tma_load_4d(dst + r * kRegion, map, slot_full(s), r * 64, hk,
+                      ((blk & 1) ? kb_odd : kb_even) * 128, b);
+        issued = i + 1;
       }
       // copies still in flight must land before the CTA may exit
       drain_wait(q_full, 0);
@@ -185,65 +195,79 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
     }
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ----------------------------
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0, 0);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);
-      bool ok = mbar_wait(q_full, 0, abort_flag, err, kErrBsaTc, kSiteQFull);
-      auto issue_pv = [&](int i) -> bool {
-        const int g = i & 1;
-        const int item = 2 * i + 1;  // V_i
-        const int s = item % L::kSlots;
-        if (!mbar_wait(p_full(g), (i >> 1) & 1, abort_flag, err, kErrBsaTc, kSitePFull))
-          return false;
-        if (!mbar_wait(slot_full(s), (item / L::kSlots) & 1, abort_flag, err, kErrBsaTc,
-                       kSiteKvFull))
-          return false;
-        tc_fence_after();
-        const uint32_t vbase = sb + L::kRing + s * L::kTile;
-        const uint32_t p_tmem = tmem_s0 + g * 128;  // P(i) overwrote S(i)
-        const uint32_t o_tmem = tmem_o0 + g * D;
+    // The whole warp runs the loop, so that slot addresses and descriptors are
+    // warp-uniform values formed once per block; one elected lane issues the
+    // tcgen05 instructions.  (A single-lane issuer sharing its scheduler with
+    // ALU-bound softmax warps could not keep the tensor pipe fed.)
+    constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0, 0);
+    constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);
+    const bool leader = elect_one_sync();
+    auto wait_all = [&](uint32_t bar, uint32_t parity, unsigned site) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, err, kErrBsaTc, site));
+    };
+    // ring position of K_m and V_j (the producer's order)
+    auto kpos = [&](int m) { return m == 0 ? 0 : 2 * m - 1; };
+    auto vpos = [&](int j) { return j == n - 1 ? 2 * n - 1 : 2 * j + 2; };
+    // The start-address field of a shared-memory descriptor is (address >> 4)
+    // in its low bits; shared addresses are below 256 KB, so adding
+    // (offset >> 4) to a descriptor moves it by `offset` bytes.
+    const uint64_t dq = smem_desc_sw128(sb + L::kQ, 16, 1024);
+    const uint64_t dk0 = smem_desc_sw128(sb + L::kRing, 16, 1024);
+    const uint64_t dv0 = smem_desc_sw128(sb + L::kRing, kRegion, 1024);
+    bool ok = wait_all(q_full, 0, kSiteQFull);
+    auto issue_pv = [&](int i) -> bool {
+      const int g = i & 1;
+      const int item = vpos(i);
+      const int s = item % L::kSlots;
+      if (!wait_all(p_full(g), (i >> 1) & 1, kSitePFull)) return false;
+      if (!wait_all(slot_full(s), (item / L::kSlots) & 1, kSiteKvFull)) return false;
+      tc_fence_after();
+      const uint64_t dv = dv0 + (uint64_t)((s * L::kTile) >> 4);
+      const uint32_t p_tmem = tmem_s0 + g * 128;  // P(i) overwrote S(i)
+      const uint32_t o_tmem = tmem_o0 + g * D;
+      if (leader) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {  // 16 keys per MMA: 8 TMEM columns of bf16 pairs
-          const uint64_t bd = smem_desc_sw128(vbase + k * 2048, kRegion, 1024);
-          mma_bf16_tmem_a(o_tmem, p_tmem + k * 8, bd, idesc_pv, (i >= 2 || k > 0) ? 1u : 0u);
-        }
+        for (int k = 0; k < 8; ++k)  // 16 keys per MMA: 8 TMEM columns of bf16 pairs
+          mma_bf16_tmem_a(o_tmem, p_tmem + k * 8, dv + (uint64_t)((k * 2048) >> 4), idesc_pv,
+                          (i >= 2 || k > 0) ? 1u : 0u);
         mma_commit(o_done(g));
         mma_commit(slot_empty(s));
-        return true;
-      };
-      int j = 0;
-      for (; ok && j < n; ++j) {
-        const int item = 2 * j;  // K_j
-        const int s = item % L::kSlots;
-        const int g = j & 1;
-        // S(j) overwrites P(j-2) in buffer g: P V(j-2) was issued in the
-        // previous iteration and the tensor pipe runs the MMAs in order
-        if (!mbar_wait(slot_full(s), (item / L::kSlots) & 1, abort_flag, err, kErrBsaTc,
-                       kSiteKvFull)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t kbase = sb + L::kRing + s * L::kTile;
+      }
+      __syncwarp();
+      return true;
+    };
+    for (int j = 0; ok && j < n; ++j) {
+      const int item = kpos(j);
+      const int s = item % L::kSlots;
+      const int g = j & 1;
+      // S(j) overwrites P(j-2) in buffer g: P V(j-2) was issued in the
+      // previous iteration and the tensor pipe runs the MMAs in order
+      if (!wait_all(slot_full(s), (item / L::kSlots) & 1, kSiteKvFull)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint64_t dk = dk0 + (uint64_t)((s * L::kTile) >> 4);
+      if (leader) {
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {  // 16 features per MMA
-          const uint32_t off = (k >> 2) * kRegion + (k & 3) * 32;
-          const uint64_t a = smem_desc_sw128(sb + L::kQ + off, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(kbase + off, 16, 1024);
-          mma_bf16(tmem_s0 + g * 128, a, bd, idesc_qk, k > 0 ? 1u : 0u);
+          const uint32_t off = ((k >> 2) * kRegion + (k & 3) * 32) >> 4;
+          mma_bf16(tmem_s0 + g * 128, dq + off, dk + off, idesc_qk, k > 0 ? 1u : 0u);
         }
         mma_commit(s_full(g));
         mma_commit(slot_empty(s));
-        if (j >= 1 && !issue_pv(j - 1)) {
-          ok = false;
-          break;
-        }
       }
-      if (ok) issue_pv(n - 1);
-      // every MMA issued above completes before TMEM is released
-      mma_commit(mma_final);
-      drain_wait(mma_final, 0);
+      __syncwarp();
+      if (j >= 1 && !issue_pv(j - 1)) {
+        ok = false;
+        break;
+      }
     }
+    if (ok) issue_pv(n - 1);
+    // every MMA issued above completes before TMEM is released
+    if (leader) mma_commit(mma_final);
+    __syncwarp();
+    drain_wait(mma_final, 0);
   } else {
     // ------------------------------ softmax -------------------------------
     const int quad = warp & 3;           // TMEM lane quadrant this warp may access

@@ -61,6 +61,16 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 // the device error word.
 // Wait for work this CTA already issued (copies or MMAs) even after an
 // abort; bounded so that a broken phase cannot hang the CTA.
+// True in exactly one lane of a converged warp.  Call it once and keep the
+// result when the same lane must issue a sequence of tcgen05 operations.
+__device__ __forceinline__ bool elect_one_sync() {
+  uint32_t pred;
+  asm volatile(
+      "{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity)) {
