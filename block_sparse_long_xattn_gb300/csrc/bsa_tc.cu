@@ -292,13 +292,20 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
         for (int c = 0; c < 128; ++c)
           if (c > row) x[c] = -INFINITY;
       }
+      // Row max in eight independent chains of three-input max.  The
+      // softmax warps share their schedulers with the MMA issuer and the
+      // producer, so every ALU instruction saved here is issue time given
+      // back to them; the exponent argument and the row sum below use the
+      // packed two-wide fp32 FMA/add for the same reason.
       float mx[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) mx[e] = -INFINITY;
+      for (int e = 0; e < 8; ++e) mx[e] = x[e];
 #pragma unroll
-      for (int c = 0; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], x[c]);
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * scale_log2;
+      for (int c = 8; c < 128; c += 16)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx[e] = fmax3(mx[e], x[c + e], x[c + 8 + e]);
+      const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                             fmaxf(mx[6], mx[7])) * scale_log2;
       const bool need = mt > m_run + kRescaleThreshold;
       float alpha = 1.f;
       if (need) {
@@ -307,17 +314,18 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
       }
       // P = exp2(x * scale - m) as bf16 pairs
       uint32_t pk[64];
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};
-      const float neg_m = -m_run;
+      float2 ps[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      const float2 sc2 = make_float2(scale_log2, scale_log2);
+      const float2 nm2 = make_float2(-m_run, -m_run);
 #pragma unroll
       for (int c = 0; c < 128; c += 2) {
-        const float p0 = fast_exp2(fmaf(x[c], scale_log2, neg_m));
-        const float p1 = fast_exp2(fmaf(x[c + 1], scale_log2, neg_m));
-        ps[(c >> 1) & 3] += p0 + p1;
-        __nv_bfloat162 t = __floats2bfloat162_rn(p0, p1);
-        pk[c >> 1] = *reinterpret_cast<uint32_t*>(&t);
+        const float2 t = __ffma2_rn(make_float2(x[c], x[c + 1]), sc2, nm2);
+        const float2 p = make_float2(fast_exp2(t.x), fast_exp2(t.y));
+        ps[(c >> 1) & 1] = __fadd2_rn(ps[(c >> 1) & 1], p);
+        __nv_bfloat162 b2 = __floats2bfloat162_rn(p.x, p.y);
+        pk[c >> 1] = *reinterpret_cast<uint32_t*>(&b2);
       }
-      l_run = l_run * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
+      l_run = l_run * alpha + ((ps[0].x + ps[0].y) + (ps[1].x + ps[1].y));
       // O_g is rescaled between P V(j-2) and P V(j).  P V(j-2) is complete:
       // the tensor pipe ran it before S(j), which we have read.
       if (j >= 2 && __any_sync(0xffffffffu, need)) {
