@@ -196,14 +196,20 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ----------------------------
     // The whole warp runs the loop, so that slot addresses and descriptors are
-    // warp-uniform values formed once per block; one elected lane issues the
-    // tcgen05 instructions.  (A single-lane issuer sharing its scheduler with
-    // ALU-bound softmax warps could not keep the tensor pipe fed.)
+    // warp-uniform values; one elected lane issues the tcgen05 instructions.
+    // (A single-lane issuer sharing its scheduler with ALU-bound softmax warps
+    // cannot keep the tensor pipe fed.)  The tensor pipe accepts only a few
+    // MMAs ahead, so the work between two batches is kept small: the order is
+    //   S(0), S(1), [P V(0), S(2)], [P V(1), S(3)], ..., [P V(n-1)]
+    // and each bracketed pair follows one group of waits (P(j), V_j, K_{j+2}).
+    // Every lane keeps its own wait result and runs the same number of
+    // iterations and __syncwarp()s; only the issuing lane's result decides
+    // whether it issues, so a timed-out wait needs no warp vote.
     constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0, 0);
     constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);
     const bool leader = elect_one_sync();
-    auto wait_all = [&](uint32_t bar, uint32_t parity, unsigned site) -> bool {
-      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, err, kErrBsaTc, site));
+    auto wait = [&](bool ok, uint32_t bar, uint32_t parity, unsigned site) -> bool {
+      return ok && mbar_wait(bar, parity, abort_flag, err, kErrBsaTc, site);
     };
     // ring position of K_m and V_j (the producer's order)
     auto kpos = [&](int m) { return m == 0 ? 0 : 2 * m - 1; };
@@ -214,56 +220,64 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
     const uint64_t dq = smem_desc_sw128(sb + L::kQ, 16, 1024);
     const uint64_t dk0 = smem_desc_sw128(sb + L::kRing, 16, 1024);
     const uint64_t dv0 = smem_desc_sw128(sb + L::kRing, kRegion, 1024);
-    bool ok = wait_all(q_full, 0, kSiteQFull);
-    auto issue_pv = [&](int i) -> bool {
-      const int g = i & 1;
-      const int item = vpos(i);
-      const int s = item % L::kSlots;
-      if (!wait_all(p_full(g), (i >> 1) & 1, kSitePFull)) return false;
-      if (!wait_all(slot_full(s), (item / L::kSlots) & 1, kSiteKvFull)) return false;
+    // S(m) = Q K_m^T into TMEM buffer m % 2 (K_m already waited for)
+    auto issue_s = [&](int m) {
+      const int s = kpos(m) % L::kSlots;
+      const uint64_t dk = dk0 + (uint64_t)((s * L::kTile) >> 4);
+      const uint32_t d_tmem = tmem_s0 + (m & 1) * 128;
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k) {  // 16 features per MMA
+        const uint32_t off = ((k >> 2) * kRegion + (k & 3) * 32) >> 4;
+        mma_bf16(d_tmem, dq + off, dk + off, idesc_qk, k > 0 ? 1u : 0u);
+      }
+      mma_commit(s_full(m & 1));
+      mma_commit(slot_empty(s));
+    };
+    bool ok = wait(true, q_full, 0, kSiteQFull);
+    for (int m = 0; m < 2 && m < n; ++m) {
+      ok = wait(ok, slot_full(kpos(m) % L::kSlots), (kpos(m) / L::kSlots) & 1, kSiteKvFull);
       tc_fence_after();
-      const uint64_t dv = dv0 + (uint64_t)((s * L::kTile) >> 4);
-      const uint32_t p_tmem = tmem_s0 + g * 128;  // P(i) overwrote S(i)
-      const uint32_t o_tmem = tmem_o0 + g * D;
-      if (leader) {
+      if (leader && ok) issue_s(m);
+      __syncwarp();
+    }
+    for (int j = 0; j < n; ++j) {
+      const int g = j & 1;
+      const int iv = vpos(j), sv = iv % L::kSlots;
+      const bool next_s = j + 2 < n;
+      const int ik = kpos(j + 2), sk = ik % L::kSlots;
+      // the three probes are issued back to back so that their latencies
+      // overlap; the bounded waits run only if one of them found its phase
+      // still open
+      bool ready = false;
+      if (ok) {
+        const bool r0 = mbar_try_wait(p_full(g), (j >> 1) & 1);
+        const bool r1 = mbar_try_wait(slot_full(sv), (iv / L::kSlots) & 1);
+        const bool r2 = !next_s || mbar_try_wait(slot_full(sk), (ik / L::kSlots) & 1);
+        ready = r0 & r1 & r2;
+      }
+      if (!ready) {
+        ok = wait(ok, p_full(g), (j >> 1) & 1, kSitePFull);
+        ok = wait(ok, slot_full(sv), (iv / L::kSlots) & 1, kSiteKvFull);
+        if (next_s) ok = wait(ok, slot_full(sk), (ik / L::kSlots) & 1, kSiteKvFull);
+      }
+      tc_fence_after();
+      if (leader && ok) {
+        // O_g += P(j) V_j with P(j) read from TMEM buffer g (it overwrote S(j))
+        const uint64_t dv = dv0 + (uint64_t)((sv * L::kTile) >> 4);
+        const uint32_t p_tmem = tmem_s0 + g * 128;
+        const uint32_t o_tmem = tmem_o0 + g * D;
 #pragma unroll
         for (int k = 0; k < 8; ++k)  // 16 keys per MMA: 8 TMEM columns of bf16 pairs
           mma_bf16_tmem_a(o_tmem, p_tmem + k * 8, dv + (uint64_t)((k * 2048) >> 4), idesc_pv,
-                          (i >= 2 || k > 0) ? 1u : 0u);
+                          (j >= 2 || k > 0) ? 1u : 0u);
         mma_commit(o_done(g));
-        mma_commit(slot_empty(s));
+        mma_commit(slot_empty(sv));
+        // S(j+2) overwrites buffer g after P V(j) has read it: the tensor
+        // pipe runs the MMAs in issue order
+        if (next_s) issue_s(j + 2);
       }
       __syncwarp();
-      return true;
-    };
-    for (int j = 0; ok && j < n; ++j) {
-      const int item = kpos(j);
-      const int s = item % L::kSlots;
-      const int g = j & 1;
-      // S(j) overwrites P(j-2) in buffer g: P V(j-2) was issued in the
-      // previous iteration and the tensor pipe runs the MMAs in order
-      if (!wait_all(slot_full(s), (item / L::kSlots) & 1, kSiteKvFull)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint64_t dk = dk0 + (uint64_t)((s * L::kTile) >> 4);
-      if (leader) {
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {  // 16 features per MMA
-          const uint32_t off = ((k >> 2) * kRegion + (k & 3) * 32) >> 4;
-          mma_bf16(tmem_s0 + g * 128, dq + off, dk + off, idesc_qk, k > 0 ? 1u : 0u);
-        }
-        mma_commit(s_full(g));
-        mma_commit(slot_empty(s));
-      }
-      __syncwarp();
-      if (j >= 1 && !issue_pv(j - 1)) {
-        ok = false;
-        break;
-      }
     }
-    if (ok) issue_pv(n - 1);
     // every MMA issued above completes before TMEM is released
     if (leader) mma_commit(mma_final);
     __syncwarp();
