@@ -88,8 +88,11 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
   const uint32_t mma_final = bar0 + 8 * (kB2 + 6);
   const uint32_t xbar = bar0 + 8 * (kB2 + 7);                    // end-of-row merge
 
-  const int qb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int nqb = gridDim.x;
+  // heads vary fastest and query tiles run last-first: with causal masking
+  // the late tiles see the most key blocks, so the long CTAs start first
+  const int h = blockIdx.x, b = blockIdx.z;
+  const int nqb = gridDim.y;
+  const int qb = nqb - 1 - (int)blockIdx.y;
   const int nkb = Lk / kBlock;
   const int hk = h / (Hq / Hkv);
   const int diag = cur + qb;
@@ -448,7 +451,7 @@ cudaError_t launch_d(const Problem& p, const void* q, const void* k, const void*
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
-  dim3 grid(p.nqb, p.Hq, p.B);
+  dim3 grid(p.Hq, p.nqb, p.B);
   bsa_tc_kernel<D><<<grid, kThreads, smem, st>>>(
       mq, mk, mv, mask, p.q_len, p.Lk, p.Hq, p.Hkv, p.q_start_pos / kBlock, kb_begin, kb_end,
       scale_log2, static_cast<__nv_bfloat16*>(o), lse, err);

@@ -16,20 +16,29 @@ namespace {
 
 __global__ void __launch_bounds__(256) map_kernel(
     const uint8_t* __restrict__ mask, int Hq, int nqb, int nkb, int per,
-    int n_cpu, int force_first_last, uint8_t* __restrict__ keep) {
+    int n_cpu, int force_first_last, int words, uint8_t* __restrict__ keep) {
   const int c = blockIdx.x;
   const int b = blockIdx.y;
   const int pairs = Hq * nqb;
-  int any = 0;
-  for (int idx = threadIdx.x; idx < pairs * per; idx += blockDim.x) {
-    const int hq = idx / per;   // (h, qb) row
-    const int u = idx % per;
-    any |= mask[((long long)b * pairs + hq) * nkb + (long long)c * per + u];
+  const uint8_t* base = mask + (long long)b * pairs * nkb + (long long)c * per;
+  unsigned long long any = 0;
+  if (words) {
+    // the CPU block's bytes of every (h, qb) row are 8-byte aligned words
+    const int wpr = per >> 3;  // words per row
+    for (int idx = threadIdx.x; idx < pairs * wpr; idx += blockDim.x) {
+      const int hq = idx / wpr, w = idx - hq * wpr;
+      any |= __ldg(reinterpret_cast<const unsigned long long*>(base + (long long)hq * nkb) + w);
+    }
+  } else {
+    for (int idx = threadIdx.x; idx < pairs * per; idx += blockDim.x) {
+      const int hq = idx / per, u = idx - hq * per;
+      any |= base[(long long)hq * nkb + u];
+    }
   }
-  any = __syncthreads_or(any);
+  const int hit = __syncthreads_or(any != 0ull);
   if (threadIdx.x == 0) {
-    if (force_first_last && (c == 0 || c == n_cpu - 1)) any = 1;
-    keep[(long long)b * n_cpu + c] = any ? 1 : 0;
+    const bool k = hit || (force_first_last && (c == 0 || c == n_cpu - 1));
+    keep[(long long)b * n_cpu + c] = k ? 1 : 0;
   }
 }
 
@@ -68,8 +77,10 @@ cudaError_t launch_map(const Problem& p, const uint8_t* mask, int cpu_block_toke
   if (n_cpu == 0 || p.B == 0) return cudaSuccess;
   const int per = cpu_block_tokens / kBlock;
   dim3 grid(n_cpu, p.B);
+  // 8-byte loads when the mask, its rows and the CPU blocks are 8-byte aligned
+  const int words = (reinterpret_cast<uintptr_t>(mask) % 8 == 0) && p.nkb % 8 == 0 && per % 8 == 0;
   map_kernel<<<grid, 256, 0, st>>>(mask, p.Hq, p.nqb, p.nkb, per, n_cpu,
-                                    (flags & 1) ? 1 : 0, keep);
+                                    (flags & 1) ? 1 : 0, words, keep);
   return cudaGetLastError();
 }
 

@@ -14,7 +14,9 @@
 // threshold * sum(A).  The crossing block is kept (the section's worked
 // example); threshold >= 1 keeps every causal block.  One CTA per (b, h, qb):
 // a bitonic sort of packed (A, kb) keys in shared memory, then a block-wide
-// exclusive scan of the sorted masses.
+// exclusive scan of the sorted masses.  Rows of at most 1024 key blocks take
+// select_warp_kernel instead: one warp per (b, h, qb), everything in
+// registers and warp shuffles.
 #include "common.cuh"
 #include "launchers.h"
 
@@ -226,9 +228,197 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
   }
 }
 
+// ---------------------------------------------------------------------------
+// The same computation with one warp per (b, h, qb) row, for rows of at most
+// 32 * KPL key blocks.  Element i of the row (key block i before sorting,
+// sorted position i after) lives in lane i % 32, register i / 32, so every
+// compare-exchange of the bitonic network is either a warp shuffle (partner
+// distance below 32) or a swap between two registers of one lane; no block
+// barrier is needed anywhere.
+constexpr int kWarpsPerCta = 4;
+
+template <int RB, int KPL>
+__global__ void __launch_bounds__(32 * kWarpsPerCta, KPL <= 8 ? 4 : 2) select_warp_kernel(
+    const float* __restrict__ lse_part, int Hq, int nqb, int nkb, int R, int cur,
+    float threshold, uint8_t* __restrict__ mask, float* __restrict__ block_sums) {
+  constexpr int N = 32 * KPL;  // padded row length (a power of two)
+  __shared__ __align__(16) uint8_t sel_all[kWarpsPerCta][N];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int row_id = blockIdx.x * kWarpsPerCta + wid;  // (h, qb) flattened
+  if (row_id >= Hq * nqb) return;
+  const int qb = row_id % nqb;
+  const int h = row_id / nqb;
+  const int b = blockIdx.y;
+  uint8_t* sel = sel_all[wid];
+  const int diag = cur + qb;
+  const int ncausal = diag + 1;
+  const float* base = lse_part + ((long long)(b * Hq + h) * nkb) * R + qb * RB;
+
+  // ---- row maxima, then row sums -> row LSE ----
+  float acc[RB];
+#pragma unroll
+  for (int i = 0; i < RB; ++i) acc[i] = -INFINITY;
+  for (int kb = lane; kb < ncausal; kb += 32) {
+    const float4* q = reinterpret_cast<const float4*>(base + (long long)kb * R);
+#pragma unroll
+    for (int c = 0; c < RB / 4; ++c) {
+      const float4 v = __ldg(q + c);
+      acc[4 * c + 0] = fmaxf(acc[4 * c + 0], v.x);
+      acc[4 * c + 1] = fmaxf(acc[4 * c + 1], v.y);
+      acc[4 * c + 2] = fmaxf(acc[4 * c + 2], v.z);
+      acc[4 * c + 3] = fmaxf(acc[4 * c + 3], v.w);
+    }
+  }
+  float rmax[RB];
+#pragma unroll
+  for (int i = 0; i < RB; ++i) {
+    rmax[i] = warp_max(acc[i]);
+    acc[i] = 0.f;
+  }
+  for (int kb = lane; kb < ncausal; kb += 32) {
+    const float4* q = reinterpret_cast<const float4*>(base + (long long)kb * R);
+#pragma unroll
+    for (int c = 0; c < RB / 4; ++c) {
+      const float4 v = __ldg(q + c);
+      acc[4 * c + 0] += __expf(v.x - rmax[4 * c + 0]);
+      acc[4 * c + 1] += __expf(v.y - rmax[4 * c + 1]);
+      acc[4 * c + 2] += __expf(v.z - rmax[4 * c + 2]);
+      acc[4 * c + 3] += __expf(v.w - rmax[4 * c + 3]);
+    }
+  }
+  float rlse[RB];
+#pragma unroll
+  for (int i = 0; i < RB; ++i) rlse[i] = rmax[i] + logf(warp_sum(acc[i]));
+
+  // ---- block sums A[kb], kb = t * 32 + lane ----
+  float a[KPL];
+  float part = 0.f;
+#pragma unroll
+  for (int t = 0; t < KPL; ++t) {
+    const int kb = t * 32 + lane;
+    float v = 0.f;
+    if (kb < ncausal) {
+      const float4* q = reinterpret_cast<const float4*>(base + (long long)kb * R);
+#pragma unroll
+      for (int c = 0; c < RB / 4; ++c) {
+        const float4 w = __ldg(q + c);
+        v += __expf(w.x - rlse[4 * c + 0]) + __expf(w.y - rlse[4 * c + 1]) +
+             __expf(w.z - rlse[4 * c + 2]) + __expf(w.w - rlse[4 * c + 3]);
+      }
+    }
+    a[t] = v;
+    part += v;
+    if (block_sums && kb < nkb) block_sums[(((long long)b * Hq + h) * nqb + qb) * nkb + kb] = v;
+  }
+  const float total = warp_sum(part);
+
+  uint8_t* mrow = mask + (((long long)b * Hq + h) * nqb + qb) * nkb;
+  if (threshold >= 1.0f) {
+    for (int kb = lane; kb < nkb; kb += 32) mrow[kb] = kb < ncausal ? 1 : 0;
+    return;
+  }
+
+  // ---- bitonic sort of (A, kb) keys, descending (ties: lower kb first) ----
+  unsigned long long key[KPL];
+#pragma unroll
+  for (int t = 0; t < KPL; ++t) {
+    const int kb = t * 32 + lane;
+    key[t] = (kb < ncausal && kb != 0 && kb != diag)
+                 ? ((unsigned long long)__float_as_uint(a[t]) << 32) |
+                       (unsigned long long)(0xFFFFFFFFu - (unsigned)kb)
+                 : 0ull;
+  }
+#pragma unroll
+  for (int k = 2; k <= N; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (j >= 32) {
+        const int tj = j >> 5;
+#pragma unroll
+        for (int t = 0; t < KPL; ++t) {
+          if ((t & tj) == 0) {
+            const int i = t * 32 + lane;  // lower index of the pair
+            const bool desc = (i & k) == 0;
+            const unsigned long long x = key[t], y = key[t | tj];
+            const bool swap = desc ? (x < y) : (x > y);
+            key[t] = swap ? y : x;
+            key[t | tj] = swap ? x : y;
+          }
+        }
+      } else {
+        const bool lower = (lane & j) == 0;
+#pragma unroll
+        for (int t = 0; t < KPL; ++t) {
+          const int i = t * 32 + lane;
+          const bool desc = (i & k) == 0;
+          const unsigned long long y = __shfl_xor_sync(0xffffffffu, key[t], j);
+          const unsigned long long x = key[t];
+          // the lower index keeps the larger key in a descending run
+          const bool take_max = (lower == desc);
+          key[t] = take_max ? (x > y ? x : y) : (x < y ? x : y);
+        }
+      }
+    }
+  }
+
+  // ---- exclusive scan of the sorted masses; keep while below the target ----
+  const int nforced = diag == 0 ? 1 : 2;
+  const int ncand = ncausal - nforced;
+  // A of the diagonal block, recomputed by every lane the way its owner did
+  // (selecting it from the owner's registers would need a runtime index)
+  float a_diag = 0.f;
+  {
+    const float4* q = reinterpret_cast<const float4*>(base + (long long)diag * R);
+#pragma unroll
+    for (int c = 0; c < RB / 4; ++c) {
+      const float4 w = __ldg(q + c);
+      a_diag += __expf(w.x - rlse[4 * c + 0]) + __expf(w.y - rlse[4 * c + 1]) +
+                __expf(w.z - rlse[4 * c + 2]) + __expf(w.w - rlse[4 * c + 3]);
+    }
+  }
+  const float forced_mass = __shfl_sync(0xffffffffu, a[0], 0) + (diag != 0 ? a_diag : 0.f);
+  const float target = threshold * total;
+  for (int kb = lane; kb < N; kb += 32) sel[kb] = 0;
+  __syncwarp();
+  float carry = 0.f;  // mass of the sorted positions before register t
+#pragma unroll
+  for (int t = 0; t < KPL; ++t) {
+    const int i = t * 32 + lane;
+    const float v = i < ncand ? __uint_as_float((unsigned)(key[t] >> 32)) : 0.f;
+    float incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    const float excl = carry + incl - v;
+    if (i < ncand && forced_mass + excl < target)
+      sel[0xFFFFFFFFu - (unsigned)(key[t] & 0xFFFFFFFFull)] = 1;
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  __syncwarp();
+  for (int kb = lane; kb < nkb; kb += 32) {
+    uint8_t m = sel[kb];
+    if (kb == 0 || kb == diag) m = 1;
+    mrow[kb] = kb < ncausal ? m : 0;
+  }
+}
+
 template <int RB>
 cudaError_t launch_rb(const Problem& p, float threshold, const float* lse_part,
                       uint8_t* mask, float* block_sums, cudaStream_t st) {
+  const int R = p.q_len / (kBlock / RB);
+  const int rows = p.B * p.Hq * p.nqb;
+  if (p.nkb <= 1024) {
+    dim3 grid((rows / p.B + kWarpsPerCta - 1) / kWarpsPerCta, p.B);
+    if (p.nkb <= 256)
+      select_warp_kernel<RB, 8><<<grid, 32 * kWarpsPerCta, 0, st>>>(
+          lse_part, p.Hq, p.nqb, p.nkb, R, p.q_start_pos / kBlock, threshold, mask, block_sums);
+    else
+      select_warp_kernel<RB, 32><<<grid, 32 * kWarpsPerCta, 0, st>>>(
+          lse_part, p.Hq, p.nqb, p.nkb, R, p.q_start_pos / kBlock, threshold, mask, block_sums);
+    return cudaGetLastError();
+  }
   int n_pad = 1;
   while (n_pad < p.nkb) n_pad <<= 1;
   const size_t smem = (size_t)n_pad * 8 + (size_t)p.nkb * 4 + (size_t)p.nkb + 16;
@@ -236,7 +426,6 @@ cudaError_t launch_rb(const Problem& p, float threshold, const float* lse_part,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  const int R = p.q_len / (kBlock / RB);
   dim3 grid(p.nqb, p.Hq, p.B);
   select_kernel<RB><<<grid, kSelThreads, smem, st>>>(
       lse_part, p.Hq, p.nkb, R, p.q_start_pos / kBlock, threshold, mask,

@@ -32,10 +32,12 @@ BLOCK = 128
 def round_to_bf16(x: np.ndarray) -> np.ndarray:
     """Round float32 values to the nearest bf16 (ties to even); return float32."""
     x = np.ascontiguousarray(x, np.float32)
-    bits = x.view(np.uint32).astype(np.uint64)
-    lsb = (bits >> 16) & 1
-    rounded = ((bits + 0x7FFF + lsb) >> 16) << 16
-    out = (rounded & 0xFFFFFFFF).astype(np.uint32).view(np.float32)
+    bits = x.view(np.uint32)
+    # add 0x7FFF plus the lowest kept bit, then drop the low half; for finite
+    # values the sum stays below 2**32 (the largest is 0xFF807FFF)
+    lsb = (bits >> np.uint32(16)) & np.uint32(1)
+    rounded = (bits + (np.uint32(0x7FFF) + lsb)) & np.uint32(0xFFFF0000)
+    out = rounded.view(np.float32)
     # NaN/Inf never occur in these draws; keep them out explicitly
     assert np.isfinite(out).all()
     return out

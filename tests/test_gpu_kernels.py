@@ -40,6 +40,8 @@ ESTIMATE_CASES = [
     (1, 2, 2, 128, 640, 0, 8, 0.8, "f32", 0.0, 0),
     (1, 4, 1, 128, 1152, 1024, 8, 0.99, "bf16", 3.0, 2),  # chunk of one block
     (1, 4, 2, 64, 896, 384, 16, 0.5, "bf16", 3.0, 1),
+    (1, 2, 1, 64, 40960, 40704, 8, 0.9, "bf16", 3.0, 4),     # 320 key blocks per row
+    (1, 1, 1, 64, 132096, 131968, 16, 0.9, "bf16", 3.0, 4),  # 1032: the CTA-per-row path
 ]
 
 
@@ -127,10 +129,16 @@ def test_merge(dt, d):
 
 
 @pytest.mark.parametrize("cpu_tokens,force", [(1024, False), (1024, True), (4096, False), (128, True)])
-def test_map(cpu_tokens, force):
-    P, Lq = 8192, 512
+@pytest.mark.parametrize("Lq,offset", [(512, 0), (1024, 0), (1024, 1)])
+def test_map(cpu_tokens, force, Lq, offset):
+    """Lk/128 = 68 (byte loads), 72 (8-byte loads), 72 with a mask that starts
+    one byte past an aligned address (byte loads)."""
+    P = 8192
     mask = random_block_mask(3, 2, 4, Lq // 128, (P + Lq) // 128, P, 0.01)
-    keep = bsx_map_mask_to_cpu_blocks(torch.from_numpy(mask).cuda(), P, cpu_tokens, force)
+    buf = torch.zeros(mask.size + offset, dtype=torch.uint8, device="cuda")
+    dmask = buf[offset:].view(mask.shape)
+    dmask.copy_(torch.from_numpy(mask))
+    keep = bsx_map_mask_to_cpu_blocks(dmask, P, cpu_tokens, force)
     torch.cuda.synchronize()
     ref = O.map_mask_to_cpu_blocks(mask.astype(bool), P, cpu_tokens, force)
     np.testing.assert_array_equal(keep.cpu().numpy(), ref)
