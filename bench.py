@@ -219,6 +219,11 @@ def run_gpu(args):
         return lambda q, k, v: bsx.bsx_bsa_prefill(q, k, v, m, P, kb0, kb1, o=o, lse=lse,
                                                    stream=stream)
 
+    def bsa_split(m):
+        # history and current chunk, one launch, each into its own (O, LSE)
+        return lambda q, k, v: bsx.bsx_bsa_prefill_split(q, k, v, m, P, o_hist=oh, lse_hist=lh,
+                                                         o_curr=oc, lse_curr=lc, stream=stream)
+
     def merge_map(q, k, v):
         bsx.bsx_merge_attn(oh, lh, oc, lc, stream=stream)
         if P >= cpu_tokens:
@@ -233,18 +238,16 @@ def run_gpu(args):
 
     # phases of one step, timed separately; the BSA phases give the roofline
     if args.step == "chunk":
-        phases = [("estimate", est), ("bsa_hist", bsa(mask, 0, cur, oh, lh)),
-                  ("bsa_curr", bsa(mask, cur, nkb, oc, lc)), ("merge_map", merge_map)]
-        launches = 6
+        phases = [("estimate", est), ("bsa_split", bsa_split(mask)), ("merge_map", merge_map)]
+        launches = 5
     elif args.step in ("fused", "prefill"):
         # the launches bsx_chunk_prefill enqueues, timed one by one
         phases = [("estimate", est), ("bsa_all", bsa(mask, 0, nkb, oh, lh))]
         launches = 3
     elif args.step == "offload":
         phases = [("estimate", est), ("cpu_blocks", offload_mask),
-                  ("bsa_hist", bsa(omask, 0, cur, oh, lh)),
-                  ("bsa_curr", bsa(omask, cur, nkb, oc, lc)), ("merge", merge_only)]
-        launches = 7
+                  ("bsa_split", bsa_split(omask)), ("merge", merge_only)]
+        launches = 6
     else:
         raise ValueError(args.step)
 
@@ -262,8 +265,9 @@ def run_gpu(args):
     bsa_mask = (omask if args.step == "offload" else mask).cpu().numpy()
     causal_blocks = sum(cur + qb + 1 for qb in range(Lq // 128)) * B * Hq
     density = float(mask.cpu().numpy().astype(bool).sum()) / causal_blocks
-    ranges = {"bsa_hist": (0, cur), "bsa_curr": (cur, nkb), "bsa_all": (0, nkb)}
-    flops = {n: bsa_flops(bsa_mask, P, *ranges[n], d) for n, _ in phases if n in ranges}
+    ranges = {"bsa_split": ((0, cur), (cur, nkb)), "bsa_all": ((0, nkb),)}
+    flops = {n: sum(bsa_flops(bsa_mask, P, r0, r1, d) for r0, r1 in ranges[n])
+             for n, _ in phases if n in ranges}
 
     np_ = len(phases)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(np_ + 1)]

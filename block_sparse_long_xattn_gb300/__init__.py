@@ -11,6 +11,7 @@ from ._lib import (  # noqa: F401
     BsxError,
     BsxShape,
     bsx_bsa_prefill,
+    bsx_bsa_prefill_split,
     bsx_chunk_prefill,
     bsx_cpu_block_mask,
     bsx_estimate_workspace_bytes,

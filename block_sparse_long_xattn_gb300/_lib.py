@@ -25,7 +25,7 @@ STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported", -3: "CUDA error",
 EXPORTS = ("bsx_version", "bsx_status_string", "bsx_estimate_workspace_bytes",
            "bsx_xattn_estimate", "bsx_bsa_prefill", "bsx_merge_attn",
            "bsx_map_mask_to_cpu_blocks", "bsx_last_error", "bsx_xattn_estimate_noalloc",
-           "bsx_cpu_block_mask", "bsx_chunk_prefill")
+           "bsx_cpu_block_mask", "bsx_chunk_prefill", "bsx_bsa_prefill_split")
 
 
 class BsxShape(ctypes.Structure):
@@ -70,6 +70,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.bsx_bsa_prefill.restype = i32
         lib.bsx_bsa_prefill.argtypes = [BsxShape, vp, vp, vp, vp, i32, i32, i32, i32,
                                         vp, vp, vp]
+        lib.bsx_bsa_prefill_split.restype = i32
+        lib.bsx_bsa_prefill_split.argtypes = [BsxShape, vp, vp, vp, vp, i32, i32, vp, vp, vp, vp,
+                                              vp]
         lib.bsx_merge_attn.restype = i32
         lib.bsx_merge_attn.argtypes = [BsxShape, i32, vp, vp, vp, vp, vp]
         lib.bsx_map_mask_to_cpu_blocks.restype = i32
@@ -178,6 +181,25 @@ def bsx_bsa_prefill(q, k, v, mask, q_start_pos: int, kb_begin: int = 0,
         shape_of(q, k), _ptr(q), _ptr(k), _ptr(v), _ptr(mask), q_len, q_start_pos,
         kb_begin, kb_end, _ptr(o), _ptr(lse), _stream(stream)))
     return o, lse
+
+
+def bsx_bsa_prefill_split(q, k, v, mask, q_start_pos: int, *, o_hist=None, lse_hist=None,
+                          o_curr=None, lse_curr=None, stream=None):
+    """History and current-chunk block-sparse attention in one launch
+    -> (o_hist, lse_hist, o_curr, lse_curr)."""
+    lib = load()
+    B, q_len, Hq, d = q.shape
+    outs = []
+    for t in (o_hist, o_curr):
+        outs.append(torch.empty_like(q) if t is None else t)
+    lses = []
+    for t in (lse_hist, lse_curr):
+        lses.append(torch.empty((B, Hq, q_len), dtype=torch.float32, device=q.device)
+                    if t is None else t)
+    _check("bsx_bsa_prefill_split", lib.bsx_bsa_prefill_split(
+        shape_of(q, k), _ptr(q), _ptr(k), _ptr(v), _ptr(mask), q_len, q_start_pos,
+        _ptr(outs[0]), _ptr(lses[0]), _ptr(outs[1]), _ptr(lses[1]), _stream(stream)))
+    return outs[0], lses[0], outs[1], lses[1]
 
 
 def bsx_chunk_prefill(q, k, v, q_start_pos: int, stride: int, threshold: float, *,

@@ -125,9 +125,37 @@ int bsx_bsa_prefill(bsx_shape s, const void* q, const void* k, const void* v,
   if (p.dtype == BSX_BF16) {
     // tcgen05 path: one 128-row q-tile per CTA, up to kMaxKeyBlocks per row
     if (kb_end - kb_begin > kMaxKeyBlocks) return BSX_ERR_UNSUPPORTED;
-    e = bsx::launch_bsa_tc(p, q, k, v, mask, kb_begin, kb_end, o, lse, err_word(), st);
+    const bsx::BsaRange r{kb_begin, kb_end, o, lse};
+    e = bsx::launch_bsa_tc(p, q, k, v, mask, 1, &r, err_word(), st);
   } else {
     e = bsx::launch_bsa_simt(p, q, k, v, mask, kb_begin, kb_end, o, lse, st);
+  }
+  return cuda_status(e);
+}
+
+int bsx_bsa_prefill_split(bsx_shape s, const void* q, const void* k, const void* v,
+                          const uint8_t* mask, int q_len, int q_start_pos, void* o_hist,
+                          float* lse_hist, void* o_curr, float* lse_curr, void* stream) {
+  bsx::Problem p;
+  int rc = make_problem(s, q_len, q_start_pos, &p);
+  if (rc != BSX_OK) return rc;
+  if (!q || !k || !v || !mask || !o_hist || !lse_hist || !o_curr || !lse_curr)
+    return BSX_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o_hist) ||
+      !aligned16(lse_hist) || !aligned16(o_curr) || !aligned16(lse_curr))
+    return BSX_ERR_INVALID_ARG;
+  const int cur = q_start_pos / 128;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (p.dtype == BSX_BF16) {
+    if (cur > kMaxKeyBlocks || p.nkb - cur > kMaxKeyBlocks) return BSX_ERR_UNSUPPORTED;
+    // history CTAs (the long ones) first, the current chunk's fill the tail
+    const bsx::BsaRange r[2] = {{0, cur, o_hist, lse_hist}, {cur, p.nkb, o_curr, lse_curr}};
+    e = bsx::launch_bsa_tc(p, q, k, v, mask, 2, r, err_word(), st);
+  } else {
+    e = bsx::launch_bsa_simt(p, q, k, v, mask, 0, cur, o_hist, lse_hist, st);
+    if (e == cudaSuccess)
+      e = bsx::launch_bsa_simt(p, q, k, v, mask, cur, p.nkb, o_curr, lse_curr, st);
   }
   return cuda_status(e);
 }

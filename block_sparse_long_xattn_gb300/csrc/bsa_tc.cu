@@ -60,13 +60,30 @@ struct Layout {
   static constexpr uint32_t kTmemCols = 512;              // S/P 0, S/P 1, O_0, O_1
 };
 
+// One launch computes up to two key-block ranges of the same queries, each
+// into its own O and LSE (the history and the current chunk of a chunk step).
+struct BsaPart {
+  int kb_begin, kb_end;
+  __nv_bfloat16* o;
+  float* lse;
+};
+struct BsaParts {
+  BsaPart p0, p1;
+  int B;
+};
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const uint8_t* __restrict__ mask, int q_len,
-    int Lk, int Hq, int Hkv, int cur, int kb_begin, int kb_end, float scale_log2,
-    __nv_bfloat16* __restrict__ o, float* __restrict__ lse, unsigned* err) {
+    int Lk, int Hq, int Hkv, int cur, float scale_log2, const BsaParts parts, unsigned* err) {
   using L = Layout<D>;
+  // blockIdx.z = b + B * part: the parts' CTAs run in order, part 0 first
+  const int part = (int)blockIdx.z / parts.B;
+  const int kb_begin = part ? parts.p1.kb_begin : parts.p0.kb_begin;
+  const int kb_end = part ? parts.p1.kb_end : parts.p0.kb_end;
+  __nv_bfloat16* __restrict__ o = part ? parts.p1.o : parts.p0.o;
+  float* __restrict__ lse = part ? parts.p1.lse : parts.p0.lse;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -90,7 +107,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
 
   // heads vary fastest and query tiles run last-first: with causal masking
   // the late tiles see the most key blocks, so the long CTAs start first
-  const int h = blockIdx.x, b = blockIdx.z;
+  const int h = blockIdx.x, b = (int)blockIdx.z % parts.B;
   const int nqb = gridDim.y;
   const int qb = nqb - 1 - (int)blockIdx.y;
   const int nkb = Lk / kBlock;
@@ -428,8 +445,8 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
 
 template <int D>
 cudaError_t launch_d(const Problem& p, const void* q, const void* k, const void* v,
-                     const uint8_t* mask, int kb_begin, int kb_end, void* o, float* lse,
-                     unsigned* err, cudaStream_t st) {
+                     const uint8_t* mask, int nparts, const BsaRange* ranges, unsigned* err,
+                     cudaStream_t st) {
   using L = Layout<D>;
   CUtensorMap mq, mk, mv;
   const uint32_t box[4] = {64, 1, 128, 1};
@@ -451,21 +468,27 @@ cudaError_t launch_d(const Problem& p, const void* q, const void* k, const void*
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
-  dim3 grid(p.Hq, p.nqb, p.B);
-  bsa_tc_kernel<D><<<grid, kThreads, smem, st>>>(
-      mq, mk, mv, mask, p.q_len, p.Lk, p.Hq, p.Hkv, p.q_start_pos / kBlock, kb_begin, kb_end,
-      scale_log2, static_cast<__nv_bfloat16*>(o), lse, err);
+  BsaParts parts;
+  parts.B = p.B;
+  parts.p0 = {ranges[0].kb_begin, ranges[0].kb_end, static_cast<__nv_bfloat16*>(ranges[0].o),
+              ranges[0].lse};
+  parts.p1 = nparts > 1 ? BsaPart{ranges[1].kb_begin, ranges[1].kb_end,
+                                  static_cast<__nv_bfloat16*>(ranges[1].o), ranges[1].lse}
+                        : parts.p0;
+  dim3 grid(p.Hq, p.nqb, p.B * nparts);
+  bsa_tc_kernel<D><<<grid, kThreads, smem, st>>>(mq, mk, mv, mask, p.q_len, p.Lk, p.Hq, p.Hkv,
+                                                 p.q_start_pos / kBlock, scale_log2, parts, err);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_bsa_tc(const Problem& p, const void* q, const void* k, const void* v,
-                          const uint8_t* mask, int kb_begin, int kb_end, void* o, float* lse,
+                          const uint8_t* mask, int nparts, const BsaRange* ranges,
                           unsigned* err, cudaStream_t st) {
-  if (p.dtype != 1) return cudaErrorInvalidValue;
-  if (p.d == 64) return launch_d<64>(p, q, k, v, mask, kb_begin, kb_end, o, lse, err, st);
-  if (p.d == 128) return launch_d<128>(p, q, k, v, mask, kb_begin, kb_end, o, lse, err, st);
+  if (p.dtype != 1 || nparts < 1 || nparts > 2) return cudaErrorInvalidValue;
+  if (p.d == 64) return launch_d<64>(p, q, k, v, mask, nparts, ranges, err, st);
+  if (p.d == 128) return launch_d<128>(p, q, k, v, mask, nparts, ranges, err, st);
   return cudaErrorInvalidValue;
 }
 

@@ -47,10 +47,18 @@ cudaError_t launch_bsa_simt(const Problem& p, const void* q, const void* k,
                             const void* v, const uint8_t* mask, int kb_begin,
                             int kb_end, void* o, float* lse, cudaStream_t st);
 
-// a5: block-sparse attention on tcgen05 tensor cores (bf16).
+// One key-block range of a5 and where its result goes.
+struct BsaRange {
+  int kb_begin, kb_end;
+  void* o;
+  float* lse;
+};
+
+// a5: block-sparse attention on tcgen05 tensor cores (bf16), for one or two
+// key-block ranges of the same queries in a single launch (the ranges' CTAs
+// run in order, range 0 first).
 cudaError_t launch_bsa_tc(const Problem& p, const void* q, const void* k,
-                          const void* v, const uint8_t* mask, int kb_begin,
-                          int kb_end, void* o, float* lse, unsigned* err,
-                          cudaStream_t st);
+                          const void* v, const uint8_t* mask, int nparts,
+                          const BsaRange* ranges, unsigned* err, cudaStream_t st);
 
 }  // namespace bsx

@@ -161,6 +161,23 @@ int bsx_bsa_prefill(bsx_shape s, const void* q, const void* k, const void* v,
                     void* stream);
 
 /*
+ * Both parts of one chunk's block-sparse attention in a single launch: the
+ * history, key blocks [0, q_start_pos/128), into (o_hist, lse_hist), and the
+ * current chunk, key blocks [q_start_pos/128, Lk/128), into (o_curr,
+ * lse_curr).  Each part is exactly what bsx_bsa_prefill computes for that
+ * range (xattn_bsa.py compute_chunked_prefill attends to the history and to
+ * the current chunk separately and merges the two by LSE, bsx_merge_attn).
+ * One launch lets the short current-chunk work fill the tail of the history
+ * work on the GPU.  Arguments, layouts and errors as bsx_bsa_prefill; the
+ * four outputs must not overlap.  With q_start_pos == 0 the history part is
+ * empty (o_hist = 0, lse_hist = -inf).
+ */
+int bsx_bsa_prefill_split(bsx_shape s, const void* q, const void* k, const void* v,
+                          const uint8_t* mask, int q_len, int q_start_pos,
+                          void* o_hist, float* lse_hist, void* o_curr, float* lse_curr,
+                          void* stream);
+
+/*
  * One chunk of XAttention prefill with the KV resident on the device:
  * bsx_xattn_estimate followed by bsx_bsa_prefill over every key block
  * [0, Lk/128) in one launch.  By the merge identity this equals attending to

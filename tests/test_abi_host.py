@@ -83,6 +83,9 @@ def test_bsa_merge_map_reject_bad_arguments(lib):
     assert lib.bsx_bsa_prefill(s, p, p, p, p, 256, 256, 2, 1, p, p, None) == -1
     assert lib.bsx_bsa_prefill(s, p, p, p, p, 256, 256, 0, 5, p, p, None) == -1
     assert lib.bsx_bsa_prefill(s, p, None, p, p, 256, 256, 0, 4, p, p, None) == -1
+    # split launch: every output required, q_start_pos a multiple of 128
+    assert lib.bsx_bsa_prefill_split(s, p, p, p, p, 256, 256, p, p, None, p, None) == -1
+    assert lib.bsx_bsa_prefill_split(s, p, p, p, p, 256, 200, p, p, p, p, None) == -1
     assert lib.bsx_merge_attn(s, 100, p, p, p, p, None) == -1
     assert lib.bsx_merge_attn(s, 128, p, None, p, p, None) == -1
     # cpu block size must divide q_start_pos and be a multiple of 128

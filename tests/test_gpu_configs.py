@@ -17,8 +17,8 @@ import pytest
 import torch
 
 from block_sparse_long_xattn_gb300 import (
-    bsx_bsa_prefill, bsx_last_error, bsx_map_mask_to_cpu_blocks, bsx_merge_attn,
-    bsx_xattn_estimate)
+    bsx_bsa_prefill, bsx_bsa_prefill_split, bsx_last_error, bsx_map_mask_to_cpu_blocks,
+    bsx_merge_attn, bsx_xattn_estimate)
 from block_sparse_long_xattn_gb300.inputs import CONFIGS, make_workload
 from oracle import xattn_oracle as O
 from tests.helpers import LSE_TOL, O_TOL, check_block_sums, check_mask, to_dev
@@ -38,8 +38,7 @@ def gpu_chunk_step(q, k, v, P, S, tau, mask_for_bsa=None, cpu_tokens=1024):
     A = torch.empty((B, Hq, Lq // 128, nkb), dtype=torch.float32, device=q.device)
     mask = bsx_xattn_estimate(q, k, P, S, tau, block_sums=A)
     m = mask if mask_for_bsa is None else mask_for_bsa
-    oh, lh = bsx_bsa_prefill(q, k, v, m, P, 0, cur)
-    oc, lc = bsx_bsa_prefill(q, k, v, m, P, cur, nkb)
+    oh, lh, oc, lc = bsx_bsa_prefill_split(q, k, v, m, P)
     bsx_merge_attn(oh, lh, oc, lc)
     keep = bsx_map_mask_to_cpu_blocks(m, P, cpu_tokens) if P >= cpu_tokens else None
     torch.cuda.synchronize()

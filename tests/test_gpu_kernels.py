@@ -12,8 +12,8 @@ import pytest
 import torch
 
 from block_sparse_long_xattn_gb300 import (
-    bsx_bsa_prefill, bsx_chunk_prefill, bsx_cpu_block_mask, bsx_last_error,
-    bsx_map_mask_to_cpu_blocks, bsx_merge_attn, bsx_xattn_estimate)
+    bsx_bsa_prefill, bsx_bsa_prefill_split, bsx_chunk_prefill, bsx_cpu_block_mask,
+    bsx_last_error, bsx_map_mask_to_cpu_blocks, bsx_merge_attn, bsx_xattn_estimate)
 from block_sparse_long_xattn_gb300.inputs import make_workload, random_block_mask
 from oracle import xattn_oracle as O
 from tests.helpers import LSE_TOL, O_TOL, check_block_sums, check_mask, to_dev
@@ -144,8 +144,34 @@ def test_map(cpu_tokens, force, Lq, offset):
     np.testing.assert_array_equal(keep.cpu().numpy(), ref)
 
 
+@pytest.mark.parametrize("P,Lq,d", [(1024, 512, 128), (0, 384, 128), (896, 256, 64)])
+def test_bsa_split_equals_two_calls(P, Lq, d):
+    """bsx_bsa_prefill_split gives, bit for bit, what bsx_bsa_prefill gives for
+    the history and the current-chunk ranges, and both match the oracle."""
+    w = make_workload(seed=31 + P + d, B=2, Hq=4, Hkv=2, d=d, Lk=P + Lq, q_start_pos=P,
+                      alpha=3.0, n_hot=2, dtype="bf16")
+    nqb, nkb, cur = Lq // 128, (P + Lq) // 128, P // 128
+    mask = random_block_mask(5 + P, 2, 4, nqb, nkb, P, 0.6)
+    q, k, v = (to_dev(x, "bf16") for x in (w.q, w.k, w.v))
+    dm = torch.from_numpy(mask).cuda()
+    oh, lh, oc, lc = bsx_bsa_prefill_split(q, k, v, dm, P)
+    oh2, lh2 = bsx_bsa_prefill(q, k, v, dm, P, 0, cur)
+    oc2, lc2 = bsx_bsa_prefill(q, k, v, dm, P, cur, nkb)
+    torch.cuda.synchronize()
+    assert torch.equal(oh, oh2) and torch.equal(oc, oc2)
+    assert torch.equal(lh, lh2) and torch.equal(lc, lc2)
+    for (o_g, l_g), (kb0, kb1) in (((oc, lc), (cur, nkb)), ((oh, lh), (0, cur))):
+        o_ref, l_ref = O.bsa_prefill(w.q, w.k, w.v, mask.astype(bool), P, kb0, kb1)
+        fin = np.isfinite(l_ref)
+        lg = l_g.cpu().numpy()
+        assert np.array_equal(np.isfinite(lg), fin)
+        if fin.any():
+            assert np.abs(lg[fin] - l_ref[fin]).max() <= LSE_TOL
+        assert np.abs(o_g.float().cpu().numpy() - o_ref).max() <= O_TOL["bf16"]
+
+
 def test_chunk_step_small():
-    """Estimate -> BSA(history) -> BSA(current) -> merge -> map, small chunk."""
+    """Estimate -> BSA(history and current, one launch) -> merge -> map, small chunk."""
     P, S, tau = 768, 8, 0.9
     w = make_workload(seed=77, B=1, Hq=8, Hkv=2, d=128, Lk=P + 512, q_start_pos=P,
                       alpha=3.0, n_hot=2, dtype="bf16")
@@ -157,8 +183,7 @@ def test_chunk_step_small():
     check_mask(mask_g.cpu().numpy(), est, tau, P, A.cpu().numpy())
     mask = torch.from_numpy(est.mask.astype(np.uint8)).cuda()
     cur, nkb = P // 128, (P + 512) // 128
-    oh, lh = bsx_bsa_prefill(q, k, v, mask, P, 0, cur)
-    oc, lc = bsx_bsa_prefill(q, k, v, mask, P, cur, nkb)
+    oh, lh, oc, lc = bsx_bsa_prefill_split(q, k, v, mask, P)
     bsx_merge_attn(oh, lh, oc, lc)
     keep = bsx_map_mask_to_cpu_blocks(mask, P, 256)
     torch.cuda.synchronize()
