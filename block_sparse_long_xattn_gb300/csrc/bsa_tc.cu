@@ -69,7 +69,7 @@ struct BsaPart {
 };
 struct BsaParts {
   BsaPart p0, p1;
-  int B;
+  int B, nqb;
 };
 
 template <int D>
@@ -78,8 +78,20 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
     const __grid_constant__ CUtensorMap tm_v, const uint8_t* __restrict__ mask, int q_len,
     int Lk, int Hq, int Hkv, int cur, float scale_log2, const BsaParts parts, unsigned* err) {
   using L = Layout<D>;
-  // blockIdx.z = b + B * part: the parts' CTAs run in order, part 0 first
-  const int part = (int)blockIdx.z / parts.B;
+  // One linear grid, decoded here so that the dispatch order is explicit:
+  // part 0 before part 1, then batch, then heads, query tiles fastest.  The
+  // CTAs resident together then cover a few heads of one GQA group or two,
+  // whose K/V stay in L2 for the whole wave (heads fastest would stream every
+  // kv-head's K/V in every wave and re-read it from DRAM).  Query tiles run
+  // last-first: with causal masking the late tiles see the most key blocks.
+  const int nqb = parts.nqb;
+  const int per_part = parts.B * nqb * Hq;
+  const int part = (int)blockIdx.x / per_part;
+  const int rem = (int)blockIdx.x - part * per_part;
+  const int b = rem / (nqb * Hq);
+  const int r2 = rem - b * (nqb * Hq);
+  const int h = r2 / nqb;
+  const int qb = nqb - 1 - (r2 - h * nqb);
   const int kb_begin = part ? parts.p1.kb_begin : parts.p0.kb_begin;
   const int kb_end = part ? parts.p1.kb_end : parts.p0.kb_end;
   __nv_bfloat16* __restrict__ o = part ? parts.p1.o : parts.p0.o;
@@ -105,11 +117,6 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
   const uint32_t mma_final = bar0 + 8 * (kB2 + 6);
   const uint32_t xbar = bar0 + 8 * (kB2 + 7);                    // end-of-row merge
 
-  // heads vary fastest and query tiles run last-first: with causal masking
-  // the late tiles see the most key blocks, so the long CTAs start first
-  const int h = blockIdx.x, b = (int)blockIdx.z % parts.B;
-  const int nqb = gridDim.y;
-  const int qb = nqb - 1 - (int)blockIdx.y;
   const int nkb = Lk / kBlock;
   const int hk = h / (Hq / Hkv);
   const int diag = cur + qb;
@@ -470,12 +477,13 @@ cudaError_t launch_d(const Problem& p, const void* q, const void* k, const void*
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
   BsaParts parts;
   parts.B = p.B;
+  parts.nqb = p.nqb;
   parts.p0 = {ranges[0].kb_begin, ranges[0].kb_end, static_cast<__nv_bfloat16*>(ranges[0].o),
               ranges[0].lse};
   parts.p1 = nparts > 1 ? BsaPart{ranges[1].kb_begin, ranges[1].kb_end,
                                   static_cast<__nv_bfloat16*>(ranges[1].o), ranges[1].lse}
                         : parts.p0;
-  dim3 grid(p.Hq, p.nqb, p.B * nparts);
+  const dim3 grid(p.Hq * p.nqb * p.B * nparts);
   bsa_tc_kernel<D><<<grid, kThreads, smem, st>>>(mq, mk, mv, mask, p.q_len, p.Lk, p.Hq, p.Hkv,
                                                  p.q_start_pos / kBlock, scale_log2, parts, err);
   return cudaGetLastError();
