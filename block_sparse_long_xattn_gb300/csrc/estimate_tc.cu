@@ -150,41 +150,46 @@ __global__ void __launch_bounds__(kThreads, 1) estimate_tc_kernel(
     }
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ----------------------------
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(kM, kN, 0, 0);
-      int it = 0, ti = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; ok && t < T.total; t += gridDim.x, ++ti) {
-        const int buf = ti & 1;
-        if (ti >= 2 && !mbar_wait(acc_empty(buf), ((ti >> 1) - 1) & 1, abort_flag, err,
-                                  kErrEstimateTc, kSiteAccEmpty)) {
-          ok = false;
-          break;
-        }
+    // The whole warp runs the loop (warp-uniform slot addresses and
+    // descriptors, formed by adding offsets to one base descriptor: the
+    // start-address field is address >> 4 in the low bits, and shared
+    // addresses are below 256 KB); one elected lane issues.  A single-lane
+    // issuer sharing its scheduler with the ALU-bound epilogue warps cannot
+    // keep the tensor pipe fed.  Every lane keeps its own wait result over the
+    // same trip count, so a timed-out wait needs no warp vote.
+    constexpr uint32_t idesc = idesc_bf16_f32(kM, kN, 0, 0);
+    const bool leader = elect_one_sync();
+    const uint64_t d_base = smem_desc_sw128(sb, 16, 1024);
+    int it = 0, ti = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < T.total; t += gridDim.x, ++ti) {
+      const int buf = ti & 1;
+      if (ti >= 2)
+        ok = ok && mbar_wait(acc_empty(buf), ((ti >> 1) - 1) & 1, abort_flag, err,
+                             kErrEstimateTc, kSiteAccEmpty);
+      tc_fence_after();
+      const uint32_t acc = tmem + buf * kN;
+      for (int ch = 0; ch < NCH; ++ch, ++it) {
+        const int s = it % kStages;
+        ok = ok && mbar_wait(full(s), (it / kStages) & 1, abort_flag, err, kErrEstimateTc,
+                             kSiteFull);
         tc_fence_after();
-        const uint32_t acc = tmem + buf * kN;
-        for (int ch = 0; ch < NCH; ++ch, ++it) {
-          const int s = it % kStages;
-          if (!mbar_wait(full(s), (it / kStages) & 1, abort_flag, err, kErrEstimateTc,
-                         kSiteFull)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a_base = sb + s * kStageBytes;
+        if (leader && ok) {
+          const uint64_t da = d_base + (uint64_t)((s * kStageBytes) >> 4);
+          const uint64_t db = da + (uint64_t)(kABytes >> 4);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {  // 16 features per MMA, 32 bytes along the row
-            const uint64_t a = smem_desc_sw128(a_base + k * 32, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(a_base + kABytes + k * 32, 16, 1024);
-            mma_bf16(acc, a, bd, idesc, (ch > 0 || k > 0) ? 1u : 0u);
-          }
+          for (int k = 0; k < 4; ++k)  // 16 features per MMA, 32 bytes along the row
+            mma_bf16(acc, da + 2 * k, db + 2 * k, idesc, (ch > 0 || k > 0) ? 1u : 0u);
           mma_commit(empty(s));
         }
-        if (ok) mma_commit(acc_full(buf));
+        __syncwarp();
       }
-      mma_commit(mma_final);
-      drain_wait(mma_final, 0);
+      if (leader && ok) mma_commit(acc_full(buf));
+      __syncwarp();
     }
+    if (leader) mma_commit(mma_final);
+    __syncwarp();
+    drain_wait(mma_final, 0);
   } else {
     // ------------------------------ epilogue ------------------------------
     const int quad = warp & 3;
