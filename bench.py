@@ -212,8 +212,32 @@ def run_gpu(args):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
+    e4m3 = args.estimator == "e4m3"
+    if e4m3:
+        # e4m3 copies of Q and K for the estimator: the history's K is kept in
+        # e4m3 next to the bf16 KV (made once here); each step quantizes the
+        # chunk's Q and the chunk's own keys
+        if B != 1:
+            raise SystemExit("--estimator e4m3 runs batch 1 (the chunk's keys are one slice)")
+        q8 = torch.empty(dq.shape, dtype=torch.float8_e4m3fn, device=dev)
+        k8 = bsx.bsx_quantize_e4m3(dk)
+        torch.cuda.synchronize()
+
     def est(q, k, v):
+        if e4m3:
+            bsx.bsx_quantize_e4m3(q, out=q8, stream=stream)
+            bsx.bsx_quantize_e4m3(k[:, P:], out=k8[:, P:], stream=stream)
+            q, k = q8, k8
         bsx.bsx_xattn_estimate(q, k, P, S, tau, mask=mask, workspace=ws, stream=stream)
+
+    def est_e2e(q, k, v):
+        # the uploaded K has no e4m3 copy yet: quantize all of it
+        if e4m3:
+            bsx.bsx_quantize_e4m3(k, out=k8, stream=stream)
+            bsx.bsx_quantize_e4m3(q, out=q8, stream=stream)
+            bsx.bsx_xattn_estimate(q8, k8, P, S, tau, mask=mask, workspace=ws, stream=stream)
+        else:
+            est(q, k, v)
 
     def bsa(m, kb0, kb1, o, lse):
         return lambda q, k, v: bsx.bsx_bsa_prefill(q, k, v, m, P, kb0, kb1, o=o, lse=lse,
@@ -303,7 +327,7 @@ def run_gpu(args):
         e0.record(stream)
         q2.copy_(host["q"], non_blocking=True)
         k2.copy_(host["k"], non_blocking=True)
-        if args.step in ("fused", "prefill"):
+        if args.step in ("fused", "prefill") and not e4m3:
             v2.copy_(host["v"], non_blocking=True)
             bsx.bsx_chunk_prefill(q2, k2, v2, P, S, tau, mask=mask, o=oh, lse=lh,
                                   workspace=ws, stream=stream)
@@ -315,7 +339,7 @@ def run_gpu(args):
                 v2.copy_(host["v"], non_blocking=True)
             v_in = torch.cuda.Event()
             v_in.record(copy_stream)
-            phases[0][1](q2, k2, v2)          # the estimate reads Q and K only
+            est_e2e(q2, k2, v2)               # the estimate reads Q and K only
             stream.wait_event(v_in)
             for _, fn in phases[1:]:
                 fn(q2, k2, v2)
@@ -364,7 +388,8 @@ def run_gpu(args):
                    "Hkv": Hkv, "d": d, "q_len": Lq, "q_start_pos": P, "Lk": Lk, "stride": S,
                    "threshold": tau, "cpu_block_tokens": cpu_tokens,
                    "parallelism": f"replicas{world}",
-                   "l2": "flushed (256 MiB write) between timed steps", "seed": args.seed},
+                   "l2": "flushed (256 MiB write) between timed steps", "seed": args.seed,
+                   "estimator_operands": args.estimator},
         "roofline": {"kernel": DOMINANT, "bound": "tensor", "achieved": achieved,
                      "peak": tc_peak, "unit": "TFLOP/s", "frac": achieved / tc_peak,
                      "traffic": traffic, "peak_source": peak_src,
@@ -456,6 +481,9 @@ def main():
                          "(the default); fused: estimate + one BSA launch over all key "
                          "blocks; offload: the pages' CPU-block-dense history; prefill: "
                          "fused on a whole-sequence workload")
+    ap.add_argument("--estimator", default="bf16", choices=["bf16", "e4m3"],
+                    help="operand type of the estimator's scores (e4m3: Q and the chunk's K "
+                         "quantized each step, the history's K kept in e4m3)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-heads", type=int, default=4,
                     help="q-heads in the oracle sample of the cpu_baseline leg")

@@ -7,6 +7,7 @@ Importing the package does not load the library; the first call does, and it
 raises if the library has not been built.
 """
 from ._lib import (  # noqa: F401
+    BSX_F8E4M3,
     BSX_FORCE_FIRST_LAST,
     BsxError,
     BsxShape,
@@ -18,6 +19,7 @@ from ._lib import (  # noqa: F401
     bsx_last_error,
     bsx_map_mask_to_cpu_blocks,
     bsx_merge_attn,
+    bsx_quantize_e4m3,
     bsx_version,
     bsx_xattn_estimate,
     bsx_xattn_estimate_noalloc,

@@ -17,7 +17,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libbsxattn.so")
 
-BSX_F32, BSX_BF16 = 0, 1
+BSX_F32, BSX_BF16, BSX_F8E4M3 = 0, 1, 2
 BSX_FORCE_FIRST_LAST = 1
 STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported", -3: "CUDA error",
           -4: "bounded device wait expired", -5: "workspace missing or too small"}
@@ -25,7 +25,8 @@ STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported", -3: "CUDA error",
 EXPORTS = ("bsx_version", "bsx_status_string", "bsx_estimate_workspace_bytes",
            "bsx_xattn_estimate", "bsx_bsa_prefill", "bsx_merge_attn",
            "bsx_map_mask_to_cpu_blocks", "bsx_last_error", "bsx_xattn_estimate_noalloc",
-           "bsx_cpu_block_mask", "bsx_chunk_prefill", "bsx_bsa_prefill_split")
+           "bsx_cpu_block_mask", "bsx_chunk_prefill", "bsx_bsa_prefill_split",
+           "bsx_quantize_e4m3")
 
 
 class BsxShape(ctypes.Structure):
@@ -70,6 +71,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.bsx_bsa_prefill.restype = i32
         lib.bsx_bsa_prefill.argtypes = [BsxShape, vp, vp, vp, vp, i32, i32, i32, i32,
                                         vp, vp, vp]
+        lib.bsx_quantize_e4m3.restype = i32
+        lib.bsx_quantize_e4m3.argtypes = [vp, vp, ctypes.c_longlong, vp]
         lib.bsx_bsa_prefill_split.restype = i32
         lib.bsx_bsa_prefill_split.argtypes = [BsxShape, vp, vp, vp, vp, i32, i32, vp, vp, vp, vp,
                                               vp]
@@ -98,7 +101,10 @@ def _dtype_code(t: torch.Tensor) -> int:
         return BSX_BF16
     if t.dtype == torch.float32:
         return BSX_F32
-    raise TypeError(f"unsupported dtype {t.dtype}; bsxattn takes bfloat16 or float32")
+    if t.dtype == torch.float8_e4m3fn:
+        return BSX_F8E4M3
+    raise TypeError(f"unsupported dtype {t.dtype}; bsxattn takes bfloat16, float32 "
+                    "or (estimate only) float8_e4m3fn")
 
 
 def _ptr(t):
@@ -181,6 +187,19 @@ def bsx_bsa_prefill(q, k, v, mask, q_start_pos: int, kb_begin: int = 0,
         shape_of(q, k), _ptr(q), _ptr(k), _ptr(v), _ptr(mask), q_len, q_start_pos,
         kb_begin, kb_end, _ptr(o), _ptr(lse), _stream(stream)))
     return o, lse
+
+
+def bsx_quantize_e4m3(src, *, out=None, stream=None):
+    """bf16 tensor -> float8_e4m3fn tensor of the same shape (nearest, ties to
+    even, saturated to +-448)."""
+    lib = load()
+    if src.dtype != torch.bfloat16:
+        raise TypeError("bsx_quantize_e4m3 takes bfloat16")
+    if out is None:
+        out = torch.empty(src.shape, dtype=torch.float8_e4m3fn, device=src.device)
+    _check("bsx_quantize_e4m3", lib.bsx_quantize_e4m3(_ptr(src), _ptr(out), src.numel(),
+                                                       _stream(stream)))
+    return out
 
 
 def bsx_bsa_prefill_split(q, k, v, mask, q_start_pos: int, *, o_hist=None, lse_hist=None,

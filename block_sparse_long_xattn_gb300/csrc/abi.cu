@@ -32,10 +32,14 @@ unsigned* err_word() {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Common shape checks; fills the internal problem description.
-int make_problem(const bsx_shape& s, int q_len, int q_start_pos, bsx::Problem* p) {
+// e4m3 operands are accepted only where `allow_e4m3` (the estimate), with d = 128.
+int make_problem(const bsx_shape& s, int q_len, int q_start_pos, bsx::Problem* p,
+                 bool allow_e4m3 = false) {
   if (s.B < 1 || s.Hq < 1 || s.Hkv < 1 || s.Hq % s.Hkv != 0) return BSX_ERR_INVALID_ARG;
-  if (s.dtype != BSX_F32 && s.dtype != BSX_BF16) return BSX_ERR_UNSUPPORTED;
+  const bool e4m3 = s.dtype == BSX_F8E4M3 && allow_e4m3;
+  if (s.dtype != BSX_F32 && s.dtype != BSX_BF16 && !e4m3) return BSX_ERR_UNSUPPORTED;
   if (s.d != 64 && s.d != 128) return BSX_ERR_UNSUPPORTED;
+  if (e4m3 && s.d != 128) return BSX_ERR_UNSUPPORTED;
   if (q_len < 128 || q_len % 128 != 0) return BSX_ERR_INVALID_ARG;
   if (q_start_pos < 0 || q_start_pos % 128 != 0) return BSX_ERR_INVALID_ARG;
   const long long Lk = (long long)q_start_pos + q_len;
@@ -81,7 +85,7 @@ const char* bsx_status_string(int status) {
 
 size_t bsx_estimate_workspace_bytes(bsx_shape s, int q_len, int q_start_pos, int stride) {
   bsx::Problem p;
-  if (make_problem(s, q_len, q_start_pos, &p) != BSX_OK) return 0;
+  if (make_problem(s, q_len, q_start_pos, &p, true) != BSX_OK) return 0;
   if (stride != 4 && stride != 8 && stride != 16) return 0;
   return (size_t)p.B * p.Hq * p.nkb * (size_t)(q_len / stride) * sizeof(float);
 }
@@ -91,7 +95,7 @@ int bsx_xattn_estimate(bsx_shape s, const void* q, const void* k, int q_len,
                        float* block_sums, void* workspace, size_t workspace_bytes,
                        void* stream) {
   bsx::Problem p;
-  int rc = make_problem(s, q_len, q_start_pos, &p);
+  int rc = make_problem(s, q_len, q_start_pos, &p, true);
   if (rc != BSX_OK) return rc;
   if (stride != 4 && stride != 8 && stride != 16) return BSX_ERR_UNSUPPORTED;
   if (!(threshold > 0.0f) || isnan(threshold)) return BSX_ERR_INVALID_ARG;
@@ -102,9 +106,9 @@ int bsx_xattn_estimate(bsx_shape s, const void* q, const void* k, int q_len,
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return BSX_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float* lse_part = static_cast<float*>(workspace);
-  cudaError_t e = p.dtype == BSX_BF16
-                      ? bsx::launch_estimate_tc(p, q, k, stride, lse_part, err_word(), st)
-                      : bsx::launch_estimate_simt(p, q, k, stride, lse_part, st);
+  cudaError_t e = p.dtype == BSX_F32
+                      ? bsx::launch_estimate_simt(p, q, k, stride, lse_part, st)
+                      : bsx::launch_estimate_tc(p, q, k, stride, lse_part, err_word(), st);
   if (e != cudaSuccess) return cuda_status(e);
   e = bsx::launch_select(p, stride, threshold, lse_part, mask, block_sums, st);
   return cuda_status(e);
@@ -158,6 +162,11 @@ int bsx_bsa_prefill_split(bsx_shape s, const void* q, const void* k, const void*
       e = bsx::launch_bsa_simt(p, q, k, v, mask, cur, p.nkb, o_curr, lse_curr, st);
   }
   return cuda_status(e);
+}
+
+int bsx_quantize_e4m3(const void* src, uint8_t* dst, long long n, void* stream) {
+  if (n < 0 || (n > 0 && (!src || !dst))) return BSX_ERR_INVALID_ARG;
+  return cuda_status(bsx::launch_quantize_e4m3(src, dst, n, static_cast<cudaStream_t>(stream)));
 }
 
 int bsx_merge_attn(bsx_shape s, int q_len, void* o1, float* lse1, const void* o2,

@@ -1,5 +1,5 @@
-// a1-a2 partial on tcgen05 tensor cores (bf16): per-(row, key block)
-// log-sum-exp of the scaled antidiagonal scores.
+// a1-a2 partial on tcgen05 tensor cores (bf16, or e4m3 Q and K): per-(row,
+// key block) log-sum-exp of the scaled antidiagonal scores.
 //
 // docs/xattention_algorithm_guide.md "Stride Reshape 详解" and "Triton Kernels
 // 详解" (flat_group_gemm_fuse_reshape): the scores are Q_r K_r^T with
@@ -72,12 +72,15 @@ __device__ __forceinline__ void tile_coords(const Tiles& T, int t, int& b, int& 
   kt = rem;
 }
 
-template <int S, int D>
+// F8: Q and K are e4m3 bytes (kind::f8f6f4 MMAs); otherwise bf16.  Either way
+// a TMA row is 128 bytes: 64 bf16 or 128 e4m3 features.
+template <int S, int D, bool F8>
 __global__ void __launch_bounds__(kThreads, 1) estimate_tc_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     Tiles T, int Hkv, int nkb, float scale_log2, float* __restrict__ lse_part, unsigned* err) {
   constexpr int RB = kBlock / S;          // reshaped keys (and rows) per 128-token block
-  constexpr int FCH = D / 64;             // 64-feature chunks per token
+  constexpr int CW = F8 ? 128 : 64;      // features per 128-byte chunk
+  constexpr int FCH = D / CW;             // chunks per token
   constexpr int NCH = S * FCH;            // reduction chunks per tile
   constexpr int GPC = 32 / RB;            // key blocks per 32-column TMEM load
   extern __shared__ uint8_t smem_raw[];
@@ -138,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1) estimate_tc_kernel(
             ok = false;
             break;
           }
-          const int phase = ch / FCH, c0 = (ch % FCH) * 64;
+          const int phase = ch / FCH, c0 = (ch % FCH) * CW;
           const uint32_t a_dst = sb + s * kStageBytes;
           mbar_arrive_expect_tx(full(s), kStageBytes);
           tma_load_5d(a_dst, &tm_q, full(s), c0, h, S - 1 - phase, rt * kM, b);
@@ -157,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1) estimate_tc_kernel(
     // issuer sharing its scheduler with the ALU-bound epilogue warps cannot
     // keep the tensor pipe fed.  Every lane keeps its own wait result over the
     // same trip count, so a timed-out wait needs no warp vote.
-    constexpr uint32_t idesc = idesc_bf16_f32(kM, kN, 0, 0);
+    constexpr uint32_t idesc = F8 ? idesc_e4m3_f32(kM, kN) : idesc_bf16_f32(kM, kN, 0, 0);
     const bool leader = elect_one_sync();
     const uint64_t d_base = smem_desc_sw128(sb, 16, 1024);
     int it = 0, ti = 0;
@@ -178,8 +181,12 @@ __global__ void __launch_bounds__(kThreads, 1) estimate_tc_kernel(
           const uint64_t da = d_base + (uint64_t)((s * kStageBytes) >> 4);
           const uint64_t db = da + (uint64_t)(kABytes >> 4);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)  // 16 features per MMA, 32 bytes along the row
-            mma_bf16(acc, da + 2 * k, db + 2 * k, idesc, (ch > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < 4; ++k) {  // 32 bytes along the row per MMA
+            if constexpr (F8)
+              mma_f8(acc, da + 2 * k, db + 2 * k, idesc, (ch > 0 || k > 0) ? 1u : 0u);
+            else
+              mma_bf16(acc, da + 2 * k, db + 2 * k, idesc, (ch > 0 || k > 0) ? 1u : 0u);
+          }
           mma_commit(empty(s));
         }
         __syncwarp();
@@ -245,26 +252,29 @@ __global__ void __launch_bounds__(kThreads, 1) estimate_tc_kernel(
   }
 }
 
-template <int S, int D>
+template <int S, int D, bool F8>
 cudaError_t launch_sd(const Problem& p, const void* q, const void* k, float* lse_part,
                       unsigned* err, cudaStream_t st) {
   const int R = p.q_len / S, Ck = p.Lk / S;
+  constexpr uint64_t es = F8 ? 1 : 2;          // bytes per element
+  constexpr uint32_t cw = F8 ? 128 : 64;       // features per 128-byte TMA row
+  auto encode = F8 ? encode_tmap_u8 : encode_tmap_bf16;
   CUtensorMap mq, mk;
   {
     const uint64_t dims[5] = {(uint64_t)D, (uint64_t)p.Hq, (uint64_t)S, (uint64_t)R,
                               (uint64_t)p.B};
-    const uint64_t strides[4] = {(uint64_t)D * 2, (uint64_t)p.Hq * D * 2,
-                                 (uint64_t)S * p.Hq * D * 2, (uint64_t)p.q_len * p.Hq * D * 2};
-    const uint32_t box[5] = {64, 1, 1, (uint32_t)kM, 1};
-    if (!encode_tmap_bf16(&mq, q, 5, dims, strides, box)) return cudaErrorInvalidValue;
+    const uint64_t strides[4] = {(uint64_t)D * es, (uint64_t)p.Hq * D * es,
+                                 (uint64_t)S * p.Hq * D * es, (uint64_t)p.q_len * p.Hq * D * es};
+    const uint32_t box[5] = {cw, 1, 1, (uint32_t)kM, 1};
+    if (!encode(&mq, q, 5, dims, strides, box)) return cudaErrorInvalidValue;
   }
   {
     const uint64_t dims[5] = {(uint64_t)D, (uint64_t)p.Hkv, (uint64_t)S, (uint64_t)Ck,
                               (uint64_t)p.B};
-    const uint64_t strides[4] = {(uint64_t)D * 2, (uint64_t)p.Hkv * D * 2,
-                                 (uint64_t)S * p.Hkv * D * 2, (uint64_t)p.Lk * p.Hkv * D * 2};
-    const uint32_t box[5] = {64, 1, 1, (uint32_t)kN, 1};
-    if (!encode_tmap_bf16(&mk, k, 5, dims, strides, box)) return cudaErrorInvalidValue;
+    const uint64_t strides[4] = {(uint64_t)D * es, (uint64_t)p.Hkv * D * es,
+                                 (uint64_t)S * p.Hkv * D * es, (uint64_t)p.Lk * p.Hkv * D * es};
+    const uint32_t box[5] = {cw, 1, 1, (uint32_t)kN, 1};
+    if (!encode(&mk, k, 5, dims, strides, box)) return cudaErrorInvalidValue;
   }
   Tiles T;
   T.Hq = p.Hq;
@@ -280,21 +290,25 @@ cudaError_t launch_sd(const Problem& p, const void* q, const void* k, float* lse
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const size_t smem = kSmemBytes + 1024;
-  e = cudaFuncSetAttribute(estimate_tc_kernel<S, D>,
+  e = cudaFuncSetAttribute(estimate_tc_kernel<S, D, F8>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const float scale_log2 = 1.4426950408889634f / (sqrtf((float)D) * (float)S);
   const int grid = T.total < sms ? T.total : sms;
-  estimate_tc_kernel<S, D><<<grid, kThreads, smem, st>>>(mq, mk, T, p.Hkv, p.nkb, scale_log2,
-                                                         lse_part, err);
+  estimate_tc_kernel<S, D, F8><<<grid, kThreads, smem, st>>>(mq, mk, T, p.Hkv, p.nkb,
+                                                             scale_log2, lse_part, err);
   return cudaGetLastError();
 }
 
 template <int S>
 cudaError_t launch_s(const Problem& p, const void* q, const void* k, float* lse_part,
                      unsigned* err, cudaStream_t st) {
-  if (p.d == 64) return launch_sd<S, 64>(p, q, k, lse_part, err, st);
-  if (p.d == 128) return launch_sd<S, 128>(p, q, k, lse_part, err, st);
+  if (p.dtype == 2) {  // e4m3: d = 128 (one 128-byte row per token)
+    if (p.d == 128) return launch_sd<S, 128, true>(p, q, k, lse_part, err, st);
+    return cudaErrorInvalidValue;
+  }
+  if (p.d == 64) return launch_sd<S, 64, false>(p, q, k, lse_part, err, st);
+  if (p.d == 128) return launch_sd<S, 128, false>(p, q, k, lse_part, err, st);
   return cudaErrorInvalidValue;
 }
 
@@ -302,7 +316,7 @@ cudaError_t launch_s(const Problem& p, const void* q, const void* k, float* lse_
 
 cudaError_t launch_estimate_tc(const Problem& p, const void* q, const void* k, int stride,
                                float* lse_part, unsigned* err, cudaStream_t st) {
-  if (p.dtype != 1) return cudaErrorInvalidValue;
+  if (p.dtype != 1 && p.dtype != 2) return cudaErrorInvalidValue;
   switch (stride) {
     case 4: return launch_s<4>(p, q, k, lse_part, err, st);
     case 8: return launch_s<8>(p, q, k, lse_part, err, st);

@@ -10,7 +10,7 @@ namespace bsx {
 
 struct Problem {
   int B, Hq, Hkv, d;
-  int dtype;        // 0 = f32, 1 = bf16
+  int dtype;        // 0 = f32, 1 = bf16, 2 = e4m3 (the estimate only)
   int q_len, q_start_pos, Lk;
   int nqb, nkb;     // q_len/128, Lk/128
 };
@@ -41,6 +41,9 @@ cudaError_t launch_estimate_tc(const Problem& p, const void* q, const void* k,
 cudaError_t launch_select(const Problem& p, int stride, float threshold,
                           const float* lse_part, uint8_t* mask, float* block_sums,
                           cudaStream_t st);
+
+// bf16 -> e4m3 bytes (round to nearest even, saturate to +-448), n values.
+cudaError_t launch_quantize_e4m3(const void* src, uint8_t* dst, long long n, cudaStream_t st);
 
 // a5: block-sparse attention on CUDA cores (any dtype, d in {64, 128}).
 cudaError_t launch_bsa_simt(const Problem& p, const void* q, const void* k,

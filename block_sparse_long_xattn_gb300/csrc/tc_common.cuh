@@ -293,6 +293,27 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, in
          | ((uint32_t)(M >> 4) << 24);   // M / 16
 }
 
+// Instruction descriptor of kind::f8f6f4 with e4m3 A and B (format code 0
+// for both), fp32 D, both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4)                       // D format: f32
+         | (0u << 7)                     // A format: e4m3
+         | (0u << 10)                    // B format: e4m3
+         | ((uint32_t)(N >> 3) << 17)    // N / 8
+         | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f8f6f4 (32 8-bit elements of K per
+// instruction: the same 32 bytes of a row as a kind::f16 instruction).
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 }  // namespace tc
 
 // Host: encode a bf16 tensor map of rank <= 5 with 128-byte swizzle.
@@ -302,5 +323,8 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, in
 // the map.
 bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                       const uint64_t* strides_bytes, const uint32_t* box);
+// The same for 8-bit elements (e4m3 bytes; box[0] <= 128).
+bool encode_tmap_u8(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                    const uint64_t* strides_bytes, const uint32_t* box);
 
 }  // namespace bsx

@@ -23,8 +23,10 @@ void resolve() {
 
 }  // namespace
 
-bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
-                      const uint64_t* strides_bytes, const uint32_t* box) {
+namespace {
+
+bool encode(CUtensorMap* map, CUtensorMapDataType type, const void* base, int rank,
+            const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box) {
   std::call_once(g_encode_once, resolve);
   if (!g_encode || rank < 1 || rank > 5) return false;
   cuuint64_t gdim[5], gstride[4];
@@ -35,12 +37,23 @@ bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64
     estride[i] = 1;
   }
   for (int i = 0; i + 1 < rank; ++i) gstride[i] = strides_bytes[i];
-  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
-                              const_cast<void*>(base), gdim, gstride, bdim, estride,
-                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  const CUresult r = g_encode(map, type, (cuuint32_t)rank, const_cast<void*>(base), gdim,
+                              gstride, bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                      const uint64_t* strides_bytes, const uint32_t* box) {
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, rank, dims, strides_bytes, box);
+}
+
+bool encode_tmap_u8(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                    const uint64_t* strides_bytes, const uint32_t* box) {
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, rank, dims, strides_bytes, box);
 }
 
 }  // namespace bsx

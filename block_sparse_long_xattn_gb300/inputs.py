@@ -43,6 +43,39 @@ def round_to_bf16(x: np.ndarray) -> np.ndarray:
     return out
 
 
+E4M3_MAX = 448.0
+
+
+def round_to_e4m3(x: np.ndarray) -> np.ndarray:
+    """Nearest e4m3 value (1 sign, 4 exponent bits with bias 7, 3 mantissa
+    bits, no infinities) to each value, ties to even, saturated to +-448;
+    returned as float32 holding those values exactly.
+
+    The spacing of e4m3 values is 2**(floor(log2|x|) - 3) from 2**-6 up and
+    2**-9 below it (subnormals); every step here is exact in float64.
+    """
+    x = np.asarray(x, np.float32).astype(np.float64)
+    a = np.abs(x)
+    _, e = np.frexp(a)                       # a = m * 2**e with m in [0.5, 1)
+    ex = np.maximum(np.where(a > 0, e - 1, -6), -6)
+    q = np.ldexp(1.0, ex - 3)
+    r = np.minimum(np.round(a / q) * q, E4M3_MAX)   # np.round: half to even
+    return np.copysign(r, x).astype(np.float32)
+
+
+def e4m3_bits(x: np.ndarray) -> np.ndarray:
+    """The e4m3 bit patterns (uint8) of e4m3-exact values."""
+    x = np.asarray(x, np.float32)
+    a = np.abs(x).astype(np.float64)
+    _, e = np.frexp(a)
+    normal = a >= 2.0 ** -6
+    exp_field = np.where(normal, e - 1 + 7, 0).astype(np.int64)
+    mant = np.where(normal, np.round((a / np.ldexp(1.0, e - 1) - 1.0) * 8.0),
+                    np.round(a / 2.0 ** -9)).astype(np.int64)
+    sign = np.signbit(x).astype(np.int64)
+    return ((sign << 7) | (exp_field << 3) | mant).astype(np.uint8)
+
+
 def bf16_bits(x: np.ndarray) -> np.ndarray:
     """The upper 16 bits of bf16-exact float32 values, as uint16."""
     x = np.ascontiguousarray(x, np.float32)

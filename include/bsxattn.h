@@ -58,7 +58,14 @@ typedef enum {
   BSX_ERR_WORKSPACE = -5
 } bsx_status;
 
-typedef enum { BSX_F32 = 0, BSX_BF16 = 1 } bsx_dtype;
+/*
+ * Element types.  BSX_F8E4M3 (fp8: 1 sign, 4 exponent, 3 mantissa bits, no
+ * infinities, largest finite value 448) is accepted by bsx_xattn_estimate and
+ * bsx_xattn_estimate_noalloc only, for q and k with d = 128: the estimator's
+ * reduced-precision operands (the pages keep the estimator in the model
+ * dtype; e4m3 K halves its largest input).  bsx_quantize_e4m3 makes them.
+ */
+typedef enum { BSX_F32 = 0, BSX_BF16 = 1, BSX_F8E4M3 = 2 } bsx_dtype;
 
 /* Problem shape shared by all calls.  Hq % Hkv == 0; d in {64, 128}. */
 typedef struct {
@@ -103,7 +110,9 @@ size_t bsx_estimate_workspace_bytes(bsx_shape s, int q_len, int q_start_pos,
  *   the block that crosses the threshold is kept; threshold >= 1 keeps every
  *   causal block; blocks after the diagonal are never kept.
  *
- * q [B,q_len,Hq,d], k [B,Lk,Hkv,d] (device, `s.dtype`).
+ * q [B,q_len,Hq,d], k [B,Lk,Hkv,d] (device, `s.dtype`: f32, bf16, or e4m3
+ * bytes with d = 128; with e4m3 the scores are those of the e4m3 values,
+ * accumulated in fp32).
  * mask (out, device) uint8 [B, Hq, q_len/128, Lk/128]; every byte written.
  * block_sums (out, device, nullable) float32 [B, Hq, q_len/128, Lk/128]:
  *   A for kb <= diag, 0 after it.
@@ -115,6 +124,16 @@ int bsx_xattn_estimate(bsx_shape s, const void* q, const void* k, int q_len,
                        int q_start_pos, int stride, float threshold,
                        uint8_t* mask, float* block_sums, void* workspace,
                        size_t workspace_bytes, void* stream);
+
+/*
+ * bf16 -> e4m3: dst[i] = the e4m3 value nearest to src[i] (ties to even
+ * mantissa), values beyond +-448 saturated to +-448, for i < n.
+ * src (device) bf16 [n]; dst (out, device) uint8 [n] (e4m3 bit patterns).
+ * Enqueued on `stream`; n == 0 enqueues nothing; NULL pointers with n > 0 or
+ * n < 0 are BSX_ERR_INVALID_ARG.  Any alignment (16-byte aligned src and
+ * 8-byte aligned dst with n % 8 == 0 take the faster path).
+ */
+int bsx_quantize_e4m3(const void* src, uint8_t* dst, long long n, void* stream);
 
 /*
  * bsx_xattn_estimate without a caller-provided workspace.  The pages have no

@@ -18,8 +18,8 @@ import torch
 
 from block_sparse_long_xattn_gb300 import (
     bsx_bsa_prefill, bsx_bsa_prefill_split, bsx_last_error, bsx_map_mask_to_cpu_blocks,
-    bsx_merge_attn, bsx_xattn_estimate)
-from block_sparse_long_xattn_gb300.inputs import CONFIGS, make_workload
+    bsx_merge_attn, bsx_quantize_e4m3, bsx_xattn_estimate)
+from block_sparse_long_xattn_gb300.inputs import CONFIGS, make_workload, round_to_e4m3
 from oracle import xattn_oracle as O
 from tests.helpers import LSE_TOL, O_TOL, check_block_sums, check_mask, to_dev
 
@@ -112,6 +112,26 @@ def test_tiny_1k_f32_full_parity():
 
 def test_llama8b_32k_chunk4096():
     _run_single_chunk("llama8b-32k-chunk4096", heads=[0, 13, 31])
+
+
+def test_llama8b_32k_chunk4096_e4m3_estimate():
+    """The 32K chunk's estimate on e4m3 Q and K, every row against the oracle's
+    estimate of the same e4m3 values; the mask's density next to bf16's."""
+    c, S, tau, _ = _cfg("llama8b-32k-chunk4096")
+    w = make_workload(seed=0, **c)
+    P = w.q_start_pos
+    est = O.xattn_estimate(round_to_e4m3(w.q), round_to_e4m3(w.k), P, S, tau)
+    q8 = bsx_quantize_e4m3(to_dev(w.q, "bf16"))
+    k8 = bsx_quantize_e4m3(to_dev(w.k, "bf16"))
+    A = torch.empty(est.block_sums.shape, dtype=torch.float32, device="cuda")
+    mask = bsx_xattn_estimate(q8, k8, P, S, tau, block_sums=A)
+    torch.cuda.synchronize()
+    A_g = A.cpu().numpy()
+    err = check_block_sums(A_g, est.block_sums, S)
+    n_rows, n_near, n_tie = check_mask(mask.cpu().numpy(), est, tau, P, A_g)
+    print(f"e4m3 estimate: {n_rows} rows, {n_near} near the threshold, {n_tie} near-tie "
+          f"swaps; block-sum max error {err:.2e}; density {_density(est.mask, P):.4f}")
+    assert bsx_last_error() == 0
 
 
 def test_llama8b_128k_chunk4096():

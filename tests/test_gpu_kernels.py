@@ -13,8 +13,10 @@ import torch
 
 from block_sparse_long_xattn_gb300 import (
     bsx_bsa_prefill, bsx_bsa_prefill_split, bsx_chunk_prefill, bsx_cpu_block_mask,
-    bsx_last_error, bsx_map_mask_to_cpu_blocks, bsx_merge_attn, bsx_xattn_estimate)
-from block_sparse_long_xattn_gb300.inputs import make_workload, random_block_mask
+    bsx_last_error, bsx_map_mask_to_cpu_blocks, bsx_merge_attn, bsx_quantize_e4m3,
+    bsx_xattn_estimate)
+from block_sparse_long_xattn_gb300.inputs import (
+    e4m3_bits, make_workload, random_block_mask, round_to_bf16, round_to_e4m3)
 from oracle import xattn_oracle as O
 from tests.helpers import LSE_TOL, O_TOL, check_block_sums, check_mask, to_dev
 
@@ -281,3 +283,49 @@ def test_whole_sequence_prefill(S, dt):
     o_ref, lse_ref = O.bsa_prefill(w.q, w.k, w.v, est.mask, 0, 0, Lk // 128)
     assert np.abs(o.float().cpu().numpy() - o_ref).max() <= O_TOL[dt]
     assert np.abs(lse.cpu().numpy() - lse_ref).max() <= LSE_TOL
+
+
+@pytest.mark.parametrize("n,offset", [(8192, 0), (1000, 0), (4096, 2)])
+def test_quantize_e4m3_bit_exact(n, offset):
+    """bf16 -> e4m3 bytes: nearest, ties to even, saturated; the 8-wide path
+    (n % 8 == 0, aligned) and the one-value path (odd n, or an offset source)."""
+    rng = np.random.default_rng(n + offset)
+    x = np.concatenate([rng.standard_normal(n // 2).astype(np.float32) * 3,
+                        rng.standard_normal(n - n // 2).astype(np.float32) * 200])
+    x[:6] = [0.0, -0.0, 448.0, 464.0, -1e5, 2.0 ** -12]
+    xb = round_to_bf16(x)
+    buf = torch.from_numpy(np.concatenate([np.zeros(offset, np.float32), xb])).to(torch.bfloat16)
+    src = buf.cuda()[offset:]
+    out = bsx_quantize_e4m3(src)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(out.view(torch.uint8).cpu().numpy(),
+                                  e4m3_bits(round_to_e4m3(xb)))
+
+
+E4M3_CASES = [
+    # (B, Hq, Hkv, Lk, P, stride, tau, alpha, n_hot), d = 128
+    (1, 4, 2, 1024, 512, 8, 0.95, 3.0, 2),
+    (2, 4, 1, 768, 256, 4, 0.9, 2.0, 1),
+    (1, 8, 2, 2048, 1536, 16, 0.9, 4.0, 3),
+    (1, 4, 2, 640, 0, 8, 0.8, 0.0, 0),
+    (1, 2, 1, 40960, 40704, 8, 0.9, 3.0, 4),   # 320 key blocks per row
+]
+
+
+@pytest.mark.parametrize("case", E4M3_CASES)
+def test_estimate_e4m3_operands(case):
+    """The estimate on e4m3 Q and K (bsx_quantize_e4m3 of bf16 inputs) against
+    the oracle's estimate of the same e4m3 values."""
+    B, Hq, Hkv, Lk, P, S, tau, alpha, n_hot = case
+    w = make_workload(seed=300 + Lk + P, B=B, Hq=Hq, Hkv=Hkv, d=128, Lk=Lk, q_start_pos=P,
+                      alpha=alpha, n_hot=n_hot, dtype="bf16")
+    est = O.xattn_estimate(round_to_e4m3(w.q), round_to_e4m3(w.k), P, S, tau)
+    q8 = bsx_quantize_e4m3(to_dev(w.q, "bf16"))
+    k8 = bsx_quantize_e4m3(to_dev(w.k, "bf16"))
+    A = torch.empty(est.block_sums.shape, dtype=torch.float32, device="cuda")
+    mask = bsx_xattn_estimate(q8, k8, P, S, tau, block_sums=A)
+    torch.cuda.synchronize()
+    A_g = A.cpu().numpy()
+    check_block_sums(A_g, est.block_sums, S)
+    check_mask(mask.cpu().numpy(), est, tau, P, A_g)
+    assert bsx_last_error() == 0
