@@ -237,8 +237,28 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
 // barrier is needed anywhere.
 constexpr int kWarpsPerCta = 4;
 
+// One bitonic stage between registers t and t + TJ of every lane (element
+// i = t * 32 + lane; partner distance 32 * TJ); descending runs where
+// (i & k) == 0.
+template <int KPL, int TJ>
+__device__ __forceinline__ void bitonic_regs(unsigned long long (&key)[KPL], int k, int lane) {
+  if constexpr (TJ < KPL) {
+#pragma unroll
+    for (int t = 0; t < KPL; ++t) {
+      if ((t & TJ) == 0) {
+        const int i = t * 32 + lane;  // lower index of the pair
+        const bool desc = (i & k) == 0;
+        const unsigned long long x = key[t], y = key[t | TJ];
+        const bool swap = desc ? (x < y) : (x > y);
+        key[t] = swap ? y : x;
+        key[t | TJ] = swap ? x : y;
+      }
+    }
+  }
+}
+
 template <int RB, int KPL>
-__global__ void __launch_bounds__(32 * kWarpsPerCta, KPL <= 8 ? 4 : 2) select_warp_kernel(
+__global__ void __launch_bounds__(32 * kWarpsPerCta, (KPL <= 8 && RB <= 16) ? 4 : 2) select_warp_kernel(
     const float* __restrict__ lse_part, int Hq, int nqb, int nkb, int R, int cur,
     float threshold, uint8_t* __restrict__ mask, float* __restrict__ block_sums) {
   constexpr int N = 32 * KPL;  // padded row length (a power of two)
@@ -258,6 +278,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta, KPL <= 8 ? 4 : 2) select_wa
   float acc[RB];
 #pragma unroll
   for (int i = 0; i < RB; ++i) acc[i] = -INFINITY;
+#pragma unroll 4
   for (int kb = lane; kb < ncausal; kb += 32) {
     const float4* q = reinterpret_cast<const float4*>(base + (long long)kb * R);
 #pragma unroll
@@ -275,6 +296,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta, KPL <= 8 ? 4 : 2) select_wa
     rmax[i] = warp_max(acc[i]);
     acc[i] = 0.f;
   }
+#pragma unroll 4
   for (int kb = lane; kb < ncausal; kb += 32) {
     const float4* q = reinterpret_cast<const float4*>(base + (long long)kb * R);
 #pragma unroll
@@ -328,22 +350,22 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta, KPL <= 8 ? 4 : 2) select_wa
                        (unsigned long long)(0xFFFFFFFFu - (unsigned)kb)
                  : 0ull;
   }
-#pragma unroll
+  // The stage loops stay rolled and only the per-register work is unrolled:
+  // the fully unrolled network of a 1024-key row overflows the instruction
+  // cache.  Register distances (partner 32 or more elements away) dispatch
+  // to bodies with a compile-time distance, so no register is indexed at
+  // run time.
+#pragma unroll 1
   for (int k = 2; k <= N; k <<= 1) {
-#pragma unroll
+#pragma unroll 1
     for (int j = k >> 1; j > 0; j >>= 1) {
       if (j >= 32) {
-        const int tj = j >> 5;
-#pragma unroll
-        for (int t = 0; t < KPL; ++t) {
-          if ((t & tj) == 0) {
-            const int i = t * 32 + lane;  // lower index of the pair
-            const bool desc = (i & k) == 0;
-            const unsigned long long x = key[t], y = key[t | tj];
-            const bool swap = desc ? (x < y) : (x > y);
-            key[t] = swap ? y : x;
-            key[t | tj] = swap ? x : y;
-          }
+        switch (j >> 5) {
+          case 1: bitonic_regs<KPL, 1>(key, k, lane); break;
+          case 2: bitonic_regs<KPL, 2>(key, k, lane); break;
+          case 4: bitonic_regs<KPL, 4>(key, k, lane); break;
+          case 8: bitonic_regs<KPL, 8>(key, k, lane); break;
+          default: bitonic_regs<KPL, 16>(key, k, lane); break;
         }
       } else {
         const bool lower = (lane & j) == 0;
