@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
   if (tid < RB) {
     float s = 0.f;
     for (int w = 0; w < kSelThreads / 32; ++w) s += red_rows[w][tid];
-    row_lse[tid] = rmax[tid] + logf(s);
+    row_lse[tid] += logf(s);  // it still holds the row max
   }
   __syncthreads();
   float rlse[RB];
@@ -350,37 +350,44 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta, (KPL <= 8 && RB <= 16) ? 4 
                        (unsigned long long)(0xFFFFFFFFu - (unsigned)kb)
                  : 0ull;
   }
-  // The stage loops stay rolled and only the per-register work is unrolled:
-  // the fully unrolled network of a 1024-key row overflows the instruction
+  // For 1024-key rows the stage loops stay rolled and only the per-register
+  // work is unrolled: their fully unrolled network overflows the instruction
   // cache.  Register distances (partner 32 or more elements away) dispatch
   // to bodies with a compile-time distance, so no register is indexed at
-  // run time.
-#pragma unroll 1
-  for (int k = 2; k <= N; k <<= 1) {
-#pragma unroll 1
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      if (j >= 32) {
-        switch (j >> 5) {
-          case 1: bitonic_regs<KPL, 1>(key, k, lane); break;
-          case 2: bitonic_regs<KPL, 2>(key, k, lane); break;
-          case 4: bitonic_regs<KPL, 4>(key, k, lane); break;
-          case 8: bitonic_regs<KPL, 8>(key, k, lane); break;
-          default: bitonic_regs<KPL, 16>(key, k, lane); break;
-        }
-      } else {
-        const bool lower = (lane & j) == 0;
+  // run time; for 256-key rows everything unrolls.
+  auto stage = [&](int k, int j) {
+    if (j >= 32) {
+      switch (j >> 5) {
+        case 1: bitonic_regs<KPL, 1>(key, k, lane); break;
+        case 2: bitonic_regs<KPL, 2>(key, k, lane); break;
+        case 4: bitonic_regs<KPL, 4>(key, k, lane); break;
+        case 8: bitonic_regs<KPL, 8>(key, k, lane); break;
+        default: bitonic_regs<KPL, 16>(key, k, lane); break;
+      }
+    } else {
+      const bool lower = (lane & j) == 0;
 #pragma unroll
-        for (int t = 0; t < KPL; ++t) {
-          const int i = t * 32 + lane;
-          const bool desc = (i & k) == 0;
-          const unsigned long long y = __shfl_xor_sync(0xffffffffu, key[t], j);
-          const unsigned long long x = key[t];
-          // the lower index keeps the larger key in a descending run
-          const bool take_max = (lower == desc);
-          key[t] = take_max ? (x > y ? x : y) : (x < y ? x : y);
-        }
+      for (int t = 0; t < KPL; ++t) {
+        const int i = t * 32 + lane;
+        const bool desc = (i & k) == 0;
+        const unsigned long long y = __shfl_xor_sync(0xffffffffu, key[t], j);
+        const unsigned long long x = key[t];
+        // the lower index keeps the larger key in a descending run
+        const bool take_max = (lower == desc);
+        key[t] = take_max ? (x > y ? x : y) : (x < y ? x : y);
       }
     }
+  };
+  if constexpr (KPL <= 8) {
+#pragma unroll
+    for (int k = 2; k <= N; k <<= 1)
+#pragma unroll
+      for (int j = k >> 1; j > 0; j >>= 1) stage(k, j);
+  } else {
+#pragma unroll 1
+    for (int k = 2; k <= N; k <<= 1)
+#pragma unroll 1
+      for (int j = k >> 1; j > 0; j >>= 1) stage(k, j);
   }
 
   // ---- exclusive scan of the sorted masses; keep while below the target ----
