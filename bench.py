@@ -230,15 +230,6 @@ def run_gpu(args):
             q, k = q8, k8
         bsx.bsx_xattn_estimate(q, k, P, S, tau, mask=mask, workspace=ws, stream=stream)
 
-    def est_e2e(q, k, v):
-        # the uploaded K has no e4m3 copy yet: quantize all of it
-        if e4m3:
-            bsx.bsx_quantize_e4m3(k, out=k8, stream=stream)
-            bsx.bsx_quantize_e4m3(q, out=q8, stream=stream)
-            bsx.bsx_xattn_estimate(q8, k8, P, S, tau, mask=mask, workspace=ws, stream=stream)
-        else:
-            est(q, k, v)
-
     def bsa(m, kb0, kb1, o, lse):
         return lambda q, k, v: bsx.bsx_bsa_prefill(q, k, v, m, P, kb0, kb1, o=o, lse=lse,
                                                    stream=stream)
@@ -311,13 +302,19 @@ def run_gpu(args):
                for j, (n, _) in enumerate(phases)}
     ms_step = float(np.mean(t_step))
 
-    # end to end through the public API: pinned host inputs in, O/LSE(/flags) out
+    # end to end through the C ABI's host-buffer entry point: pinned host Q/K/V
+    # in, O/LSE(/flags) out; bsx_chunk_step_host enqueues the uploads (V on a
+    # second stream, behind Q and K, overlapping the estimate), the step's
+    # launches and the read-back
+    fused = args.step in ("fused", "prefill")
+    offload = args.step == "offload"
+    with_keep = keep.numel() > 0 and not fused
     out_host = torch.empty(oh.shape, dtype=oh.dtype).pin_memory()
     lse_host = torch.empty(lh.shape, dtype=torch.float32).pin_memory()
-    keep_host = torch.empty(keep.shape, dtype=torch.uint8).pin_memory()
-    # Q and K go first; V is copied on a second stream while the estimate
-    # (which does not read V) runs, and the step waits for it before BSA.
-    q2, k2, v2 = (torch.empty_like(t) for t in (dq, dk, dv))
+    keep_host = torch.empty(keep.shape, dtype=torch.uint8).pin_memory() if with_keep else None
+    bufs = bsx.make_chunk_buffers(host["q"], host["k"], P, S, cpu_tokens, offload=offload,
+                                  e4m3_estimate=e4m3, fused=fused, with_keep=with_keep,
+                                  device=dev)
     copy_stream = torch.cuda.Stream(device=dev)
     e2e_ms = []
     for i in range(max(3, args.steps // 2)):
@@ -325,34 +322,17 @@ def run_gpu(args):
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        q2.copy_(host["q"], non_blocking=True)
-        k2.copy_(host["k"], non_blocking=True)
-        if args.step in ("fused", "prefill") and not e4m3:
-            v2.copy_(host["v"], non_blocking=True)
-            bsx.bsx_chunk_prefill(q2, k2, v2, P, S, tau, mask=mask, o=oh, lse=lh,
-                                  workspace=ws, stream=stream)
-        else:
-            k_in = torch.cuda.Event()
-            k_in.record(stream)
-            copy_stream.wait_event(k_in)
-            with torch.cuda.stream(copy_stream):
-                v2.copy_(host["v"], non_blocking=True)
-            v_in = torch.cuda.Event()
-            v_in.record(copy_stream)
-            est_e2e(q2, k2, v2)               # the estimate reads Q and K only
-            stream.wait_event(v_in)
-            for _, fn in phases[1:]:
-                fn(q2, k2, v2)
-        out_host.copy_(oh, non_blocking=True)
-        lse_host.copy_(lh, non_blocking=True)
-        if keep.numel() and args.step in ("chunk", "offload"):
-            keep_host.copy_(keep, non_blocking=True)
+        bsx.bsx_chunk_step_host(host["q"], host["k"], host["v"], P, S, tau, buffers=bufs,
+                                o_host=out_host, lse_host=lse_host, keep_host=keep_host,
+                                cpu_block_tokens=cpu_tokens, force_first_last=offload,
+                                offload=offload, e4m3_estimate=e4m3, fused=fused,
+                                stream=stream, copy_stream=copy_stream)
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in (out_host, lse_host))
-    if keep.numel() and args.step in ("chunk", "offload"):
+    if with_keep:
         d2h += keep_host.numel()
 
     (ms_step, ms_e2e), tokens, value = aggregate_ranks(

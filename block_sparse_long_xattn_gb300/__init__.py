@@ -9,11 +9,16 @@ raises if the library has not been built.
 from ._lib import (  # noqa: F401
     BSX_F8E4M3,
     BSX_FORCE_FIRST_LAST,
+    BSX_STEP_E4M3_ESTIMATE,
+    BSX_STEP_FUSED,
+    BSX_STEP_OFFLOAD,
+    BsxChunkBuffers,
     BsxError,
     BsxShape,
     bsx_bsa_prefill,
     bsx_bsa_prefill_split,
     bsx_chunk_prefill,
+    bsx_chunk_step_host,
     bsx_cpu_block_mask,
     bsx_estimate_workspace_bytes,
     bsx_last_error,
@@ -24,5 +29,6 @@ from ._lib import (  # noqa: F401
     bsx_xattn_estimate,
     bsx_xattn_estimate_noalloc,
     load,
+    make_chunk_buffers,
     shape_of,
 )

@@ -26,12 +26,19 @@ EXPORTS = ("bsx_version", "bsx_status_string", "bsx_estimate_workspace_bytes",
            "bsx_xattn_estimate", "bsx_bsa_prefill", "bsx_merge_attn",
            "bsx_map_mask_to_cpu_blocks", "bsx_last_error", "bsx_xattn_estimate_noalloc",
            "bsx_cpu_block_mask", "bsx_chunk_prefill", "bsx_bsa_prefill_split",
-           "bsx_quantize_e4m3")
+           "bsx_quantize_e4m3", "bsx_chunk_step_host")
+BSX_STEP_OFFLOAD, BSX_STEP_E4M3_ESTIMATE, BSX_STEP_FUSED = 2, 4, 8
 
 
 class BsxShape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int),
                 ("d", ctypes.c_int), ("dtype", ctypes.c_int)]
+
+
+class BsxChunkBuffers(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("q", "k", "v", "mask", "bsa_mask", "o", "lse", "o_curr", "lse_curr", "keep",
+                 "q8", "k8", "workspace")] + [("workspace_bytes", ctypes.c_size_t)]
 
 
 class BsxError(RuntimeError):
@@ -87,6 +94,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.bsx_cpu_block_mask.argtypes = [BsxShape, vp, i32, i32, i32, vp, vp]
         lib.bsx_last_error.restype = i32
         lib.bsx_last_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+        lib.bsx_chunk_step_host.restype = i32
+        lib.bsx_chunk_step_host.argtypes = [BsxShape, vp, vp, vp, i32, i32, i32, f32, i32, i32,
+                                            ctypes.POINTER(BsxChunkBuffers), vp, vp, vp, vp, vp]
         _lib = lib
         return lib
 
@@ -112,6 +122,16 @@ def _ptr(t):
         return None
     if not t.is_cuda:
         raise ValueError("bsxattn takes CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("bsxattn takes contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _hptr(t):
+    if t is None:
+        return None
+    if t.is_cuda:
+        raise ValueError("this argument is a host buffer")
     if not t.is_contiguous():
         raise ValueError("bsxattn takes contiguous tensors")
     return ctypes.c_void_p(t.data_ptr())
@@ -292,3 +312,74 @@ def bsx_last_error() -> int:
     if status not in (0, -4):
         raise BsxError("bsx_last_error", status)
     return int(code.value)
+
+
+def make_chunk_buffers(q_host, k_host, q_start_pos: int, stride: int,
+                       cpu_block_tokens: int = 1024, *, offload: bool = False,
+                       e4m3_estimate: bool = False, fused: bool = False,
+                       with_keep: bool = True, device=None) -> dict:
+    """Device buffers for bsx_chunk_step_host, allocated once by the caller
+    (torch) and reused across steps; the library allocates nothing."""
+    device = torch.device("cuda") if device is None else torch.device(device)
+    B, q_len, Hq, d = q_host.shape
+    Lk, Hkv = k_host.shape[1], k_host.shape[2]
+    dt = q_host.dtype
+    u8 = torch.uint8
+    n_cpu = q_start_pos // cpu_block_tokens
+    need = load().bsx_estimate_workspace_bytes(BsxShape(B, Hq, Hkv, d, _dtype_code(q_host)),
+                                               q_len, q_start_pos, stride)
+    mshape = (B, Hq, q_len // 128, Lk // 128)
+    return {
+        "q": torch.empty(q_host.shape, dtype=dt, device=device),
+        "k": torch.empty(k_host.shape, dtype=dt, device=device),
+        "v": torch.empty(k_host.shape, dtype=dt, device=device),
+        "mask": torch.empty(mshape, dtype=u8, device=device),
+        "bsa_mask": torch.empty(mshape, dtype=u8, device=device) if offload else None,
+        "o": torch.empty(q_host.shape, dtype=dt, device=device),
+        "lse": torch.empty((B, Hq, q_len), dtype=torch.float32, device=device),
+        "o_curr": None if fused else torch.empty(q_host.shape, dtype=dt, device=device),
+        "lse_curr": None if fused else torch.empty((B, Hq, q_len), dtype=torch.float32,
+                                                   device=device),
+        "keep": (torch.empty((B, n_cpu), dtype=u8, device=device)
+                 if n_cpu > 0 and (with_keep or offload) else None),
+        "q8": torch.empty(q_host.shape, dtype=u8, device=device) if e4m3_estimate else None,
+        "k8": torch.empty(k_host.shape, dtype=u8, device=device) if e4m3_estimate else None,
+        "workspace": torch.empty(max(int(need), 16), dtype=u8, device=device),
+    }
+
+
+def bsx_chunk_step_host(q_host, k_host, v_host, q_start_pos: int, stride: int,
+                        threshold: float, *, buffers: dict, o_host=None, lse_host=None,
+                        keep_host=None, cpu_block_tokens: int = 1024,
+                        force_first_last: bool = False, offload: bool = False,
+                        e4m3_estimate: bool = False, fused: bool = False, stream=None,
+                        copy_stream=None):
+    """The chunk step from (pinned) host q/k/v to host (o, lse, keep); the
+    results are valid once `stream` has completed (see bsxattn.h)."""
+    lib = load()
+    B, q_len, Hq, d = q_host.shape
+    Hkv = k_host.shape[2]
+    n_cpu = q_start_pos // cpu_block_tokens
+    if o_host is None:
+        o_host = torch.empty(q_host.shape, dtype=q_host.dtype, pin_memory=True)
+    if lse_host is None:
+        lse_host = torch.empty((B, Hq, q_len), dtype=torch.float32, pin_memory=True)
+    with_keep = n_cpu > 0 and buffers.get("keep") is not None
+    if keep_host is None and with_keep:
+        keep_host = torch.empty((B, n_cpu), dtype=torch.uint8, pin_memory=True)
+    bufs = BsxChunkBuffers(*[None if buffers.get(n) is None else _ptr(buffers[n]).value
+                             for n in
+                             ("q", "k", "v", "mask", "bsa_mask", "o", "lse", "o_curr",
+                              "lse_curr", "keep", "q8", "k8", "workspace")],
+                           buffers["workspace"].numel())
+    flags = ((BSX_FORCE_FIRST_LAST if force_first_last else 0) |
+             (BSX_STEP_OFFLOAD if offload else 0) |
+             (BSX_STEP_E4M3_ESTIMATE if e4m3_estimate else 0) |
+             (BSX_STEP_FUSED if fused else 0))
+    cs = None if copy_stream is None else ctypes.c_void_p(copy_stream.cuda_stream)
+    _check("bsx_chunk_step_host", lib.bsx_chunk_step_host(
+        BsxShape(B, Hq, Hkv, d, _dtype_code(q_host)), _hptr(q_host), _hptr(k_host),
+        _hptr(v_host), q_len, q_start_pos, stride, float(threshold), cpu_block_tokens, flags,
+        ctypes.byref(bufs), _hptr(o_host), _hptr(lse_host),
+        _hptr(keep_host) if with_keep else None, _stream(stream), cs))
+    return o_host, lse_host, keep_host

@@ -14,14 +14,17 @@
  *                            selected 128-token blocks -> O and LSE
  *   bsx_merge_attn           LSE merge of two partial (O, LSE) pairs
  *   bsx_map_mask_to_cpu_blocks  1024-token CPU-block keep flags
+ *   bsx_chunk_step_host      the whole chunk step from host inputs to host
+ *                            outputs (uploads, the four steps, read-back)
  *
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - Tensors are caller-owned, contiguous, device-resident (CUDA global
- *    memory) and 16-byte aligned.  The library never allocates, frees or
- *    copies to the host on these calls, and never synchronises: work is
- *    enqueued on `stream` (a cudaStream_t; NULL means the legacy default
- *    stream) and the call returns.
+ *    memory) and 16-byte aligned; bsx_chunk_step_host alone also takes host
+ *    buffers and copies to and from them.  The library never allocates
+ *    device memory or frees it, and never synchronises: work is enqueued on
+ *    `stream` (a cudaStream_t; NULL means the legacy default stream) and the
+ *    call returns.
  *  - Layouts are token-major:
  *        q     [B, q_len, Hq, d]            element type `dtype`
  *        k, v  [B, Lk, Hkv, d]              Lk = q_start_pos + q_len
@@ -262,6 +265,78 @@ int bsx_map_mask_to_cpu_blocks(bsx_shape s, const uint8_t* mask, int q_len,
 int bsx_cpu_block_mask(bsx_shape s, const uint8_t* keep, int q_len,
                        int q_start_pos, int cpu_block_tokens, uint8_t* mask,
                        void* stream);
+
+/* Flags for bsx_chunk_step_host (BSX_FORCE_FIRST_LAST applies there too). */
+#define BSX_STEP_OFFLOAD 2        /* attention of the pages' CPU-offload mode */
+#define BSX_STEP_E4M3_ESTIMATE 4  /* estimator on e4m3 copies of q and k */
+#define BSX_STEP_FUSED 8          /* one attention launch over all key blocks */
+
+/* Caller-owned device buffers of bsx_chunk_step_host (16-byte aligned). */
+typedef struct {
+  void* q;                /* [B,q_len,Hq,d]  receives q_host */
+  void* k;                /* [B,Lk,Hkv,d]    receives k_host */
+  void* v;                /* [B,Lk,Hkv,d]    receives v_host */
+  uint8_t* mask;          /* [B,Hq,q_len/128,Lk/128]  the estimator's mask */
+  uint8_t* bsa_mask;      /* same shape; BSX_STEP_OFFLOAD only, else NULL */
+  void* o;                /* [B,q_len,Hq,d]  history part, then the merged O */
+  float* lse;             /* [B,Hq,q_len]    history part, then the merged LSE */
+  void* o_curr;           /* [B,q_len,Hq,d]  current-chunk part; unused if fused */
+  float* lse_curr;        /* [B,Hq,q_len]    current-chunk part; unused if fused */
+  uint8_t* keep;          /* [B,q_start_pos/cpu_block_tokens] or NULL (no flags) */
+  uint8_t* q8;            /* [B,q_len,Hq,d] e4m3; BSX_STEP_E4M3_ESTIMATE only */
+  uint8_t* k8;            /* [B,Lk,Hkv,d]   e4m3; BSX_STEP_E4M3_ESTIMATE only */
+  void* workspace;        /* bsx_estimate_workspace_bytes(s, ...) bytes */
+  size_t workspace_bytes;
+} bsx_chunk_buffers;
+
+/*
+ * One chunk step of XAttention chunked prefill from host memory to host
+ * memory: the structure of nano-vllm xattn_bsa.py (select_blocks, then
+ * compute_chunked_prefill) with every input uploaded and every result read
+ * back inside the call's stream work.
+ *
+ *   q_host [B,q_len,Hq,d], k_host / v_host [B,Lk,Hkv,d]  (in, host, `s.dtype`)
+ *   -> upload into dev->q, dev->k, dev->v
+ *   -> bsx_xattn_estimate -> dev->mask
+ *   -> bsx_bsa_prefill_split -> (dev->o, dev->lse), (dev->o_curr, dev->lse_curr)
+ *   -> bsx_merge_attn into (dev->o, dev->lse)
+ *   -> bsx_map_mask_to_cpu_blocks -> dev->keep   (when dev->keep is not
+ *      NULL and q_start_pos >= cpu_block_tokens)
+ *   -> o_host [B,q_len,Hq,d], lse_host [B,Hq,q_len] float32 and, when
+ *      keep_host is not NULL, keep_host [B, q_start_pos/cpu_block_tokens]
+ *      (out, host; needs dev->keep).
+ *
+ * flags: BSX_FORCE_FIRST_LAST as for bsx_map_mask_to_cpu_blocks.
+ * BSX_STEP_OFFLOAD attends as the pages' offload mode does (the keep flags,
+ * then bsx_cpu_block_mask into dev->bsa_mask, and the split attention over
+ * that mask); the pages' offload mode also sets BSX_FORCE_FIRST_LAST.
+ * BSX_STEP_E4M3_ESTIMATE quantizes the uploaded q and k into dev->q8 and
+ * dev->k8 (bsx_quantize_e4m3) and runs the estimate on them (bf16, d = 128).
+ * BSX_STEP_FUSED replaces the split attention and the merge by one
+ * bsx_bsa_prefill over every key block into (dev->o, dev->lse), as
+ * bsx_chunk_prefill does (with q_start_pos = 0: whole-sequence prefill);
+ * dev->o_curr and dev->lse_curr are then not used and may be NULL.
+ * With BSX_STEP_OFFLOAD and q_start_pos >= cpu_block_tokens, dev->keep is
+ * required.
+ *
+ * Streams: everything is enqueued on `stream` except the upload of v, which
+ * goes on `copy_stream` after q and k (so that it overlaps the estimate,
+ * which does not read v); the attention waits for it.  copy_stream NULL or
+ * equal to stream puts the upload of v on `stream`.  The call returns
+ * without synchronising: the host outputs are valid once `stream` has
+ * completed, and the host buffers must stay untouched until then.  Host
+ * buffers should be page-locked (cudaHostAlloc / cudaHostRegister) for the
+ * copies to be asynchronous and to overlap.
+ *
+ * Every argument is validated before anything is enqueued (as the entry
+ * points above validate theirs); a CUDA error after that returns
+ * BSX_ERR_CUDA and may leave part of the step enqueued.
+ */
+int bsx_chunk_step_host(bsx_shape s, const void* q_host, const void* k_host,
+                        const void* v_host, int q_len, int q_start_pos, int stride,
+                        float threshold, int cpu_block_tokens, int flags,
+                        const bsx_chunk_buffers* dev, void* o_host, float* lse_host,
+                        uint8_t* keep_host, void* stream, void* copy_stream);
 
 /*
  * Read and clear the device error word of the current device.  Waits for

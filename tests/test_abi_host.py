@@ -94,6 +94,49 @@ def test_bsa_merge_map_reject_bad_arguments(lib):
     assert lib.bsx_map_mask_to_cpu_blocks(s, p, 128, 4096, 1024, 4, p, None) == -1
 
 
+def _host_step(lib, shape=None, q_len=256, P=1024, stride=8, tau=0.9, cpu=1024, flags=0,
+               host=64, ws=1 << 30, drop=(), **set_fields):
+    """bsx_chunk_step_host with fake, aligned, never-dereferenced pointers:
+    every case below must be rejected before anything is enqueued."""
+    shape = shape or L.BsxShape(1, 4, 2, 128, L.BSX_BF16)
+    fields = {n: 4096 for n in ("q", "k", "v", "mask", "bsa_mask", "o", "lse", "o_curr",
+                                "lse_curr", "keep", "q8", "k8", "workspace")}
+    fields.update(set_fields)
+    for n in drop:
+        fields[n] = None
+    bufs = L.BsxChunkBuffers(*[fields[n] for n in (
+        "q", "k", "v", "mask", "bsa_mask", "o", "lse", "o_curr", "lse_curr", "keep", "q8", "k8",
+        "workspace")], ws)
+    h = ctypes.c_void_p(host) if host else None
+    return lib.bsx_chunk_step_host(shape, h, h, h, q_len, P, stride, tau, cpu, flags,
+                                   ctypes.byref(bufs), h, h, h, None, None)
+
+
+def test_chunk_step_host_rejects_bad_arguments(lib):
+    assert _host_step(lib, host=0) == -1                              # host inputs required
+    assert lib.bsx_chunk_step_host(L.BsxShape(1, 4, 2, 128, 1), ctypes.c_void_p(64),
+                                   ctypes.c_void_p(64), ctypes.c_void_p(64), 256, 1024, 8, 0.9,
+                                   1024, 0, None, ctypes.c_void_p(64), ctypes.c_void_p(64),
+                                   None, None, None) == -1          # no device buffers
+    assert _host_step(lib, shape=L.BsxShape(1, 4, 2, 128, L.BSX_F8E4M3)) == -2  # e4m3 in
+    assert _host_step(lib, shape=L.BsxShape(1, 3, 2, 128, 1)) == -1   # Hq % Hkv
+    assert _host_step(lib, stride=3) == -2
+    assert _host_step(lib, tau=float("nan")) == -1
+    assert _host_step(lib, q_len=200) == -1
+    assert _host_step(lib, cpu=1000) == -1                            # cpu block % 128
+    assert _host_step(lib, P=1536, cpu=1024) == -1                    # cpu block divides P
+    assert _host_step(lib, o=4100) == -1                              # misaligned output
+    assert _host_step(lib, drop=("keep",)) == -1                      # keep_host needs keep
+    assert _host_step(lib, cpu=0) == -1                               # no division by zero
+    assert _host_step(lib, flags=2, drop=("keep",)) == -1             # offload needs keep
+    assert _host_step(lib, flags=16) == -1                            # unknown flag
+    assert _host_step(lib, drop=("o_curr",)) == -1                    # split needs o_curr
+    assert _host_step(lib, flags=2, drop=("bsa_mask",)) == -1         # offload needs its mask
+    assert _host_step(lib, flags=4, drop=("k8",)) == -1               # e4m3 needs its copies
+    assert _host_step(lib, flags=4, shape=L.BsxShape(1, 4, 2, 64, 1)) == -2  # e4m3: d = 128
+    assert _host_step(lib, ws=16) == -5                               # workspace too small
+
+
 def test_binding_requires_cuda_tensors():
     import torch
     q = torch.zeros(1, 128, 2, 64)

@@ -329,3 +329,77 @@ def test_estimate_e4m3_operands(case):
     check_block_sums(A_g, est.block_sums, S)
     check_mask(mask.cpu().numpy(), est, tau, P, A_g)
     assert bsx_last_error() == 0
+
+
+HOST_STEP_CASES = [
+    # (name, dtype, d, P, Lq, cpu, offload, force, e4m3, fused, two_streams)
+    ("chunk", "bf16", 128, 768, 512, 256, False, False, False, False, True),
+    ("one_stream", "bf16", 128, 768, 512, 256, False, True, False, False, False),
+    ("offload", "bf16", 128, 1024, 512, 256, True, True, False, False, True),
+    ("e4m3_estimate", "bf16", 128, 768, 512, 256, False, False, True, False, True),
+    ("f32", "f32", 64, 512, 256, 256, False, False, False, False, True),
+    ("first_chunk", "bf16", 128, 0, 384, 1024, False, False, False, False, True),
+    ("fused", "bf16", 128, 768, 512, 256, False, False, False, True, True),
+    ("whole_sequence", "bf16", 64, 0, 640, 1024, False, False, False, True, True),
+]
+
+
+@pytest.mark.parametrize("case", HOST_STEP_CASES, ids=[c[0] for c in HOST_STEP_CASES])
+def test_chunk_step_host(case):
+    """bsx_chunk_step_host (pinned host inputs -> host outputs, the uploads and
+    read-back inside the call's stream work) equals the same step run through
+    the device entry points bit for bit, and the oracle within the bar."""
+    from block_sparse_long_xattn_gb300 import bsx_chunk_step_host, make_chunk_buffers
+    _, dt, d, P, Lq, cpu, offload, force, e4m3, fused, two = case
+    S, tau, Hq, Hkv = 8, 0.9, 8, 2
+    w = make_workload(seed=500 + P + Lq + d, B=1, Hq=Hq, Hkv=Hkv, d=d, Lk=P + Lq,
+                      q_start_pos=P, alpha=3.0, n_hot=2, dtype=dt)
+    tdt = torch.bfloat16 if dt == "bf16" else torch.float32
+    host = [torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(tdt).pin_memory()
+            for x in (w.q, w.k, w.v)]
+    bufs = make_chunk_buffers(host[0], host[1], P, S, cpu, offload=offload, e4m3_estimate=e4m3,
+                              fused=fused)
+    stream = torch.cuda.Stream()
+    cs = torch.cuda.Stream() if two else None
+    o_h, lse_h, keep_h = bsx_chunk_step_host(
+        *host, P, S, tau, buffers=bufs, cpu_block_tokens=cpu, force_first_last=force,
+        offload=offload, e4m3_estimate=e4m3, fused=fused, stream=stream, copy_stream=cs)
+    stream.synchronize()
+    assert bsx_last_error() == 0
+
+    # the same step through the device entry points
+    q, k, v = (x.cuda() for x in host)
+    nkb, n_cpu = (P + Lq) // 128, P // cpu
+    qe, ke = (bsx_quantize_e4m3(q), bsx_quantize_e4m3(k)) if e4m3 else (q, k)
+    A = torch.empty((1, Hq, Lq // 128, nkb), dtype=torch.float32, device="cuda")
+    mask = bsx_xattn_estimate(qe, ke, P, S, tau, block_sums=A)
+    keep = bsx_map_mask_to_cpu_blocks(mask, P, cpu, force) if n_cpu else None
+    attn_mask = bsx_cpu_block_mask(keep, Lq, P, Hq, cpu) if offload else mask
+    if fused:
+        oh, lh = bsx_bsa_prefill(q, k, v, attn_mask, P, 0, nkb)
+    else:
+        oh, lh, oc, lc = bsx_bsa_prefill_split(q, k, v, attn_mask, P)
+        bsx_merge_attn(oh, lh, oc, lc)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(bufs["mask"].cpu().numpy(), mask.cpu().numpy())
+    assert torch.equal(o_h, oh.cpu()) and torch.equal(lse_h, lh.cpu())
+    if n_cpu:
+        np.testing.assert_array_equal(keep_h.numpy(), keep.cpu().numpy())
+    else:
+        assert keep_h is None
+
+    # against the oracle
+    qo, ko = (round_to_e4m3(w.q), round_to_e4m3(w.k)) if e4m3 else (w.q, w.k)
+    est = O.xattn_estimate(qo, ko, P, S, tau)
+    m_g = mask.cpu().numpy()
+    check_mask(m_g, est, tau, P, A.cpu().numpy())
+    if n_cpu:
+        np.testing.assert_array_equal(keep_h.numpy(), O.map_mask_to_cpu_blocks(m_g, P, cpu, force))
+    if offload:
+        am = O.offload_block_mask(keep_h.numpy(), Hq, Lq, P, cpu)
+        np.testing.assert_array_equal(attn_mask.cpu().numpy().astype(bool), am)
+    else:
+        am = m_g
+    o_ref, lse_ref = O.bsa_prefill(w.q, w.k, w.v, am, P, 0, nkb)
+    assert np.abs(o_h.float().numpy() - o_ref).max() <= O_TOL[dt]
+    assert np.abs(lse_h.numpy() - lse_ref).max() <= LSE_TOL
