@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
         for (int c = 0; c < 128; ++c)
           if (c > row) x[c] = -INFINITY;
       }
-      // Row max in eight independent chains of three-input max.  The
+      // Row max in eight independent chains of three-way max.  The
       // softmax warps share their schedulers with the MMA issuer and the
       // producer, so every ALU instruction saved here is issue time given
       // back to them; the exponent argument and the row sum below use the

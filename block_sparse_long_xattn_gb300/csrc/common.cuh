@@ -53,11 +53,13 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// max(a, b, c) in one instruction (three-input max.f32, sm_100 and later).
+// max(a, b, c) as two two-input maxima.  (The three-input max.f32 of PTX was
+// tried here and returned 0 for (-6.5, -inf, -inf) in one build of the
+// attention kernel while the same source built differently got it right; a
+// wrong row maximum only shifts the exponentials and stays within the output
+// tolerance, so nothing would flag it.  Plain fmaxf is what the kernels use.)
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
+  return fmaxf(fmaxf(a, b), c);
 }
 
 __device__ __forceinline__ float warp_max(float v) {
