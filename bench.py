@@ -22,6 +22,7 @@ independent replica; the path has no cross-GPU exchange).
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -42,7 +43,7 @@ DEFAULT_WORKLOAD = "llama8b-32k-chunk4096"
 METRIC = "chunked-prefill tokens/s/layer at 32K ctx; % of bf16 TC / HBM roofline"
 UNIT = "tokens/s/layer"
 DOMINANT = "bsa_prefill"
-BSA_SOURCES = ("bsa_tc.cu", "bsa_simt.cu")
+BSA_SOURCES = ("bsa_tc.cu", "bsa_simt.cu", "common.cuh", "tc_common.cuh")
 
 
 def _env_rank():
@@ -51,12 +52,14 @@ def _env_rank():
 
 
 def _peaks():
+    """(HBM GB/s, bf16 TFLOP/s burst, bf16 TFLOP/s sustained or None, source)."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
             p = json.load(f)
-        return p["hbm_gbs"], p["bf16_tflops"], "measured (MEASURED_PEAKS.json, burst)"
-    return 6800.0, 1900.0, "fallback"
+        return (p["hbm_gbs"], p["bf16_tflops"], p.get("bf16_tflops_sustained"),
+                "measured (MEASURED_PEAKS.json, burst)")
+    return 6800.0, 1900.0, 1700.0, "fallback"
 
 
 def _source_sha(names):
@@ -85,27 +88,35 @@ def _traffic_per_launch(kernel_key):
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled during the timed region."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.window = None
 
     def __enter__(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
         os.close(fd)
         try:
+            # 20 ms is about as often as the driver refreshes these values
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (FileNotFoundError, OSError):
             self.proc = None
         time.sleep(0.3)
         return self
+
+    def mark(self, t0, t1):
+        """Host wall-clock bounds of the timed region: only samples taken
+        inside it are summarised."""
+        self.window = (t0, t1)
 
     def __exit__(self, *a):
         if self.proc is not None:
@@ -124,20 +135,24 @@ class ClockSampler:
             if len(parts) < 9:
                 continue
             try:
-                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[4:]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[2]), float(parts[3]), float(parts[4]), parts[5:9]))
             except ValueError:
                 continue
         os.unlink(self.path)
+        if self.window is not None:
+            t0, t1 = self.window
+            rows = [r for r in rows if t0 <= r[0] <= t1]
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        pmax = max(r[2] for r in rows)
-        loaded = [r for r in rows if r[2] >= 0.5 * pmax] or rows
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3][1:5])
+            return {"sm_mhz": None, "sm_max_mhz": None, "samples": 0,
+                    "reasons": ["no samples inside the timed region"]}
+        reasons = sorted({self.REASONS[i] for r in rows for i, v in enumerate(r[4])
                           if v.lower() == "active"})
-        return {"sm_mhz": statistics.median(r[0] for r in loaded),
-                "sm_max_mhz": max(r[1] for r in rows),
-                "power_w_max": pmax, "samples": len(rows), "reasons": reasons}
+        return {"sm_mhz": statistics.median(r[1] for r in rows),
+                "sm_mhz_min": min(r[1] for r in rows),
+                "sm_max_mhz": max(r[2] for r in rows),
+                "power_w_max": max(r[3] for r in rows), "samples": len(rows),
+                "reasons": reasons}
 
 
 def bsa_flops(mask: np.ndarray, q_start_pos: int, kb_begin: int, kb_end: int, d: int) -> float:
@@ -291,10 +306,12 @@ def run_gpu(args):
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        t_wall0 = time.time()
         for i in range(args.steps):
             flush.zero_()
             step(dq, dk, dv, evs[i])
         torch.cuda.synchronize()
+        clk.mark(t_wall0, time.time())
     clocks = clk.summary()
     t_step = [evs[i][0].elapsed_time(evs[i][np_]) for i in range(args.steps)]
     t_phase = {n: float(np.mean([evs[i][j].elapsed_time(evs[i][j + 1])
@@ -338,7 +355,7 @@ def run_gpu(args):
     (ms_step, ms_e2e), tokens, value = aggregate_ranks(
         [ms_step, float(np.mean(e2e_ms))], B * Lq, world, dev)
 
-    hbm_peak, tc_peak, peak_src = _peaks()
+    hbm_peak, tc_peak, tc_sustained, peak_src = _peaks()
     bsa_names = [n for n, _ in phases if n in ranges]
     bsa_ms = float(np.mean([t_phase[n] for n in bsa_names]))        # mean launch
     bsa_flops_launch = float(np.mean([flops[n] for n in bsa_names]))
@@ -373,6 +390,11 @@ def run_gpu(args):
         "roofline": {"kernel": DOMINANT, "bound": "tensor", "achieved": achieved,
                      "peak": tc_peak, "unit": "TFLOP/s", "frac": achieved / tc_peak,
                      "traffic": traffic, "peak_source": peak_src,
+                     # the same launch against the cuBLAS figure sustained under
+                     # the power cap (the timed region's clock record says
+                     # whether the cap was reached: clocks.reasons)
+                     "peak_sustained": tc_sustained,
+                     "frac_vs_sustained": achieved / tc_sustained if tc_sustained else None,
                      "flops_per_launch": bsa_flops_launch, "ms_per_launch": bsa_ms},
         "kernels": kernels,
         "density": density,
@@ -452,7 +474,9 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default 200 for the GPU arm, about 0.3 s at 32K; "
+                         "20 for the reference arm, whose steps take seconds each)")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(CONFIGS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
@@ -469,6 +493,8 @@ def main():
                     help="q-heads in the oracle sample of the cpu_baseline leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    if args.steps is None:
+        args.steps = 200 if args.impl == "gb300" else 20
     if args.warmup < 3 and args.impl == "gb300":
         ap.error("at least 3 warm-up steps")
     if args.step == "prefill" and args.workload == DEFAULT_WORKLOAD:
