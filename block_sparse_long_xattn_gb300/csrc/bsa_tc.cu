@@ -16,12 +16,13 @@
 //               same buffer.
 //   warps 2..9  two softmax groups of four warps; group g takes the blocks
 //               j = g, g + 2, ... with one query row per thread (TMEM lane =
-//               row): read S, mask the diagonal block causally, online max
-//               with lazy rescaling of O_g (only when the running max grows
-//               by more than 8 in log2 units), P = exp2(x - m) as bf16 pairs
-//               written back over the consumed S columns, row sums.  At the
-//               end the two partial results (O_g, m_g, l_g) are merged per
-//               row and O and LSE go to global memory.
+//               row): read S, mask the diagonal block causally, P =
+//               exp2(x - m) as bf16 pairs written back over the consumed S
+//               columns, row sums; the running max m is raised (and O_g
+//               rescaled) only on a group's first block and when a block's
+//               row sum would exceed 2^32.  At the end the two partial
+//               results (O_g, m_g, l_g) are merged per row and O and LSE go
+//               to global memory.
 // Each group's chain S(j) -> softmax -> P V(j) -> S(j + 2) interleaves with
 // the other group's on the tensor pipe, and no per-block exchange between
 // warps is needed.  TMEM: S/P buffers in columns 0-255, O_0 and O_1 after.
@@ -38,7 +39,9 @@ using namespace tc;
 
 constexpr int kThreads = 320;   // producer, MMA issuer, 8 softmax warps
 constexpr int kRegion = 128 * 128;  // bytes of one 128-row x 64-feature bf16 tile
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// Largest row sum of one block's P accepted without raising the running max
+// first (2^32: P and the fp32 sums stay far from overflow).
+constexpr float kMaxBlockSum = 4294967296.0f;
 
 enum Site : unsigned {
   kSiteKvEmpty = 1, kSiteQFull, kSiteKvFull, kSitePFull, kSiteSFull, kSiteODoneFinal,
@@ -325,60 +328,85 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
         break;
       }
       tc_fence_after();
-      float x[128];
-      tmem_ld128(sbuf, x);
-      if (diag_last && j == n - 1) {
-        // diagonal block: key column c is visible to row r iff c <= r
+      // S(j) into registers, the diagonal block masked causally (key column c
+      // is visible to row r iff c <= r)
+      auto load_s = [&](float* x) {
+        tmem_ld128(sbuf, x);
+        if (diag_last && j == n - 1) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c > row) x[c] = -INFINITY;
-      }
-      // Row max in eight independent chains of three-way max.  The
-      // softmax warps share their schedulers with the MMA issuer and the
-      // producer, so every ALU instruction saved here is issue time given
-      // back to them; the exponent argument and the row sum below use the
-      // packed two-wide fp32 FMA/add for the same reason.
-      float mx[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) mx[e] = x[e];
-#pragma unroll
-      for (int c = 8; c < 128; c += 16)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) mx[e] = fmax3(mx[e], x[c + e], x[c + 8 + e]);
-      const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
-                             fmaxf(mx[6], mx[7])) * scale_log2;
-      const bool need = mt > m_run + kRescaleThreshold;
-      float alpha = 1.f;
-      if (need) {
-        alpha = fast_exp2(m_run - mt);  // 0 on the group's first block
-        m_run = mt;
-      }
-      // P = exp2(x * scale - m) as bf16 pairs
+          for (int c = 0; c < 128; ++c)
+            if (c > row) x[c] = -INFINITY;
+        }
+      };
+      // P = exp2(x * scale - m_run) as bf16 pairs, and the row sum.  The
+      // exponent argument and the sum use the packed two-wide fp32 FMA/add:
+      // the softmax warps share their schedulers with the MMA issuer and the
+      // producer, and the launch runs under the power cap, so every
+      // instruction saved counts.
       uint32_t pk[64];
-      float2 ps[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      float2 ps[2];
+      float alpha = 1.f;
       const float2 sc2 = make_float2(scale_log2, scale_log2);
-      const float2 nm2 = make_float2(-m_run, -m_run);
+      auto exps = [&](const float* x) {
+        ps[0] = make_float2(0.f, 0.f);
+        ps[1] = make_float2(0.f, 0.f);
+        const float2 nm2 = make_float2(-m_run, -m_run);
 #pragma unroll
-      for (int c = 0; c < 128; c += 2) {
-        const float2 t = __ffma2_rn(make_float2(x[c], x[c + 1]), sc2, nm2);
-        const float2 p = make_float2(fast_exp2(t.x), fast_exp2(t.y));
-        ps[(c >> 1) & 1] = __fadd2_rn(ps[(c >> 1) & 1], p);
-        __nv_bfloat162 b2 = __floats2bfloat162_rn(p.x, p.y);
-        pk[c >> 1] = *reinterpret_cast<uint32_t*>(&b2);
+        for (int c = 0; c < 128; c += 2) {
+          const float2 t = __ffma2_rn(make_float2(x[c], x[c + 1]), sc2, nm2);
+          const float2 p = make_float2(fast_exp2(t.x), fast_exp2(t.y));
+          ps[(c >> 1) & 1] = __fadd2_rn(ps[(c >> 1) & 1], p);
+          __nv_bfloat162 b2 = __floats2bfloat162_rn(p.x, p.y);
+          pk[c >> 1] = *reinterpret_cast<uint32_t*>(&b2);
+        }
+      };
+      // After the group's first block the running max is not raised before
+      // the exponentials: the block is exponentiated against the current
+      // m_run, which is correct for any m_run (O and l carry the same scale)
+      // as long as no P overflows.  A row sum within kMaxBlockSum bounds
+      // every P of the row; beyond it (or inf/NaN) the warp takes the slow
+      // path: the row max, the new m_run, the exponentials again and O_g
+      // rescaled.  That drops the max pass from almost every block.
+      bool slow = j < 2;
+      if (!slow) {
+        float x[128];
+        load_s(x);
+        exps(x);
+        const float sblk = (ps[0].x + ps[0].y) + (ps[1].x + ps[1].y);
+        slow = __any_sync(0xffffffffu, !(sblk <= kMaxBlockSum));
       }
-      l_run = l_run * alpha + ((ps[0].x + ps[0].y) + (ps[1].x + ps[1].y));
-      // O_g is rescaled between P V(j-2) and P V(j).  P V(j-2) is complete:
-      // the tensor pipe ran it before S(j), which we have read.
-      if (j >= 2 && __any_sync(0xffffffffu, need)) {
+      if (slow) {
+        float x[128];
+        load_s(x);  // S(j) is still in TMEM: P has not been written over it
+        // row max in eight independent chains of three-way max
+        float mx[8];
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          float t[32];
-          tmem_ld32(obuf + cc * 32, t);
+        for (int e = 0; e < 8; ++e) mx[e] = x[e];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) t[e] *= alpha;
-          tmem_st32(obuf + cc * 32, t);
+        for (int c = 8; c < 128; c += 16)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) mx[e] = fmax3(mx[e], x[c + e], x[c + 8 + e]);
+        const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                               fmaxf(mx[6], mx[7])) * scale_log2;
+        if (mt > m_run) {
+          alpha = fast_exp2(m_run - mt);  // 0 on the group's first block
+          m_run = mt;
+        }
+        exps(x);
+        // O_g is rescaled between P V(j-2) and P V(j).  P V(j-2) is
+        // complete: the tensor pipe ran it before S(j), which we have read.
+        if (j >= 2) {
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            float t[32];
+            tmem_ld32(obuf + cc * 32, t);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) t[e] *= alpha;
+            tmem_st32(obuf + cc * 32, t);
+          }
         }
       }
+      l_run = l_run * alpha + ((ps[0].x + ps[0].y) + (ps[1].x + ps[1].y));
       tmem_st64(sbuf, reinterpret_cast<const float*>(pk));  // P(j) over S(j)
       tc_fence_before();
       mbar_arrive(p_full(grp));
