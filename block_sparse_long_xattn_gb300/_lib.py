@@ -38,7 +38,8 @@ class BsxShape(ctypes.Structure):
 class BsxChunkBuffers(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("q", "k", "v", "mask", "bsa_mask", "o", "lse", "o_curr", "lse_curr", "keep",
-                 "q8", "k8", "workspace")] + [("workspace_bytes", ctypes.c_size_t)]
+                 "q8", "k8", "workspace")] + [("workspace_bytes", ctypes.c_size_t),
+                                              ("done", ctypes.c_void_p)]
 
 
 class BsxError(RuntimeError):
@@ -96,7 +97,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.bsx_last_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
         lib.bsx_chunk_step_host.restype = i32
         lib.bsx_chunk_step_host.argtypes = [BsxShape, vp, vp, vp, i32, i32, i32, f32, i32, i32,
-                                            ctypes.POINTER(BsxChunkBuffers), vp, vp, vp, vp, vp]
+                                            ctypes.POINTER(BsxChunkBuffers), vp, vp, vp, vp, vp,
+                                            vp]
         _lib = lib
         return lib
 
@@ -345,7 +347,15 @@ def make_chunk_buffers(q_host, k_host, q_start_pos: int, stride: int,
         "q8": torch.empty(q_host.shape, dtype=u8, device=device) if e4m3_estimate else None,
         "k8": torch.empty(k_host.shape, dtype=u8, device=device) if e4m3_estimate else None,
         "workspace": torch.empty(max(int(need), 16), dtype=u8, device=device),
+        "done": _recorded_event(device),
     }
+
+
+def _recorded_event(device):
+    """A CUDA event that exists (torch creates events on first record)."""
+    ev = torch.cuda.Event()
+    ev.record(torch.cuda.current_stream(device))
+    return ev
 
 
 def bsx_chunk_step_host(q_host, k_host, v_host, q_start_pos: int, stride: int,
@@ -353,9 +363,10 @@ def bsx_chunk_step_host(q_host, k_host, v_host, q_start_pos: int, stride: int,
                         keep_host=None, cpu_block_tokens: int = 1024,
                         force_first_last: bool = False, offload: bool = False,
                         e4m3_estimate: bool = False, fused: bool = False, stream=None,
-                        copy_stream=None):
+                        upload_stream=None, download_stream=None):
     """The chunk step from (pinned) host q/k/v to host (o, lse, keep); the
-    results are valid once `stream` has completed (see bsxattn.h)."""
+    results are valid once `download_stream` (default: `stream`) has
+    completed, or buffers["done"] has (see bsxattn.h)."""
     lib = load()
     B, q_len, Hq, d = q_host.shape
     Hkv = k_host.shape[2]
@@ -367,19 +378,22 @@ def bsx_chunk_step_host(q_host, k_host, v_host, q_start_pos: int, stride: int,
     with_keep = n_cpu > 0 and buffers.get("keep") is not None
     if keep_host is None and with_keep:
         keep_host = torch.empty((B, n_cpu), dtype=torch.uint8, pin_memory=True)
+    done = buffers.get("done")
     bufs = BsxChunkBuffers(*[None if buffers.get(n) is None else _ptr(buffers[n]).value
                              for n in
                              ("q", "k", "v", "mask", "bsa_mask", "o", "lse", "o_curr",
                               "lse_curr", "keep", "q8", "k8", "workspace")],
-                           buffers["workspace"].numel())
+                           buffers["workspace"].numel(),
+                           None if done is None else done.cuda_event)
     flags = ((BSX_FORCE_FIRST_LAST if force_first_last else 0) |
              (BSX_STEP_OFFLOAD if offload else 0) |
              (BSX_STEP_E4M3_ESTIMATE if e4m3_estimate else 0) |
              (BSX_STEP_FUSED if fused else 0))
-    cs = None if copy_stream is None else ctypes.c_void_p(copy_stream.cuda_stream)
+    us = None if upload_stream is None else ctypes.c_void_p(upload_stream.cuda_stream)
+    ds = None if download_stream is None else ctypes.c_void_p(download_stream.cuda_stream)
     _check("bsx_chunk_step_host", lib.bsx_chunk_step_host(
         BsxShape(B, Hq, Hkv, d, _dtype_code(q_host)), _hptr(q_host), _hptr(k_host),
         _hptr(v_host), q_len, q_start_pos, stride, float(threshold), cpu_block_tokens, flags,
         ctypes.byref(bufs), _hptr(o_host), _hptr(lse_host),
-        _hptr(keep_host) if with_keep else None, _stream(stream), cs))
+        _hptr(keep_host) if with_keep else None, _stream(stream), us, ds))
     return o_host, lse_host, keep_host

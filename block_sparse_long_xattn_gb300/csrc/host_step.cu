@@ -1,7 +1,7 @@
 // bsx_chunk_step_host: one chunk step from host buffers to host buffers.
-// Uploads, the step's launches and the read-back are all enqueued here; the
-// upload of V runs on a second stream so that it overlaps the estimate (which
-// reads Q and K only) and the attention waits for it by an event.
+// Uploads, the step's launches and the read-back are all enqueued here, each
+// on its own stream and ordered by events, so that a caller alternating two
+// buffer sets overlaps one step's copies with the other step's launches.
 #include <stdio.h>
 
 #include "../../include/bsxattn.h"
@@ -56,18 +56,48 @@ int validate(const bsx_shape& s, const void* qh, const void* kh, const void* vh,
 
 }  // namespace
 
+namespace {
+
+// Events of one call, created with timing off and destroyed before the call
+// returns: an event destroyed while its record is still pending is released
+// once the device has passed it.
+struct CallEvents {
+  cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
+  cudaError_t make(int n) {
+    for (int i = 0; i < n; ++i) {
+      cudaError_t e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
+  ~CallEvents() {
+    for (cudaEvent_t e : ev)
+      if (e) cudaEventDestroy(e);
+  }
+};
+
+// `dst` waits for everything enqueued on `src` so far
+cudaError_t follow(cudaStream_t dst, cudaStream_t src, cudaEvent_t ev) {
+  cudaError_t e = cudaEventRecord(ev, src);
+  return e == cudaSuccess ? cudaStreamWaitEvent(dst, ev, 0) : e;
+}
+
+}  // namespace
+
 extern "C" int bsx_chunk_step_host(bsx_shape s, const void* q_host, const void* k_host,
                                    const void* v_host, int q_len, int q_start_pos, int stride,
                                    float threshold, int cpu_block_tokens, int flags,
                                    const bsx_chunk_buffers* dev, void* o_host, float* lse_host,
-                                   uint8_t* keep_host, void* stream, void* copy_stream) {
+                                   uint8_t* keep_host, void* stream, void* upload_stream,
+                                   void* download_stream) {
   const int P = q_start_pos;
   int rc = validate(s, q_host, k_host, v_host, q_len, P, stride, threshold, cpu_block_tokens,
                     flags, dev, o_host, lse_host, keep_host);
   if (rc != BSX_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaStream_t cs = static_cast<cudaStream_t>(copy_stream);
-  const bool two_streams = cs != nullptr && cs != st;
+  cudaStream_t up = upload_stream ? static_cast<cudaStream_t>(upload_stream) : st;
+  cudaStream_t dn = download_stream ? static_cast<cudaStream_t>(download_stream) : st;
+  cudaEvent_t done = static_cast<cudaEvent_t>(dev->done);
   const size_t elt = s.dtype == BSX_BF16 ? 2 : 4;
   const long long Lk = (long long)P + q_len;
   const size_t q_elems = (size_t)s.B * q_len * s.Hq * s.d;
@@ -76,34 +106,28 @@ extern "C" int bsx_chunk_step_host(bsx_shape s, const void* q_host, const void* 
   const int n_cpu = P / cpu_block_tokens;
   const bool fused = flags & BSX_STEP_FUSED;
   const bool map = n_cpu > 0 && dev->keep != nullptr;
-
-  // uploads: Q and K first (the estimate needs them), V behind them
-  cudaError_t e = cudaMemcpyAsync(dev->q, q_host, q_elems * elt, cudaMemcpyHostToDevice, st);
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(dev->k, k_host, kv_elems * elt, cudaMemcpyHostToDevice, st);
+  CallEvents ev;  // [0] Q and K uploaded, [1] V uploaded, [2] results ready
+  cudaError_t e = ev.make(3);
   if (e != cudaSuccess) return cuda_fail(e);
-  cudaEvent_t qk_in = nullptr, v_in = nullptr;
-  if (two_streams) {
-    e = cudaEventCreateWithFlags(&qk_in, cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&v_in, cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventRecord(qk_in, st);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, qk_in, 0);
-    if (e == cudaSuccess)
-      e = cudaMemcpyAsync(dev->v, v_host, kv_elems * elt, cudaMemcpyHostToDevice, cs);
-    if (e == cudaSuccess) e = cudaEventRecord(v_in, cs);
-  } else {
-    e = cudaMemcpyAsync(dev->v, v_host, kv_elems * elt, cudaMemcpyHostToDevice, st);
+
+  // The previous step on these buffers has been read back before they are
+  // written again (its compute read q, k, v; its read-back reads o, lse, keep).
+  if (done) {
+    e = cudaStreamWaitEvent(up, done, 0);
+    if (e == cudaSuccess && st != up) e = cudaStreamWaitEvent(st, done, 0);
+    if (e != cudaSuccess) return cuda_fail(e);
   }
-  // an event may be destroyed while its record is pending: it is released
-  // once the device has passed it
-  auto release = [&] {
-    if (qk_in) cudaEventDestroy(qk_in);
-    if (v_in) cudaEventDestroy(v_in);
-  };
-  if (e != cudaSuccess) {
-    release();
-    return cuda_fail(e);
-  }
+
+  // uploads: Q and K first (the estimate needs them), V behind them, so that
+  // V's copy overlaps the estimate, which does not read it
+  e = cudaMemcpyAsync(dev->q, q_host, q_elems * elt, cudaMemcpyHostToDevice, up);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(dev->k, k_host, kv_elems * elt, cudaMemcpyHostToDevice, up);
+  if (e == cudaSuccess && up != st) e = follow(st, up, ev.ev[0]);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(dev->v, v_host, kv_elems * elt, cudaMemcpyHostToDevice, up);
+  if (e == cudaSuccess && up != st) e = cudaEventRecord(ev.ev[1], up);
+  if (e != cudaSuccess) return cuda_fail(e);
 
   // estimate (on e4m3 copies of the uploaded Q and K when asked)
   const void* qe = dev->q;
@@ -119,9 +143,8 @@ extern "C" int bsx_chunk_step_host(bsx_shape s, const void* q_host, const void* 
   if (rc == BSX_OK)
     rc = bsx_xattn_estimate(se, qe, ke, q_len, P, stride, threshold, dev->mask, nullptr,
                             dev->workspace, dev->workspace_bytes, st);
-  if (rc == BSX_OK && two_streams && cudaStreamWaitEvent(st, v_in, 0) != cudaSuccess)
+  if (rc == BSX_OK && up != st && cudaStreamWaitEvent(st, ev.ev[1], 0) != cudaSuccess)
     rc = BSX_ERR_CUDA;
-  release();
   if (rc != BSX_OK) return rc;
 
   // attention: history and current chunk in one launch, then the LSE merge
@@ -151,10 +174,14 @@ extern "C" int bsx_chunk_step_host(bsx_shape s, const void* q_host, const void* 
                                     dev->keep, st);
   if (rc != BSX_OK) return rc;
 
-  // read-back
-  e = cudaMemcpyAsync(o_host, dev->o, q_elems * elt, cudaMemcpyDeviceToHost, st);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(lse_host, dev->lse, lse_bytes, cudaMemcpyDeviceToHost, st);
+  // read-back, after the step's launches
+  e = dn != st ? follow(dn, st, ev.ev[2]) : cudaSuccess;
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(o_host, dev->o, q_elems * elt, cudaMemcpyDeviceToHost, dn);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(lse_host, dev->lse, lse_bytes, cudaMemcpyDeviceToHost, dn);
   if (e == cudaSuccess && keep_host && map)
-    e = cudaMemcpyAsync(keep_host, dev->keep, (size_t)s.B * n_cpu, cudaMemcpyDeviceToHost, st);
+    e = cudaMemcpyAsync(keep_host, dev->keep, (size_t)s.B * n_cpu, cudaMemcpyDeviceToHost, dn);
+  if (e == cudaSuccess && done) e = cudaEventRecord(done, dn);
   return e == cudaSuccess ? BSX_OK : cuda_fail(e);
 }

@@ -287,6 +287,7 @@ typedef struct {
   uint8_t* k8;            /* [B,Lk,Hkv,d]   e4m3; BSX_STEP_E4M3_ESTIMATE only */
   void* workspace;        /* bsx_estimate_workspace_bytes(s, ...) bytes */
   size_t workspace_bytes;
+  void* done;             /* a cudaEvent_t, or NULL; see bsx_chunk_step_host */
 } bsx_chunk_buffers;
 
 /*
@@ -319,14 +320,20 @@ typedef struct {
  * With BSX_STEP_OFFLOAD and q_start_pos >= cpu_block_tokens, dev->keep is
  * required.
  *
- * Streams: everything is enqueued on `stream` except the upload of v, which
- * goes on `copy_stream` after q and k (so that it overlaps the estimate,
- * which does not read v); the attention waits for it.  copy_stream NULL or
- * equal to stream puts the upload of v on `stream`.  The call returns
- * without synchronising: the host outputs are valid once `stream` has
- * completed, and the host buffers must stay untouched until then.  Host
- * buffers should be page-locked (cudaHostAlloc / cudaHostRegister) for the
- * copies to be asynchronous and to overlap.
+ * Streams: the uploads go on `upload_stream` (q and k, then v), the launches
+ * on `stream`, the read-back on `download_stream`; events order them (the
+ * estimate waits for q and k, the attention for v as well, the read-back for
+ * the launches), so v's upload overlaps the estimate, which does not read it.
+ * upload_stream or download_stream NULL means `stream`.  When dev->done is
+ * a CUDA event, the call first makes upload_stream and stream wait for it
+ * and records it after the read-back: a caller that alternates two buffer
+ * sets (each with its own event) on the same three streams overlaps one
+ * step's uploads and read-back with the other step's launches, and no
+ * buffer is written before the step that used it last has been read back.
+ * The call returns without synchronising: the host outputs are valid once
+ * download_stream has completed (or dev->done has), and the host buffers
+ * must stay untouched until then.  Host buffers should be page-locked
+ * (cudaHostAlloc / cudaHostRegister) for the copies to be asynchronous.
  *
  * Every argument is validated before anything is enqueued (as the entry
  * points above validate theirs); a CUDA error after that returns
@@ -336,7 +343,8 @@ int bsx_chunk_step_host(bsx_shape s, const void* q_host, const void* k_host,
                         const void* v_host, int q_len, int q_start_pos, int stride,
                         float threshold, int cpu_block_tokens, int flags,
                         const bsx_chunk_buffers* dev, void* o_host, float* lse_host,
-                        uint8_t* keep_host, void* stream, void* copy_stream);
+                        uint8_t* keep_host, void* stream, void* upload_stream,
+                        void* download_stream);
 
 /*
  * Read and clear the device error word of the current device.  Waits for

@@ -106,10 +106,10 @@ def _host_step(lib, shape=None, q_len=256, P=1024, stride=8, tau=0.9, cpu=1024, 
         fields[n] = None
     bufs = L.BsxChunkBuffers(*[fields[n] for n in (
         "q", "k", "v", "mask", "bsa_mask", "o", "lse", "o_curr", "lse_curr", "keep", "q8", "k8",
-        "workspace")], ws)
+        "workspace")], ws, None)
     h = ctypes.c_void_p(host) if host else None
     return lib.bsx_chunk_step_host(shape, h, h, h, q_len, P, stride, tau, cpu, flags,
-                                   ctypes.byref(bufs), h, h, h, None, None)
+                                   ctypes.byref(bufs), h, h, h, None, None, None)
 
 
 def test_chunk_step_host_rejects_bad_arguments(lib):
@@ -117,7 +117,7 @@ def test_chunk_step_host_rejects_bad_arguments(lib):
     assert lib.bsx_chunk_step_host(L.BsxShape(1, 4, 2, 128, 1), ctypes.c_void_p(64),
                                    ctypes.c_void_p(64), ctypes.c_void_p(64), 256, 1024, 8, 0.9,
                                    1024, 0, None, ctypes.c_void_p(64), ctypes.c_void_p(64),
-                                   None, None, None) == -1          # no device buffers
+                                   None, None, None, None) == -1    # no device buffers
     assert _host_step(lib, shape=L.BsxShape(1, 4, 2, 128, L.BSX_F8E4M3)) == -2  # e4m3 in
     assert _host_step(lib, shape=L.BsxShape(1, 3, 2, 128, 1)) == -1   # Hq % Hkv
     assert _host_step(lib, stride=3) == -2

@@ -360,11 +360,12 @@ def test_chunk_step_host(case):
     bufs = make_chunk_buffers(host[0], host[1], P, S, cpu, offload=offload, e4m3_estimate=e4m3,
                               fused=fused)
     stream = torch.cuda.Stream()
-    cs = torch.cuda.Stream() if two else None
+    us, ds = (torch.cuda.Stream(), torch.cuda.Stream()) if two else (None, None)
     o_h, lse_h, keep_h = bsx_chunk_step_host(
         *host, P, S, tau, buffers=bufs, cpu_block_tokens=cpu, force_first_last=force,
-        offload=offload, e4m3_estimate=e4m3, fused=fused, stream=stream, copy_stream=cs)
-    stream.synchronize()
+        offload=offload, e4m3_estimate=e4m3, fused=fused, stream=stream, upload_stream=us,
+        download_stream=ds)
+    (ds or stream).synchronize()
     assert bsx_last_error() == 0
 
     # the same step through the device entry points
@@ -403,3 +404,32 @@ def test_chunk_step_host(case):
     o_ref, lse_ref = O.bsa_prefill(w.q, w.k, w.v, am, P, 0, nkb)
     assert np.abs(o_h.float().numpy() - o_ref).max() <= O_TOL[dt]
     assert np.abs(lse_h.numpy() - lse_ref).max() <= LSE_TOL
+
+
+def test_chunk_step_host_pipelined_buffer_sets():
+    """Two buffer sets alternating on the same three streams (each step's
+    uploads and read-back overlapping the other set's launches), four steps
+    with different inputs: every step's host outputs equal the same step run
+    alone."""
+    from block_sparse_long_xattn_gb300 import bsx_chunk_step_host, make_chunk_buffers
+    P, Lq, S, tau, cpu = 768, 512, 8, 0.9, 256
+    ws = [make_workload(seed=900 + i, B=1, Hq=8, Hkv=2, d=128, Lk=P + Lq, q_start_pos=P,
+                        alpha=3.0, n_hot=2, dtype="bf16") for i in range(4)]
+    hosts = [[torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.bfloat16)
+              .pin_memory() for x in (w.q, w.k, w.v)] for w in ws]
+    sets = [make_chunk_buffers(hosts[0][0], hosts[0][1], P, S, cpu) for _ in range(2)]
+    st, us, ds = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    outs = [bsx_chunk_step_host(*hosts[i], P, S, tau, buffers=sets[i % 2], cpu_block_tokens=cpu,
+                                stream=st, upload_stream=us, download_stream=ds)
+            for i in range(4)]
+    ds.synchronize()
+    assert bsx_last_error() == 0
+    for i in range(4):
+        alone = make_chunk_buffers(hosts[i][0], hosts[i][1], P, S, cpu)
+        o, lse, keep = bsx_chunk_step_host(*hosts[i], P, S, tau, buffers=alone,
+                                           cpu_block_tokens=cpu)
+        torch.cuda.synchronize()
+        assert torch.equal(outs[i][0], o) and torch.equal(outs[i][1], lse)
+        assert torch.equal(outs[i][2], keep)
+    # different inputs gave different outputs (the sets were not mixed up)
+    assert not torch.equal(outs[0][0], outs[1][0])
