@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = grp; j < n; j += 2) {
-      if (!mbar_wait(s_full(grp), (j >> 1) & 1, abort_flag, err, kErrBsaTc, kSiteSFull)) {
+      if (!mbar_wait_warp(s_full(grp), (j >> 1) & 1, abort_flag, err, kErrBsaTc, kSiteSFull)) {
         ok = false;
         break;
       }
@@ -417,10 +417,11 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
     xm[(grp * 2 + 1) * 128 + row] = l_run;
     const int j_last = ((n - 1 - grp) >= 0) ? n - 1 - ((n - 1 - grp) & 1) : -1;
     if (ok && j_last >= 0 &&
-        !mbar_wait(o_done(grp), (j_last >> 1) & 1, abort_flag, err, kErrBsaTc, kSiteODoneFinal))
+        !mbar_wait_warp(o_done(grp), (j_last >> 1) & 1, abort_flag, err, kErrBsaTc,
+                        kSiteODoneFinal))
       ok = false;
     mbar_arrive(xbar);
-    if (!mbar_wait(xbar, 0, abort_flag, err, kErrBsaTc, kSiteXchg)) ok = false;
+    if (!mbar_wait_warp(xbar, 0, abort_flag, err, kErrBsaTc, kSiteXchg)) ok = false;
     if (ok) {
       tc_fence_after();
       const float m0 = xm[0 * 128 + row], l0 = xm[1 * 128 + row];

@@ -235,8 +235,8 @@ __global__ void __launch_bounds__(kThreads, 1) estimate_tc_kernel(
     int ti = 0;
     for (int t = cl; t < T.total; t += ncl, ++ti) {
       const int buf = ti & 1;
-      if (!mbar_wait(acc_full(buf), (ti >> 1) & 1, abort_flag, err, kErrEstimateTc,
-                     kSiteAccFull))
+      if (!mbar_wait_warp(acc_full(buf), (ti >> 1) & 1, abort_flag, err, kErrEstimateTc,
+                          kSiteAccFull))
         break;
       tc_fence_after();
       int b, h, rp, kt;

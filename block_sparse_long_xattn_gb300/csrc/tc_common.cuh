@@ -108,6 +108,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// mbar_wait with one result for the whole (converged) warp: warps that go on
+// to warp-collective tcgen05 loads and stores must leave a wait together,
+// never some lanes through the timeout and others through the phase.  One
+// vote on the fast probe; the bounded wait and a second vote only when a lane
+// found the phase open.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort,
+                                               unsigned* err, unsigned kernel, unsigned site) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, err, kernel, site));
+}
+
 // ---------------------------------------------------------------------------
 // TMA
 // ---------------------------------------------------------------------------
