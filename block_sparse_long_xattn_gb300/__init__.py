@@ -20,6 +20,7 @@ from ._lib import (  # noqa: F401
     bsx_chunk_prefill,
     bsx_chunk_step_host,
     bsx_cpu_block_mask,
+    bsx_debug_drop_ring_item,
     bsx_estimate_workspace_bytes,
     bsx_last_error,
     bsx_map_mask_to_cpu_blocks,

@@ -26,7 +26,7 @@ EXPORTS = ("bsx_version", "bsx_status_string", "bsx_estimate_workspace_bytes",
            "bsx_xattn_estimate", "bsx_bsa_prefill", "bsx_merge_attn",
            "bsx_map_mask_to_cpu_blocks", "bsx_last_error", "bsx_xattn_estimate_noalloc",
            "bsx_cpu_block_mask", "bsx_chunk_prefill", "bsx_bsa_prefill_split",
-           "bsx_quantize_e4m3", "bsx_chunk_step_host")
+           "bsx_quantize_e4m3", "bsx_chunk_step_host", "bsx_debug_drop_ring_item")
 BSX_STEP_OFFLOAD, BSX_STEP_E4M3_ESTIMATE, BSX_STEP_FUSED = 2, 4, 8
 
 
@@ -95,6 +95,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.bsx_cpu_block_mask.argtypes = [BsxShape, vp, i32, i32, i32, vp, vp]
         lib.bsx_last_error.restype = i32
         lib.bsx_last_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+        lib.bsx_debug_drop_ring_item.restype = i32
+        lib.bsx_debug_drop_ring_item.argtypes = [i32, i32]
         lib.bsx_chunk_step_host.restype = i32
         lib.bsx_chunk_step_host.argtypes = [BsxShape, vp, vp, vp, i32, i32, i32, f32, i32, i32,
                                             ctypes.POINTER(BsxChunkBuffers), vp, vp, vp, vp, vp,
@@ -305,6 +307,13 @@ def bsx_cpu_block_mask(keep, q_len: int, q_start_pos: int, Hq: int,
         shape, _ptr(keep) if keep.numel() else None, q_len, q_start_pos, cpu_block_tokens,
         _ptr(mask), _stream(stream)))
     return mask
+
+
+def bsx_debug_drop_ring_item(cta: int, item: int) -> None:
+    """Failure-path test hook: the calling thread's next bf16 attention launch
+    has CTA `cta` stop loading before K/V ring item `item`, so its bounded
+    waits run out and the error word records it (see bsxattn.h)."""
+    _check("bsx_debug_drop_ring_item", load().bsx_debug_drop_ring_item(cta, item))
 
 
 def bsx_last_error() -> int:

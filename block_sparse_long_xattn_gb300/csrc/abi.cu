@@ -65,6 +65,16 @@ int cuda_status(cudaError_t e) {
 
 constexpr int kMaxKeyBlocks = 8192;  // selection sorts up to this many blocks per row
 
+// Failure-path test hook (bsx_debug_drop_ring_item): armed per host thread,
+// consumed by the next tcgen05 attention launch of that thread.
+thread_local bsx::BsaDrop t_drop;
+
+bsx::BsaDrop take_drop() {
+  const bsx::BsaDrop d = t_drop;
+  t_drop = bsx::BsaDrop();
+  return d;
+}
+
 }  // namespace
 
 extern "C" {
@@ -130,7 +140,7 @@ int bsx_bsa_prefill(bsx_shape s, const void* q, const void* k, const void* v,
     // tcgen05 path: one 128-row q-tile per CTA, up to kMaxKeyBlocks per row
     if (kb_end - kb_begin > kMaxKeyBlocks) return BSX_ERR_UNSUPPORTED;
     const bsx::BsaRange r{kb_begin, kb_end, o, lse};
-    e = bsx::launch_bsa_tc(p, q, k, v, mask, 1, &r, err_word(), st);
+    e = bsx::launch_bsa_tc(p, q, k, v, mask, 1, &r, err_word(), st, take_drop());
   } else {
     e = bsx::launch_bsa_simt(p, q, k, v, mask, kb_begin, kb_end, o, lse, st);
   }
@@ -155,7 +165,7 @@ int bsx_bsa_prefill_split(bsx_shape s, const void* q, const void* k, const void*
     if (cur > kMaxKeyBlocks || p.nkb - cur > kMaxKeyBlocks) return BSX_ERR_UNSUPPORTED;
     // history CTAs (the long ones) first, the current chunk's fill the tail
     const bsx::BsaRange r[2] = {{0, cur, o_hist, lse_hist}, {cur, p.nkb, o_curr, lse_curr}};
-    e = bsx::launch_bsa_tc(p, q, k, v, mask, 2, r, err_word(), st);
+    e = bsx::launch_bsa_tc(p, q, k, v, mask, 2, r, err_word(), st, take_drop());
   } else {
     e = bsx::launch_bsa_simt(p, q, k, v, mask, 0, cur, o_hist, lse_hist, st);
     if (e == cudaSuccess)
@@ -220,6 +230,13 @@ int bsx_cpu_block_mask(bsx_shape s, const uint8_t* keep, int q_len, int q_start_
   if (!mask || (q_start_pos > 0 && !keep)) return BSX_ERR_INVALID_ARG;
   return cuda_status(bsx::launch_cpu_block_mask(p, keep, cpu_block_tokens, mask,
                                                 static_cast<cudaStream_t>(stream)));
+}
+
+int bsx_debug_drop_ring_item(int cta, int item) {
+  if (cta >= 0 && item < 0) return BSX_ERR_INVALID_ARG;
+  t_drop.cta = cta < 0 ? -1 : cta;
+  t_drop.item = cta < 0 ? -1 : item;
+  return BSX_OK;
 }
 
 int bsx_last_error(unsigned int* code) {

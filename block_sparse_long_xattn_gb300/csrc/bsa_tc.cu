@@ -73,6 +73,9 @@ struct BsaPart {
 struct BsaParts {
   BsaPart p0, p1;
   int B, nqb;
+  // failure-path test hook: CTA drop_cta's producer stops before ring item
+  // drop_item (no copy, no arrival), so its consumers' bounded waits run out
+  int drop_cta, drop_item;
 };
 
 template <int D>
@@ -203,6 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
         } else {
           blk = i == 2 * n - 1 ? n - 1 : (i - 2) / 2;
         }
+        if ((int)blockIdx.x == parts.drop_cta && i == parts.drop_item) break;
         const int s = i % L::kSlots;
         if (i >= L::kSlots &&
             !mbar_wait(slot_empty(s), ((i / L::kSlots) - 1) & 1, abort_flag, err, kErrBsaTc,
@@ -482,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
 template <int D>
 cudaError_t launch_d(const Problem& p, const void* q, const void* k, const void* v,
                      const uint8_t* mask, int nparts, const BsaRange* ranges, unsigned* err,
-                     cudaStream_t st) {
+                     BsaDrop drop, cudaStream_t st) {
   using L = Layout<D>;
   CUtensorMap mq, mk, mv;
   const uint32_t box[4] = {64, 1, 128, 1};
@@ -507,6 +511,8 @@ cudaError_t launch_d(const Problem& p, const void* q, const void* k, const void*
   BsaParts parts;
   parts.B = p.B;
   parts.nqb = p.nqb;
+  parts.drop_cta = drop.cta;
+  parts.drop_item = drop.item;
   parts.p0 = {ranges[0].kb_begin, ranges[0].kb_end, static_cast<__nv_bfloat16*>(ranges[0].o),
               ranges[0].lse};
   parts.p1 = nparts > 1 ? BsaPart{ranges[1].kb_begin, ranges[1].kb_end,
@@ -522,10 +528,10 @@ cudaError_t launch_d(const Problem& p, const void* q, const void* k, const void*
 
 cudaError_t launch_bsa_tc(const Problem& p, const void* q, const void* k, const void* v,
                           const uint8_t* mask, int nparts, const BsaRange* ranges,
-                          unsigned* err, cudaStream_t st) {
+                          unsigned* err, cudaStream_t st, BsaDrop drop) {
   if (p.dtype != 1 || nparts < 1 || nparts > 2) return cudaErrorInvalidValue;
-  if (p.d == 64) return launch_d<64>(p, q, k, v, mask, nparts, ranges, err, st);
-  if (p.d == 128) return launch_d<128>(p, q, k, v, mask, nparts, ranges, err, st);
+  if (p.d == 64) return launch_d<64>(p, q, k, v, mask, nparts, ranges, err, drop, st);
+  if (p.d == 128) return launch_d<128>(p, q, k, v, mask, nparts, ranges, err, drop, st);
   return cudaErrorInvalidValue;
 }
 

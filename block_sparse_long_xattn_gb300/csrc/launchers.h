@@ -60,8 +60,14 @@ struct BsaRange {
 // a5: block-sparse attention on tcgen05 tensor cores (bf16), for one or two
 // key-block ranges of the same queries in a single launch (the ranges' CTAs
 // run in order, range 0 first).
+// Failure-path test hook of launch_bsa_tc: CTA `cta` (linear grid index) stops
+// loading before ring item `item`; cta < 0 disables it.
+struct BsaDrop {
+  int cta = -1, item = -1;
+};
 cudaError_t launch_bsa_tc(const Problem& p, const void* q, const void* k,
                           const void* v, const uint8_t* mask, int nparts,
-                          const BsaRange* ranges, unsigned* err, cudaStream_t st);
+                          const BsaRange* ranges, unsigned* err, cudaStream_t st,
+                          BsaDrop drop = BsaDrop());
 
 }  // namespace bsx

@@ -347,6 +347,24 @@ int bsx_chunk_step_host(bsx_shape s, const void* q_host, const void* k_host,
                         void* download_stream);
 
 /*
+ * Test hook for the failure path (not for production use).  Arms, for the
+ * calling host thread only, the next bf16 bsx_bsa_prefill or
+ * bsx_bsa_prefill_split launch (including those made by bsx_chunk_prefill
+ * and bsx_chunk_step_host): in CTA `cta` of that launch (its linear grid
+ * index; CTA 0 is the last 128-row query tile of head 0 of batch 0 in the
+ * first key-block range) the copy producer stops before K/V ring item
+ * `item` (items in the order the tensor pipe consumes them: K_0, K_1, V_0,
+ * K_2, V_1, ...), with no copy and no arrival.  That CTA's waits for the item
+ * then run out after their bound (about 2 s), the CTA drains its own copies
+ * and MMAs, frees its tensor memory and exits without writing its O and
+ * LSE, and the device error word records the attention kernel and the
+ * wait that gave up (bsx_last_error).  Other CTAs are not affected.  The
+ * launch consumes the setting; cta < 0 disarms it.  BSX_ERR_INVALID_ARG for
+ * cta >= 0 with item < 0.
+ */
+int bsx_debug_drop_ring_item(int cta, int item);
+
+/*
  * Read and clear the device error word of the current device.  Waits for
  * the device to finish its work (this call is a diagnostic, not part of the
  * hot path).  *code receives the raw word (0 = no error; otherwise the

@@ -137,6 +137,12 @@ def test_chunk_step_host_rejects_bad_arguments(lib):
     assert _host_step(lib, ws=16) == -5                               # workspace too small
 
 
+def test_debug_drop_hook_arguments(lib):
+    assert lib.bsx_debug_drop_ring_item(0, -1) == -1     # armed needs an item
+    assert lib.bsx_debug_drop_ring_item(0, 3) == 0       # arm ...
+    assert lib.bsx_debug_drop_ring_item(-1, 0) == 0      # ... and disarm (no launch here)
+
+
 def test_binding_requires_cuda_tensors():
     import torch
     q = torch.zeros(1, 128, 2, 64)

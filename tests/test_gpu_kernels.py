@@ -433,3 +433,33 @@ def test_chunk_step_host_pipelined_buffer_sets():
         assert torch.equal(outs[i][2], keep)
     # different inputs gave different outputs (the sets were not mixed up)
     assert not torch.equal(outs[0][0], outs[1][0])
+
+
+def test_bounded_wait_timeout_is_reported_and_the_context_survives():
+    """Failure detection on the GPU without a fault: CTA 0's producer stops
+    before K_2 (a phase nothing completes), its waits run out after their
+    bound, the error word names the attention kernel and the wait that gave
+    up, and the next launch on the same context is correct."""
+    from block_sparse_long_xattn_gb300 import bsx_debug_drop_ring_item
+    P, Lq = 1024, 256
+    w = make_workload(seed=41, B=1, Hq=2, Hkv=1, d=128, Lk=P + Lq, q_start_pos=P,
+                      alpha=3.0, n_hot=1, dtype="bf16")
+    q, k, v = (to_dev(x, "bf16") for x in (w.q, w.k, w.v))
+    nkb = (P + Lq) // 128
+    mask_np = np.ones((1, 2, Lq // 128, nkb), np.uint8)   # CTA 0 has 10 key blocks
+    mask = torch.from_numpy(mask_np).cuda()
+    torch.cuda.synchronize()
+    assert bsx_last_error() == 0
+    bsx_debug_drop_ring_item(0, 3)
+    bsx_bsa_prefill(q, k, v, mask, P)
+    torch.cuda.synchronize()                  # the launch ends: no hang, no fault
+    code = bsx_last_error()
+    assert code & 0x80000000
+    assert code & 0xFF == 1                   # the tcgen05 attention kernel
+    assert (code >> 8) & 0xFF in (3, 5)       # the ring wait, or the S wait behind it
+    o, lse = bsx_bsa_prefill(q, k, v, mask, P)
+    torch.cuda.synchronize()
+    assert bsx_last_error() == 0
+    o_ref, lse_ref = O.bsa_prefill(w.q, w.k, w.v, mask_np, P, 0, nkb)
+    assert np.abs(o.float().cpu().numpy() - o_ref).max() <= O_TOL["bf16"]
+    assert np.abs(lse.cpu().numpy() - lse_ref).max() <= LSE_TOL
