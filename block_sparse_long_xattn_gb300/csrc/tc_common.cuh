@@ -67,12 +67,6 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
-// Bounded wait on an mbarrier phase.  Gives up after `limit_ns` of wall time,
-// or as soon as another thread of the CTA has raised `*abort`; returns false
-// then.  On its own expiry it raises `*abort` and records (kernel, site) in
-// the device error word.
-// Wait for work this CTA already issued (copies or MMAs) even after an
-// abort; bounded so that a broken phase cannot hang the CTA.
 // True in exactly one lane of a converged warp.  Call it once and keep the
 // result when the same lane must issue a sequence of tcgen05 operations.
 __device__ __forceinline__ bool elect_one_sync() {
@@ -83,6 +77,8 @@ __device__ __forceinline__ bool elect_one_sync() {
   return pred != 0;
 }
 
+// Wait for work this CTA already issued (copies or MMAs) even after an
+// abort; bounded so that a broken phase cannot hang the CTA.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity)) {
@@ -90,6 +86,10 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+// Bounded wait on an mbarrier phase.  Gives up after `limit_ns` of wall time,
+// or as soon as another thread of the CTA has raised `*abort`; returns false
+// then.  On its own expiry it raises `*abort` and records (kernel, site) in
+// the device error word.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
                                           unsigned* err, unsigned kernel, unsigned site,
                                           uint64_t limit_ns = 2000000000ull) {
