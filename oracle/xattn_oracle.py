@@ -29,7 +29,7 @@ Layouts (token-major, as the C ABI takes them):
   mask [B, Hq, Lq/128, Lk/128] bool
   o    [B, Lq, Hq, d]      lse  [B, Hq, Lq] (natural log)
 
-Readings of points the pages leave open (each is listed in the design doc):
+Readings of points the pages leave open, used by the oracle and the kernels alike:
   * the threshold-crossing block is kept (the worked example keeps it);
   * the forced sink/diagonal mass counts toward threshold * total;
   * ties in block mass break by ascending key-block index;
