@@ -17,6 +17,7 @@ independent replica; the path has no cross-GPU exchange).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                     [--step chunk|fused|offload|prefill]
+    python bench.py --sweep              # density sweep, one JSON line per point
     python bench.py --impl reference     # the fp64 CPU oracle, timed on a sample
 """
 from __future__ import annotations
@@ -437,6 +438,96 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+SWEEP_THRESHOLDS = (0.8, 0.9, 0.95, 0.99, 1.0)
+SWEEP_ALPHAS = (0.0, 2.0, 4.0)
+
+
+def run_sweep(args):
+    """Density sweep on the 32K / 4096-chunk shapes: for every planted
+    strength alpha (0: pure N(0,1), 16 hot blocks otherwise) and threshold,
+    the chunk step's mask density, the attention launch's TFLOP/s over the
+    selected blocks and the estimator's GB/s and TFLOP/s.  One JSON line per
+    point, device-resident inputs, L2 flushed between timed steps."""
+    import torch
+
+    import block_sparse_long_xattn_gb300 as bsx
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    hbm_peak, tc_peak, _, peak_src = _peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    base = dict(CONFIGS[DEFAULT_WORKLOAD])
+    S = base.pop("stride")
+    base.pop("threshold")
+    for alpha in SWEEP_ALPHAS:
+        c = dict(base, alpha=alpha, n_hot=16 if alpha > 0 else 0)
+        w = make_workload(seed=args.seed, **c)
+        B, Lq, Hq, d = w.q.shape
+        P, Lk = w.q_start_pos, w.k.shape[1]
+        cur, nkb = P // 128, Lk // 128
+        q, k, v = (torch.from_numpy(x).to(torch.bfloat16).to(dev) for x in (w.q, w.k, w.v))
+        mask = torch.empty((B, Hq, Lq // 128, nkb), dtype=torch.uint8, device=dev)
+        ws = torch.empty(bsx.bsx_estimate_workspace_bytes(bsx.shape_of(q, k), Lq, P, S),
+                         dtype=torch.uint8, device=dev)
+        oh, oc = torch.empty_like(q), torch.empty_like(q)
+        lh = torch.empty((B, Hq, Lq), dtype=torch.float32, device=dev)
+        lc = torch.empty_like(lh)
+        keep = torch.empty((B, P // 1024), dtype=torch.uint8, device=dev)
+        est_fl = estimate_flops(c, Lq, P, S)
+        est_bytes = (q.numel() + k.numel()) * q.element_size() + mask.numel()
+        causal_blocks = sum(cur + qb + 1 for qb in range(Lq // 128)) * B * Hq
+        for tau in SWEEP_THRESHOLDS:
+            def step(ev=None):
+                if ev:
+                    ev[0].record(stream)
+                bsx.bsx_xattn_estimate(q, k, P, S, tau, mask=mask, workspace=ws, stream=stream)
+                if ev:
+                    ev[1].record(stream)
+                bsx.bsx_bsa_prefill_split(q, k, v, mask, P, o_hist=oh, lse_hist=lh,
+                                          o_curr=oc, lse_curr=lc, stream=stream)
+                if ev:
+                    ev[2].record(stream)
+                bsx.bsx_merge_attn(oh, lh, oc, lc, stream=stream)
+                bsx.bsx_map_mask_to_cpu_blocks(mask, P, 1024, keep=keep, stream=stream)
+                if ev:
+                    ev[3].record(stream)
+
+            for _ in range(args.warmup):
+                step()
+            torch.cuda.synchronize()
+            m = mask.cpu().numpy()
+            density = float(m.astype(bool).sum()) / causal_blocks
+            fl = bsa_flops(m, P, 0, cur, d) + bsa_flops(m, P, cur, nkb, d)
+            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
+                   for _ in range(args.steps)]
+            with ClockSampler(0) as clk:
+                t0 = time.time()
+                for i in range(args.steps):
+                    flush.zero_()
+                    step(evs[i])
+                torch.cuda.synchronize()
+                clk.mark(t0, time.time())
+            t = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(3)] for e in evs])
+            t_est, t_bsa, t_rest = (float(x) for x in t.mean(axis=0))
+            ms = t_est + t_bsa + t_rest
+            bsa_tf = fl / (t_bsa / 1e3) / 1e12
+            print(json.dumps({
+                "sweep": DEFAULT_WORKLOAD, "alpha": alpha, "threshold": tau,
+                "density": density, "ms_per_step": ms,
+                "tokens_per_s_layer": B * Lq / (ms / 1e3),
+                "bsa_ms": t_bsa, "bsa_tflops": bsa_tf, "bsa_frac": bsa_tf / tc_peak,
+                "estimate_ms": t_est, "estimate_gbs": est_bytes / (t_est / 1e3) / 1e9,
+                "estimate_hbm_frac": est_bytes / (t_est / 1e3) / 1e9 / hbm_peak,
+                "estimate_tflops": est_fl / (t_est / 1e3) / 1e12,
+                "estimate_tc_frac": est_fl / (t_est / 1e3) / 1e12 / tc_peak,
+                "merge_map_ms": t_rest, "steps": args.steps, "warmup": args.warmup,
+                "peak_source": peak_src, "clocks": clk.summary()}), flush=True)
+        del q, k, v, ws, oh, oc
+    if bsx.bsx_last_error() != 0:
+        raise SystemExit("device error word set after the sweep")
+
+
 # ---------------------------------------------------------------------------
 def _oracle_threads():
     try:
@@ -517,15 +608,20 @@ def main():
     ap.add_argument("--cpu-heads", type=int, default=4,
                     help="q-heads in the oracle sample of the cpu_baseline leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="density sweep on the 32K / 4096-chunk shapes (thresholds 0.8-1.0 "
+                         "on alpha 0, 2, 4): one JSON line per point")
     args = ap.parse_args()
     if args.steps is None:
-        args.steps = 200 if args.impl == "gb300" else 20
+        args.steps = (50 if args.sweep else 200) if args.impl == "gb300" else 20
     if args.warmup < 3 and args.impl == "gb300":
         ap.error("at least 3 warm-up steps")
     if args.step == "prefill" and args.workload == DEFAULT_WORKLOAD:
         args.workload = "llama8b-32k-prefill"
     if args.impl == "reference":
         run_reference(args)
+    elif args.sweep:
+        run_sweep(args)
     else:
         run_gpu(args)
 
