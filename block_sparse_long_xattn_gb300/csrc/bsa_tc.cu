@@ -45,7 +45,7 @@ constexpr float kMaxBlockSum = 4294967296.0f;
 
 enum Site : unsigned {
   kSiteKvEmpty = 1, kSiteQFull, kSiteKvFull, kSitePFull, kSiteSFull, kSiteODoneFinal,
-  kSiteXchg
+  kSiteXchg, kSiteStage
 };
 
 template <int D>
@@ -81,7 +81,8 @@ struct BsaParts {
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-    const __grid_constant__ CUtensorMap tm_v, const uint8_t* __restrict__ mask, int q_len,
+    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o0,
+    const __grid_constant__ CUtensorMap tm_o1, const uint8_t* __restrict__ mask, int q_len,
     int Lk, int Hq, int Hkv, int cur, float scale_log2, const BsaParts parts, unsigned* err) {
   using L = Layout<D>;
   // One linear grid, decoded here so that the dispatch order is explicit:
@@ -122,11 +123,16 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
   auto o_done = [&](int g) { return bar0 + 8 * (kB2 + 4 + g); };  // P V(j) complete
   const uint32_t mma_final = bar0 + 8 * (kB2 + 6);
   const uint32_t xbar = bar0 + 8 * (kB2 + 7);                    // end-of-row merge
+  const uint32_t stage_full = bar0 + 8 * (kB2 + 8);              // O tile staged for the store
 
   const int nkb = Lk / kBlock;
   const int hk = h / (Hq / Hkv);
   const int diag = cur + qb;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint8_t* mrow = mask + (((long long)b * Hq + h) * nqb + qb) * nkb;
+  const int kb_last = min(kb_end, diag + 1);
+  const bool drop_here = (int)blockIdx.x == parts.drop_cta;
+  int kb_first = kb_last;  // producer: key block of the K tile copied before the count
 
   if (tid == 0) {
     mbar_init(q_full, 1);
@@ -140,11 +146,30 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
       mbar_init(o_done(g), 1);
     }
     mbar_init(xbar, 256);
+    mbar_init(stage_full, 256);
     mbar_init(mma_final, 1);
     *abort_flag = 0;
     *n_sm = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
+    // Q and the first selected K tile do not depend on the block count, so
+    // their copies start now and their latency overlaps the count's
+    tma_prefetch_map(&tm_q);
+    tma_prefetch_map(&tm_k);
+    tma_prefetch_map(&tm_v);
+    mbar_arrive_expect_tx(q_full, L::kTile);
+    for (int r = 0; r < L::kRegions; ++r)
+      tma_load_4d(sb + L::kQ + r * kRegion, &tm_q, q_full, r * 64, h, qb * 128, b);
+    if (!(drop_here && parts.drop_item == 0)) {
+      int kb = kb_begin;
+      while (kb < kb_last && !__ldg(mrow + kb)) ++kb;
+      if (kb < kb_last) {
+        mbar_arrive_expect_tx(slot_full(0), L::kTile);
+        for (int r = 0; r < L::kRegions; ++r)
+          tma_load_4d(sb + L::kRing + r * kRegion, &tm_k, slot_full(0), r * 64, hk, kb * 128, b);
+        kb_first = kb;
+      }
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
@@ -152,8 +177,6 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
   }
 
   // ---- count the selected key blocks of this row ----
-  const uint8_t* mrow = mask + (((long long)b * Hq + h) * nqb + qb) * nkb;
-  const int kb_last = min(kb_end, diag + 1);
   int cnt = 0;
   for (int kb = kb_begin + tid; kb < kb_last; kb += kThreads) cnt += mrow[kb] ? 1 : 0;
   cnt = __reduce_add_sync(0xffffffffu, cnt);
@@ -177,23 +200,20 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
     }
     for (int r = tid; r < 128; r += kThreads)
       lse[((long long)b * Hq + h) * q_len + qb * 128 + r] = -INFINITY;
+    if (tid == 0) drain_wait(q_full, 0);  // the early Q copy lands before the CTA exits
   } else if (warp == 0) {
     // ------------------------------ producer ------------------------------
     if (lane == 0) {
-      tma_prefetch_map(&tm_q);
-      tma_prefetch_map(&tm_k);
-      tma_prefetch_map(&tm_v);
-      mbar_arrive_expect_tx(q_full, L::kTile);
-      for (int r = 0; r < L::kRegions; ++r)
-        tma_load_4d(sb + L::kQ + r * kRegion, &tm_q, q_full, r * 64, h, qb * 128, b);
       // Ring items in the order the tensor pipe consumes them,
       //   K_0, K_1, V_0, K_2, V_1, ..., K_{n-1}, V_{n-2}, V_{n-1},
-      // item i in slot i % kSlots, so that the ring is a plain FIFO.
-      int issued = 0;
-      int kb = kb_begin - 1;
-      int kb_even = 0, kb_odd = 0;  // key blocks of the two most recent K items
+      // item i in slot i % kSlots, so that the ring is a plain FIFO.  K_0
+      // was copied before the count (unless the test hook drops item 0).
+      const bool k0_copied = kb_first < kb_last;
+      int issued = k0_copied ? 1 : 0;
+      int kb = k0_copied ? kb_first : kb_begin - 1;
+      int kb_even = k0_copied ? kb_first : 0, kb_odd = 0;  // key blocks of the two most recent K items
       bool ok = true;
-      for (int i = 0; ok && i < 2 * n; ++i) {
+      for (int i = issued; ok && i < 2 * n; ++i) {
         const bool is_k = i == 0 || ((i & 1) && (i + 1) / 2 < n);
         int blk;
         if (is_k) {
@@ -206,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
         } else {
           blk = i == 2 * n - 1 ? n - 1 : (i - 2) / 2;
         }
-        if ((int)blockIdx.x == parts.drop_cta && i == parts.drop_item) break;
+        if (drop_here && i == parts.drop_item) break;
         const int s = i % L::kSlots;
         if (i >= L::kSlots &&
             !mbar_wait(slot_empty(s), ((i / L::kSlots) - 1) & 1, abort_flag, err, kErrBsaTc,
@@ -439,8 +459,12 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
       const float l = l0 * w0 + l1 * w1;
       const float inv = 1.f / l;
       const float f0 = w0 * inv, f1 = w1 * inv;
-      // this group writes output columns [grp * D/2, grp * D/2 + D/2)
-      __nv_bfloat16* orow = o + (((long long)b * q_len + qb * 128 + row) * Hq + h) * D;
+      // This group writes output columns [grp * D/2, grp * D/2 + D/2) of its
+      // row into the Q buffer (every MMA is complete), in the 128-byte
+      // swizzled layout of the tensor map's box: feature f of row r sits in
+      // region f / 64, 16-byte chunk ((f % 64) / 8) ^ (r % 8) of the row's
+      // 128 bytes.  One TMA store then writes the tile.
+      uint8_t* stage = smem + L::kQ;
 #pragma unroll
       for (int cc = 0; cc < D / 64; ++cc) {
         const int col = grp * (D / 2) + cc * 32;
@@ -465,12 +489,27 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
           pk4.y = *reinterpret_cast<uint32_t*>(&a1);
           pk4.z = *reinterpret_cast<uint32_t*>(&a2);
           pk4.w = *reinterpret_cast<uint32_t*>(&a3);
-          reinterpret_cast<uint4*>(orow + col + e)[0] = pk4;
+          const int f = col + e;
+          *reinterpret_cast<uint4*>(stage + (f >> 6) * kRegion + row * 128 +
+                                    ((((f & 63) >> 3) ^ (row & 7)) << 4)) = pk4;
         }
       }
       if (grp == 0)
         lse[((long long)b * Hq + h) * q_len + qb * 128 + row] =
             (m + __log2f(l)) * 0.69314718055994531f;
+    }
+    // the staged tile is visible to the async proxy once every softmax
+    // thread has arrived; one thread stores it and waits until the copy has
+    // read shared memory (the CTA's shared memory must outlive the read)
+    fence_proxy_async_smem();
+    mbar_arrive(stage_full);
+    if (tid == 64 && ok &&
+        mbar_wait(stage_full, 0, abort_flag, err, kErrBsaTc, kSiteStage)) {
+      const CUtensorMap* tmo = part ? &tm_o1 : &tm_o0;
+      for (int r = 0; r < L::kRegions; ++r)
+        tma_store_4d(tmo, sb + L::kQ + r * kRegion, r * 64, h, qb * 128, b);
+      bulk_commit_group();
+      bulk_wait_group_read0();
     }
   }
 
@@ -496,6 +535,15 @@ cudaError_t launch_d(const Problem& p, const void* q, const void* k, const void*
                                  (uint64_t)p.q_len * p.Hq * D * 2};
     if (!encode_tmap_bf16(&mq, q, 4, dims, strides, box)) return cudaErrorInvalidValue;
   }
+  // O of each range, the same box as Q (stores of the staged tile)
+  CUtensorMap mo[2];
+  for (int i = 0; i < 2; ++i) {
+    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)p.Hq, (uint64_t)p.q_len, (uint64_t)p.B};
+    const uint64_t strides[3] = {(uint64_t)D * 2, (uint64_t)p.Hq * D * 2,
+                                 (uint64_t)p.q_len * p.Hq * D * 2};
+    if (!encode_tmap_bf16(&mo[i], ranges[i < nparts ? i : 0].o, 4, dims, strides, box))
+      return cudaErrorInvalidValue;
+  }
   {
     const uint64_t dims[4] = {(uint64_t)D, (uint64_t)p.Hkv, (uint64_t)p.Lk, (uint64_t)p.B};
     const uint64_t strides[3] = {(uint64_t)D * 2, (uint64_t)p.Hkv * D * 2,
@@ -519,7 +567,8 @@ cudaError_t launch_d(const Problem& p, const void* q, const void* k, const void*
                                   static_cast<__nv_bfloat16*>(ranges[1].o), ranges[1].lse}
                         : parts.p0;
   const dim3 grid(p.Hq * p.nqb * p.B * nparts);
-  bsa_tc_kernel<D><<<grid, kThreads, smem, st>>>(mq, mk, mv, mask, p.q_len, p.Lk, p.Hq, p.Hkv,
+  bsa_tc_kernel<D><<<grid, kThreads, smem, st>>>(mq, mk, mv, mo[0], mo[1], mask, p.q_len, p.Lk,
+                                                 p.Hq, p.Hkv,
                                                  p.q_start_pos / kBlock, scale_log2, parts, err);
   return cudaGetLastError();
 }
