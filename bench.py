@@ -16,7 +16,7 @@ outside the events.  value = tokens/s/layer over all ranks (each rank runs an
 independent replica; the path has no cross-GPU exchange).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--step chunk|fused|offload|prefill]
+                    [--step chunk|fused|offload|prefill|chunked]
     python bench.py --sweep              # density sweep, one JSON line per point
     python bench.py --impl reference     # the fp64 CPU oracle, timed on a sample
 """
@@ -438,6 +438,172 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+def run_chunked(args):
+    """Chunked prefill of a whole sequence (the 64K / 16 x 4096 workload): one
+    step runs the chunk step (estimate over history + chunk, attention on
+    history and current chunk in one launch, merge, CPU-block map) for every
+    chunk in order, each chunk's queries against all keys before its end.
+    value = sequence tokens / step time.  The end-to-end leg uploads each
+    chunk's Q, K and V rows from pinned host memory (appending to the device
+    KV, as a prefill does), runs the chunk step after its upload and reads the
+    chunk's O and LSE back, on three streams."""
+    import torch
+    import torch.distributed as dist
+
+    import block_sparse_long_xattn_gb300 as bsx
+
+    rank, world, local = _env_rank()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = dict(CONFIGS[args.workload])
+    S, tau, chunk = cfg.pop("stride"), cfg.pop("threshold"), cfg.pop("chunk")
+    w = make_workload(seed=args.seed + rank, q_full=True, **cfg)
+    B, L, Hq, d = w.q.shape
+    Hkv = cfg["Hkv"]
+    if B != 1 or L % chunk:
+        raise SystemExit("the chunked step takes batch 1 and whole chunks")
+    n_chunks, cpu_tokens = L // chunk, 1024
+    host = {n: torch.from_numpy(x).to(torch.bfloat16).pin_memory() for n, x in
+            (("q", w.q), ("k", w.k), ("v", w.v))}
+    dq, dk, dv = (host[n].to(dev) for n in ("q", "k", "v"))
+    o_full = torch.empty_like(dq)
+    oc = torch.empty((B, chunk, Hq, d), dtype=dq.dtype, device=dev)
+    lc = torch.empty((B, Hq, chunk), dtype=torch.float32, device=dev)
+    lse = [torch.empty((B, Hq, chunk), dtype=torch.float32, device=dev)
+           for _ in range(n_chunks)]
+    masks = [torch.empty((B, Hq, chunk // 128, (c + 1) * chunk // 128), dtype=torch.uint8,
+                         device=dev) for c in range(n_chunks)]
+    keeps = [torch.empty((B, c * chunk // cpu_tokens), dtype=torch.uint8, device=dev)
+             for c in range(n_chunks)]
+    ws = torch.empty(bsx.bsx_estimate_workspace_bytes(bsx.shape_of(dq, dk), chunk,
+                                                      L - chunk, S),
+                     dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def chunk_step(c, ev=None):
+        P = c * chunk
+        q, k, v = dq[:, P:P + chunk], dk[:, :P + chunk], dv[:, :P + chunk]
+        o = o_full[:, P:P + chunk]
+        bsx.bsx_xattn_estimate(q, k, P, S, tau, mask=masks[c], workspace=ws, stream=stream)
+        if ev:
+            ev[0].record(stream)
+        bsx.bsx_bsa_prefill_split(q, k, v, masks[c], P, o_hist=o, lse_hist=lse[c],
+                                  o_curr=oc, lse_curr=lc, stream=stream)
+        if ev:
+            ev[1].record(stream)
+        bsx.bsx_merge_attn(o, lse[c], oc, lc, stream=stream)
+        if P >= cpu_tokens:
+            bsx.bsx_map_mask_to_cpu_blocks(masks[c], P, cpu_tokens, keep=keeps[c],
+                                           stream=stream)
+
+    for _ in range(args.warmup):
+        for c in range(n_chunks):
+            chunk_step(c)
+    torch.cuda.synchronize()
+    flops = sum(bsa_flops(masks[c].cpu().numpy(), c * chunk, 0, c * chunk // 128, d) +
+                bsa_flops(masks[c].cpu().numpy(), c * chunk, c * chunk // 128,
+                          (c + 1) * chunk // 128, d) for c in range(n_chunks))
+    causal = sum(sum(c * chunk // 128 + qb + 1 for qb in range(chunk // 128))
+                 for c in range(n_chunks)) * B * Hq
+    density = sum(float(masks[c].cpu().numpy().astype(bool).sum())
+                  for c in range(n_chunks)) / causal
+
+    ev_step = [[torch.cuda.Event(enable_timing=True) for _ in range(2)]
+               for _ in range(args.steps)]
+    ev_bsa = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)]
+               for _ in range(n_chunks)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_wall0 = time.time()
+        for i in range(args.steps):
+            flush.zero_()
+            ev_step[i][0].record(stream)
+            for c in range(n_chunks):
+                chunk_step(c, ev_bsa[i][c])
+            ev_step[i][1].record(stream)
+        torch.cuda.synchronize()
+        clk.mark(t_wall0, time.time())
+    clocks = clk.summary()
+    ms_step = float(np.mean([e[0].elapsed_time(e[1]) for e in ev_step]))
+    bsa_ms = float(np.mean([sum(ev_bsa[i][c][0].elapsed_time(ev_bsa[i][c][1])
+                                for c in range(n_chunks)) for i in range(args.steps)]))
+
+    # end to end: chunk c's rows go up on one stream, its step runs on the
+    # compute stream after them, its O and LSE come back on a third
+    o_host = torch.empty(o_full.shape, dtype=o_full.dtype).pin_memory()
+    lse_host = torch.empty((n_chunks, B, Hq, chunk), dtype=torch.float32).pin_memory()
+    up, dn = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    n_e2e = max(3, args.steps // 2)
+    ups = [torch.cuda.Event() for _ in range(n_chunks)]
+    dones = [torch.cuda.Event() for _ in range(n_chunks)]
+    e2e_ms = []
+    for _ in range(n_e2e):
+        flush.zero_()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(up)
+        for c in range(n_chunks):
+            rows = slice(c * chunk, (c + 1) * chunk)
+            with torch.cuda.stream(up):
+                for n, t in (("q", dq), ("k", dk), ("v", dv)):
+                    t[:, rows].copy_(host[n][:, rows], non_blocking=True)
+                ups[c].record(up)
+            stream.wait_event(ups[c])
+            chunk_step(c)
+            dones[c].record(stream)
+            dn.wait_event(dones[c])
+            with torch.cuda.stream(dn):
+                o_host[:, rows].copy_(o_full[:, rows], non_blocking=True)
+                lse_host[c].copy_(lse[c], non_blocking=True)
+        e1.record(dn)
+        torch.cuda.synchronize()
+        e2e_ms.append(e0.elapsed_time(e1))
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = o_host.numel() * o_host.element_size() + lse_host.numel() * 4
+
+    (ms_step, ms_e2e), tokens, value = aggregate_ranks(
+        [ms_step, float(np.mean(e2e_ms))], B * L, world, dev)
+    hbm_peak, tc_peak, tc_sustained, peak_src = _peaks()
+    achieved = flops / (bsa_ms / 1e3) / 1e12
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic (seeded planted-direction N(0,1) inputs)",
+        "config": {"workload": args.workload, "step": "chunked", "B": B, "Hq": Hq, "Hkv": Hkv,
+                   "d": d, "seq_len": L, "chunk": chunk, "chunks": n_chunks, "stride": S,
+                   "threshold": tau, "cpu_block_tokens": cpu_tokens,
+                   "parallelism": f"replicas{world}",
+                   "l2": "flushed (256 MiB write) between timed steps", "seed": args.seed},
+        "roofline": {"kernel": DOMINANT, "bound": "tensor", "achieved": achieved,
+                     "peak": tc_peak, "unit": "TFLOP/s", "frac": achieved / tc_peak,
+                     "traffic": None, "peak_source": peak_src, "peak_sustained": tc_sustained,
+                     "frac_vs_sustained": achieved / tc_sustained if tc_sustained else None,
+                     "flops_per_launch": flops / n_chunks, "ms_per_launch": bsa_ms / n_chunks,
+                     "launches_per_step": n_chunks},
+        "kernels": {"bsa_ms_per_step": bsa_ms, "rest_ms_per_step": ms_step - bsa_ms},
+        "density": density,
+        "e2e": {"value": tokens / (ms_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e, "steps": n_e2e,
+                "overlap": "chunk c+1's upload runs while chunk c computes; each chunk's "
+                           "O/LSE read back while the next computes"},
+        "gpu_launches": args.steps * (4 * n_chunks - sum(1 for c in range(n_chunks)
+                                                         if c * chunk < cpu_tokens)
+                                      + n_chunks),
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
 SWEEP_THRESHOLDS = (0.8, 0.9, 0.95, 0.99, 1.0)
 SWEEP_ALPHAS = (0.0, 2.0, 4.0)
 
@@ -596,11 +762,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(CONFIGS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--step", default="chunk", choices=["chunk", "fused", "offload", "prefill"],
+    ap.add_argument("--step", default="chunk",
+                    choices=["chunk", "fused", "offload", "prefill", "chunked"],
                     help="chunk: estimate, BSA on history and current chunk, merge, map "
                          "(the default); fused: estimate + one BSA launch over all key "
                          "blocks; offload: the pages' CPU-block-dense history; prefill: "
-                         "fused on a whole-sequence workload")
+                         "fused on a whole-sequence workload; chunked: the chunk step on "
+                         "every chunk of a whole sequence in order (64K in 16 chunks)")
     ap.add_argument("--estimator", default="bf16", choices=["bf16", "e4m3"],
                     help="operand type of the estimator's scores (e4m3: Q and the chunk's K "
                          "quantized each step, the history's K kept in e4m3)")
@@ -618,10 +786,17 @@ def main():
         ap.error("at least 3 warm-up steps")
     if args.step == "prefill" and args.workload == DEFAULT_WORKLOAD:
         args.workload = "llama8b-32k-prefill"
+    if args.step == "chunked":
+        if args.workload == DEFAULT_WORKLOAD:
+            args.workload = "llama8b-64k-chunked"
+        if "chunk" not in CONFIGS[args.workload]:
+            ap.error("--step chunked takes a workload with a chunk size")
     if args.impl == "reference":
         run_reference(args)
     elif args.sweep:
         run_sweep(args)
+    elif args.step == "chunked":
+        run_chunked(args)
     else:
         run_gpu(args)
 
