@@ -1,5 +1,6 @@
 """Host logic of bench.py that needs no GPU: the clock record of the timed
-region (nvidia-smi samples filtered to the region's wall-clock window)."""
+region (nvidia-smi samples filtered to the region's wall-clock window) and
+the algorithmic flop counts behind the roofline figures."""
 import datetime
 import os
 import tempfile
@@ -44,3 +45,34 @@ def test_clock_summary_without_samples_in_the_region_says_so():
     s = c.summary()
     assert s["samples"] == 0 and s["sm_mhz"] is None
     assert s["reasons"] == ["no samples inside the timed region"]
+
+
+def test_bsa_flops_counts_the_visible_pairs_of_the_selected_tiles():
+    """The roofline's algorithmic flops: 4 * d per (query, key) pair that the
+    attention computes, counted here pair by pair on small masks (key j is
+    visible to query row i of the chunk iff j <= q_start_pos + i, and its
+    block is selected and inside the key range)."""
+    import numpy as np
+    rng = np.random.default_rng(3)
+    for B, Hq, P, Lq, d in ((1, 2, 256, 384, 128), (2, 1, 0, 256, 64)):
+        nqb, nkb = Lq // 128, (P + Lq) // 128
+        mask = (rng.random((B, Hq, nqb, nkb)) < 0.6).astype(np.uint8)
+        for kb0, kb1 in ((0, nkb), (0, P // 128), (P // 128, nkb)):
+            pairs = 0
+            for b in range(B):
+                for h in range(Hq):
+                    for i in range(Lq):
+                        for j in range(kb0 * 128, kb1 * 128):
+                            if j <= P + i and mask[b, h, i // 128, j // 128]:
+                                pairs += 1
+            assert bench.bsa_flops(mask, P, kb0, kb1, d) == 4 * d * pairs
+
+
+def test_estimate_flops_counts_the_causal_reshaped_pairs():
+    """2 * d * S flops per reshaped (row I, key J) pair with J <= I and per
+    q-head, rows I covering the chunk, counted pair by pair."""
+    for q_len, P, S in ((256, 512, 8), (512, 0, 16), (128, 128, 4)):
+        cfg = dict(B=2, Hq=3, d=64)
+        pairs = sum(1 for I in range(P // S, (P + q_len) // S) for J in range((P + q_len) // S)
+                    if J <= I)
+        assert bench.estimate_flops(cfg, q_len, P, S) == 2.0 * 64 * S * pairs * 3 * 2
