@@ -1,5 +1,6 @@
 // C ABI of the library: argument validation, kernel choice, launches.
 // Declarations and the meaning of every argument: include/bsxattn.h.
+#include <limits.h>
 #include <math.h>
 #include <stdio.h>
 
@@ -33,8 +34,11 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // Common shape checks; fills the internal problem description.
 // e4m3 operands are accepted only where `allow_e4m3` (the estimate), with d = 128.
+// Calls that work on the block mask (`masked`) also need its element count
+// B * Hq * (q_len/128) * (Lk/128) to fit a 32-bit int: their grids and tile
+// indices are 32-bit.
 int make_problem(const bsx_shape& s, int q_len, int q_start_pos, bsx::Problem* p,
-                 bool allow_e4m3 = false) {
+                 bool allow_e4m3 = false, bool masked = true) {
   if (s.B < 1 || s.Hq < 1 || s.Hkv < 1 || s.Hq % s.Hkv != 0) return BSX_ERR_INVALID_ARG;
   const bool e4m3 = s.dtype == BSX_F8E4M3 && allow_e4m3;
   if (s.dtype != BSX_F32 && s.dtype != BSX_BF16 && !e4m3) return BSX_ERR_UNSUPPORTED;
@@ -54,6 +58,7 @@ int make_problem(const bsx_shape& s, int q_len, int q_start_pos, bsx::Problem* p
   p->Lk = (int)Lk;
   p->nqb = q_len / 128;
   p->nkb = (int)(Lk / 128);
+  if (masked && (long long)s.B * s.Hq * p->nqb * p->nkb > INT_MAX) return BSX_ERR_UNSUPPORTED;
   return BSX_OK;
 }
 
@@ -182,7 +187,7 @@ int bsx_quantize_e4m3(const void* src, uint8_t* dst, long long n, void* stream) 
 int bsx_merge_attn(bsx_shape s, int q_len, void* o1, float* lse1, const void* o2,
                    const float* lse2, void* stream) {
   bsx::Problem p;
-  int rc = make_problem(s, q_len, 0, &p);
+  int rc = make_problem(s, q_len, 0, &p, false, false);
   if (rc != BSX_OK) return rc;
   if (!o1 || !lse1 || !o2 || !lse2) return BSX_ERR_INVALID_ARG;
   if (!aligned16(o1) || !aligned16(o2)) return BSX_ERR_INVALID_ARG;

@@ -37,7 +37,9 @@
  *    multiples of 128 (the BSA block size, fixed at 128 on the pages).
  *  - Arguments are validated on the host before any launch; a bad argument
  *    returns BSX_ERR_INVALID_ARG and an unsupported combination (dtype, d,
- *    stride) returns BSX_ERR_UNSUPPORTED, with nothing enqueued.  There is no
+ *    stride; Lk above 2^24; a block mask of more than 2^31 - 1 elements,
+ *    B * Hq * (q_len/128) * (Lk/128), for the calls that use one) returns
+ *    BSX_ERR_UNSUPPORTED, with nothing enqueued.  There is no
  *    fallback path.  A CUDA launch error returns BSX_ERR_CUDA.  Errors the
  *    kernels detect asynchronously (a bounded wait that expired) are
  *    recorded in a device error word read by bsx_last_error().

@@ -94,6 +94,22 @@ def test_bsa_merge_map_reject_bad_arguments(lib):
     assert lib.bsx_map_mask_to_cpu_blocks(s, p, 128, 4096, 1024, 4, p, None) == -1
 
 
+def test_mask_size_limit(lib):
+    """Calls that use the block mask index it with 32-bit grids: a mask of more
+    than 2^31 - 1 elements is unsupported, rejected before any launch; the
+    merge, which has no mask, takes the same rows."""
+    p = ctypes.c_void_p(16)
+    big = L.BsxShape(1024, 32, 8, 128, L.BSX_BF16)   # 1024*32*32*2048 = 2^31 mask elements
+    assert lib.bsx_bsa_prefill(big, p, p, p, p, 4096, 258048, 0, 1, p, p, None) == -2
+    assert lib.bsx_bsa_prefill_split(big, p, p, p, p, 4096, 258048, p, p, p, p, None) == -2
+    assert lib.bsx_map_mask_to_cpu_blocks(big, p, 4096, 258048, 1024, 0, p, None) == -2
+    assert lib.bsx_estimate_workspace_bytes(big, 4096, 258048, 8) == 0
+    ok = L.BsxShape(1023, 32, 8, 128, L.BSX_BF16)    # one batch fewer fits
+    assert lib.bsx_bsa_prefill(ok, p, p, p, p, 4096, 258048, 0, 1, p, None, None) == -1
+    # the merge sees no mask: only its own arguments are checked
+    assert lib.bsx_merge_attn(big, 4096, p, None, p, p, None) == -1
+
+
 def _host_step(lib, shape=None, q_len=256, P=1024, stride=8, tau=0.9, cpu=1024, flags=0,
                host=64, ws=1 << 30, drop=(), **set_fields):
     """bsx_chunk_step_host with fake, aligned, never-dereferenced pointers:
