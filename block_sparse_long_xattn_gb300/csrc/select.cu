@@ -257,13 +257,8 @@ __device__ __forceinline__ void bitonic_regs(unsigned long long (&key)[KPL], int
   }
 }
 
-// Rows whose partials fit in registers (KPL * RB values per lane) read them
-// once; longer rows (or stride 4) make three passes over memory instead.
-template <int KPL, int RB>
-constexpr bool kRowInRegs = KPL * RB <= 128;
-
 template <int RB, int KPL>
-__global__ void __launch_bounds__(32 * kWarpsPerCta, kRowInRegs<KPL, RB> ? 2 : ((KPL <= 8 && RB <= 16) ? 4 : 2)) select_warp_kernel(
+__global__ void __launch_bounds__(32 * kWarpsPerCta, (KPL <= 8 && RB <= 16) ? 4 : 2) select_warp_kernel(
     const float* __restrict__ lse_part, int Hq, int nqb, int nkb, int R, int cur,
     float threshold, uint8_t* __restrict__ mask, float* __restrict__ block_sums) {
   constexpr int N = 32 * KPL;  // padded row length (a power of two)
@@ -279,115 +274,63 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta, kRowInRegs<KPL, RB> ? 2 : (
   const int ncausal = diag + 1;
   const float* base = lse_part + ((long long)(b * Hq + h) * nkb) * R + qb * RB;
 
+  // ---- row maxima, then row sums -> row LSE ----
+  float acc[RB];
+#pragma unroll
+  for (int i = 0; i < RB; ++i) acc[i] = -INFINITY;
+#pragma unroll 4
+  for (int kb = lane; kb < ncausal; kb += 32) {
+    const float4* q = reinterpret_cast<const float4*>(base + (long long)kb * R);
+#pragma unroll
+    for (int c = 0; c < RB / 4; ++c) {
+      const float4 v = __ldg(q + c);
+      acc[4 * c + 0] = fmaxf(acc[4 * c + 0], v.x);
+      acc[4 * c + 1] = fmaxf(acc[4 * c + 1], v.y);
+      acc[4 * c + 2] = fmaxf(acc[4 * c + 2], v.z);
+      acc[4 * c + 3] = fmaxf(acc[4 * c + 3], v.w);
+    }
+  }
+  float rmax[RB];
+#pragma unroll
+  for (int i = 0; i < RB; ++i) {
+    rmax[i] = warp_max(acc[i]);
+    acc[i] = 0.f;
+  }
+#pragma unroll 4
+  for (int kb = lane; kb < ncausal; kb += 32) {
+    const float4* q = reinterpret_cast<const float4*>(base + (long long)kb * R);
+#pragma unroll
+    for (int c = 0; c < RB / 4; ++c) {
+      const float4 v = __ldg(q + c);
+      acc[4 * c + 0] += __expf(v.x - rmax[4 * c + 0]);
+      acc[4 * c + 1] += __expf(v.y - rmax[4 * c + 1]);
+      acc[4 * c + 2] += __expf(v.z - rmax[4 * c + 2]);
+      acc[4 * c + 3] += __expf(v.w - rmax[4 * c + 3]);
+    }
+  }
   float rlse[RB];
-  float a[KPL];  // block sums A[kb], kb = t * 32 + lane
-  float part = 0.f;
-  if constexpr (kRowInRegs<KPL, RB>) {
-    // ---- one read of the row's partials: v[t][i] for kb = t * 32 + lane ----
-    float v[KPL][RB];
 #pragma unroll
-    for (int t = 0; t < KPL; ++t) {
-      const int kb = t * 32 + lane;
-      if (kb < ncausal) {
-        const float4* q = reinterpret_cast<const float4*>(base + (long long)kb * R);
-#pragma unroll
-        for (int c = 0; c < RB / 4; ++c) {
-          const float4 x = __ldg(q + c);
-          v[t][4 * c + 0] = x.x;
-          v[t][4 * c + 1] = x.y;
-          v[t][4 * c + 2] = x.z;
-          v[t][4 * c + 3] = x.w;
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < RB; ++i) v[t][i] = -INFINITY;
-      }
-    }
-    // ---- row maxima, then row sums -> row LSE (the multi-pass order) ----
-#pragma unroll
-    for (int i = 0; i < RB; ++i) {
-      float m = v[0][i];
-#pragma unroll
-      for (int t = 1; t < KPL; ++t) m = fmaxf(m, v[t][i]);
-      const float rmax = warp_max(m);
-      float sum = 0.f;
-#pragma unroll
-      for (int t = 0; t < KPL; ++t) sum += __expf(v[t][i] - rmax);
-      rlse[i] = rmax + logf(warp_sum(sum));
-    }
-    // ---- block sums ----
-#pragma unroll
-    for (int t = 0; t < KPL; ++t) {
-      const int kb = t * 32 + lane;
-      float sa = 0.f;
-      if (kb < ncausal) {
-#pragma unroll
-        for (int c = 0; c < RB / 4; ++c)
-          sa += __expf(v[t][4 * c + 0] - rlse[4 * c + 0]) +
-                __expf(v[t][4 * c + 1] - rlse[4 * c + 1]) +
-                __expf(v[t][4 * c + 2] - rlse[4 * c + 2]) +
-                __expf(v[t][4 * c + 3] - rlse[4 * c + 3]);
-      }
-      a[t] = sa;
-      part += sa;
-      if (block_sums && kb < nkb) block_sums[(((long long)b * Hq + h) * nqb + qb) * nkb + kb] = sa;
-    }
-  } else {
-    // ---- row maxima, then row sums -> row LSE ----
-    float acc[RB];
-#pragma unroll
-    for (int i = 0; i < RB; ++i) acc[i] = -INFINITY;
-#pragma unroll 4
-    for (int kb = lane; kb < ncausal; kb += 32) {
-      const float4* q = reinterpret_cast<const float4*>(base + (long long)kb * R);
-#pragma unroll
-      for (int c = 0; c < RB / 4; ++c) {
-        const float4 v = __ldg(q + c);
-        acc[4 * c + 0] = fmaxf(acc[4 * c + 0], v.x);
-        acc[4 * c + 1] = fmaxf(acc[4 * c + 1], v.y);
-        acc[4 * c + 2] = fmaxf(acc[4 * c + 2], v.z);
-        acc[4 * c + 3] = fmaxf(acc[4 * c + 3], v.w);
-      }
-    }
-    float rmax[RB];
-#pragma unroll
-    for (int i = 0; i < RB; ++i) {
-      rmax[i] = warp_max(acc[i]);
-      acc[i] = 0.f;
-    }
-#pragma unroll 4
-    for (int kb = lane; kb < ncausal; kb += 32) {
-      const float4* q = reinterpret_cast<const float4*>(base + (long long)kb * R);
-#pragma unroll
-      for (int c = 0; c < RB / 4; ++c) {
-        const float4 v = __ldg(q + c);
-        acc[4 * c + 0] += __expf(v.x - rmax[4 * c + 0]);
-        acc[4 * c + 1] += __expf(v.y - rmax[4 * c + 1]);
-        acc[4 * c + 2] += __expf(v.z - rmax[4 * c + 2]);
-        acc[4 * c + 3] += __expf(v.w - rmax[4 * c + 3]);
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < RB; ++i) rlse[i] = rmax[i] + logf(warp_sum(acc[i]));
+  for (int i = 0; i < RB; ++i) rlse[i] = rmax[i] + logf(warp_sum(acc[i]));
 
-    // ---- block sums ----
+  // ---- block sums A[kb], kb = t * 32 + lane ----
+  float a[KPL];
+  float part = 0.f;
 #pragma unroll
-    for (int t = 0; t < KPL; ++t) {
-      const int kb = t * 32 + lane;
-      float v = 0.f;
-      if (kb < ncausal) {
-        const float4* q = reinterpret_cast<const float4*>(base + (long long)kb * R);
+  for (int t = 0; t < KPL; ++t) {
+    const int kb = t * 32 + lane;
+    float v = 0.f;
+    if (kb < ncausal) {
+      const float4* q = reinterpret_cast<const float4*>(base + (long long)kb * R);
 #pragma unroll
-        for (int c = 0; c < RB / 4; ++c) {
-          const float4 w = __ldg(q + c);
-          v += __expf(w.x - rlse[4 * c + 0]) + __expf(w.y - rlse[4 * c + 1]) +
-               __expf(w.z - rlse[4 * c + 2]) + __expf(w.w - rlse[4 * c + 3]);
-        }
+      for (int c = 0; c < RB / 4; ++c) {
+        const float4 w = __ldg(q + c);
+        v += __expf(w.x - rlse[4 * c + 0]) + __expf(w.y - rlse[4 * c + 1]) +
+             __expf(w.z - rlse[4 * c + 2]) + __expf(w.w - rlse[4 * c + 3]);
       }
-      a[t] = v;
-      part += v;
-      if (block_sums && kb < nkb) block_sums[(((long long)b * Hq + h) * nqb + qb) * nkb + kb] = v;
     }
+    a[t] = v;
+    part += v;
+    if (block_sums && kb < nkb) block_sums[(((long long)b * Hq + h) * nqb + qb) * nkb + kb] = v;
   }
   const float total = warp_sum(part);
 
@@ -450,13 +393,18 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta, kRowInRegs<KPL, RB> ? 2 : (
   // ---- exclusive scan of the sorted masses; keep while below the target ----
   const int nforced = diag == 0 ? 1 : 2;
   const int ncand = ncausal - nforced;
-  // A of the diagonal block, from its owner (lane diag % 32, register
-  // diag / 32, picked by a select chain: no register is indexed at run time)
-  float a_own = 0.f;
+  // A of the diagonal block, recomputed by every lane the way its owner did
+  // (selecting it from the owner's registers would need a runtime index)
+  float a_diag = 0.f;
+  {
+    const float4* q = reinterpret_cast<const float4*>(base + (long long)diag * R);
 #pragma unroll
-  for (int t = 0; t < KPL; ++t)
-    if (t == (diag >> 5)) a_own = a[t];
-  const float a_diag = __shfl_sync(0xffffffffu, a_own, diag & 31);
+    for (int c = 0; c < RB / 4; ++c) {
+      const float4 w = __ldg(q + c);
+      a_diag += __expf(w.x - rlse[4 * c + 0]) + __expf(w.y - rlse[4 * c + 1]) +
+                __expf(w.z - rlse[4 * c + 2]) + __expf(w.w - rlse[4 * c + 3]);
+    }
+  }
   const float forced_mass = __shfl_sync(0xffffffffu, a[0], 0) + (diag != 0 ? a_diag : 0.f);
   const float target = threshold * total;
   for (int kb = lane; kb < N; kb += 32) sel[kb] = 0;
