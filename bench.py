@@ -285,8 +285,12 @@ def run_gpu(args):
     def step(q, k, v, ev=None):
         if ev:
             ev[0].record(stream)
-        for i, (_, fn) in enumerate(phases):
+        for i, (name, fn) in enumerate(phases):
+            if args.nvtx:
+                torch.cuda.nvtx.range_push(name)
             fn(q, k, v)
+            if args.nvtx:
+                torch.cuda.nvtx.range_pop()
             if ev:
                 ev[i + 1].record(stream)
 
@@ -776,6 +780,9 @@ def main():
     ap.add_argument("--cpu-heads", type=int, default=4,
                     help="q-heads in the oracle sample of the cpu_baseline leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--nvtx", action="store_true",
+                    help="wrap each phase of the step in an NVTX range (for a profiler's "
+                         "timeline; adds host work to the timed region)")
     ap.add_argument("--sweep", action="store_true",
                     help="density sweep on the 32K / 4096-chunk shapes (thresholds 0.8-1.0 "
                          "on alpha 0, 2, 4): one JSON line per point")

@@ -32,7 +32,9 @@ def _cfg(name):
 
 
 def gpu_chunk_step(q, k, v, P, S, tau, mask_for_bsa=None, cpu_tokens=1024):
-    """The benchmark's step; returns (mask, block sums, o, lse, keep)."""
+    """The benchmark's step; returns (mask, block sums, o, lse, keep).  Every
+    output element is scanned: block sums, O and LSE are finite everywhere
+    (each query row sees at least its diagonal block), and the mask is 0/1."""
     B, Lq, Hq, _ = q.shape
     nkb, cur = k.shape[1] // 128, P // 128
     A = torch.empty((B, Hq, Lq // 128, nkb), dtype=torch.float32, device=q.device)
@@ -42,6 +44,8 @@ def gpu_chunk_step(q, k, v, P, S, tau, mask_for_bsa=None, cpu_tokens=1024):
     bsx_merge_attn(oh, lh, oc, lc)
     keep = bsx_map_mask_to_cpu_blocks(m, P, cpu_tokens) if P >= cpu_tokens else None
     torch.cuda.synchronize()
+    assert bool(torch.isfinite(A).all()) and bool((mask <= 1).all())
+    assert bool(torch.isfinite(oh.float()).all()) and bool(torch.isfinite(lh).all())
     return mask, A, oh, lh, keep
 
 
