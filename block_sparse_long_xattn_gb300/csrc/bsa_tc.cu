@@ -6,7 +6,8 @@
 // and LSE from the history part and the current-chunk part and merges them.
 //
 // One CTA per (128-row q-tile, q-head, batch); 10 warps with fixed roles:
-//   warp 0      TMA producer: Q once, then the K and V tiles of every selected
+//   warp 0      TMA producer: Q and the first selected K tile (both copied
+//               before the block count), then the K and V tiles of every selected
 //               key block, found by scanning the mask row, into a ring of
 //               tile-sized slots in the order the MMAs consume them (K_0, K_1,
 //               V_0, K_2, V_1, ...).  A K slot is freed as soon as its S MMA
@@ -21,8 +22,9 @@
 //               columns, row sums; the running max m is raised (and O_g
 //               rescaled) only on a group's first block and when a block's
 //               row sum would exceed 2^32.  At the end the two partial
-//               results (O_g, m_g, l_g) are merged per row and O and LSE go
-//               to global memory.
+//               results (O_g, m_g, l_g) are merged per row; LSE goes to
+//               global memory directly, O through the finished Q buffer and
+//               one TMA store per 64-feature region.
 // Each group's chain S(j) -> softmax -> P V(j) -> S(j + 2) interleaves with
 // the other group's on the tensor pipe, and no per-block exchange between
 // warps is needed.  TMEM: S/P buffers in columns 0-255, O_0 and O_1 after.
