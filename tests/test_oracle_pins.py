@@ -97,7 +97,9 @@ def _block_sums_via_torch(q, k, P, S):
 
 @pytest.mark.parametrize("S,P", [(8, 0), (8, 256), (4, 128), (16, 384)])
 def test_block_sums_match_torch_attention(S, P):
-    w = make_workload(seed=11 + S, B=1, Hq=2, Hkv=1, d=16, Lk=P + 256, q_start_pos=P,
+    # two kv-heads of two q-heads each: q-head h reads kv-head h // 2, which
+    # differs from h % 2 for h = 1, 2 (a wrong GQA mapping fails here)
+    w = make_workload(seed=11 + S, B=1, Hq=4, Hkv=2, d=16, Lk=P + 256, q_start_pos=P,
                       alpha=2.0, n_hot=1, dtype="f32")
     A = O.estimate_block_sums(w.q.astype(np.float64), w.k.astype(np.float64), P, S)
     ref = _block_sums_via_torch(w.q.astype(np.float64), w.k.astype(np.float64), P, S)
