@@ -5,8 +5,9 @@ tests/test_oracle_pins.py then fails.  The mistakes are the kind a restatement
 of the pages could make: a stride reshape in the wrong direction, a dropped
 factor of the softmax scale, a strict causal rule, a wrong GQA head mapping,
 a selection that drops the crossing block or ignores the forced mass, an
-attention scale of 1/d, a merge that weights by LSE instead of exp(LSE), a
-CPU-block group shifted by one.
+attention scale of 1/d (block-sparse or offload), a merge that weights by
+LSE instead of exp(LSE), a CPU-block group shifted by one, an offload mask
+without the diagonal block.
 """
 import math
 
@@ -17,6 +18,7 @@ from oracle import xattn_oracle as O
 from tests import test_oracle_pins as pins
 
 BLOCK = 128
+_offload_block_mask = O.offload_block_mask   # the unmutated function
 
 
 def _q_forward(q_head, stride):
@@ -144,6 +146,33 @@ def _map_shifted(mask, q_start_pos, cpu_block_tokens=1024, force_first_last=Fals
     return keep
 
 
+def _dense_attention_scale_1_over_d(qh, kh, vh, allowed):
+    d = qh.shape[-1]
+    s = np.where(allowed, (qh @ kh.T) / d, -np.inf)
+    m = s.max(axis=1, keepdims=True)
+    has = np.isfinite(m[:, 0])
+    m = np.where(has[:, None], m, 0.0)
+    e = np.where(allowed, np.exp(s - m), 0.0)
+    l = e.sum(axis=1)
+    o = np.zeros((qh.shape[0], vh.shape[1]))
+    o[has] = (e[has] @ vh) / l[has, None]
+    return o, np.where(has, m[:, 0] + np.log(np.where(has, l, 1.0)), -np.inf)
+
+
+def _offload_mask_strict_diagonal(keep, Hq, q_len, q_start_pos, cpu_block_tokens=1024):
+    mask = _offload_block_mask(keep, Hq, q_len, q_start_pos, cpu_block_tokens)
+    cur = q_start_pos // BLOCK
+    for qb in range(q_len // BLOCK):
+        mask[:, :, qb, cur + qb] = False           # the diagonal block dropped
+    return mask
+
+
+def _offload_pins():
+    pins.test_offload_attention_all_kept_is_dense_causal()
+    pins.test_offload_attention_equals_torch_on_kept_keys_and_bsa_with_its_mask()
+    pins.test_offload_mask_small_example()
+
+
 def _block_sum_pins():
     for S, P in ((8, 0), (8, 256), (4, 128), (16, 384)):
         pins.test_block_sums_match_torch_attention(S, P)
@@ -188,6 +217,10 @@ MUTATIONS = {
     "merge weighted by LSE": ("merge_attn", _merge_by_lse,
                               lambda: (pins.test_merge_of_split_keys_equals_single_softmax(),
                                        pins.test_merge_identities())),
+    "offload attention scale 1/d": ("_dense_attention", _dense_attention_scale_1_over_d,
+                                    _offload_pins),
+    "offload mask without the diagonal block": ("offload_block_mask",
+                                                _offload_mask_strict_diagonal, _offload_pins),
     "CPU-block group shifted by one": (
         "map_mask_to_cpu_blocks", _map_shifted,
         lambda: (pins.test_map_golden_example(), pins.test_map_by_scatter(1024))),
