@@ -24,7 +24,8 @@ STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported", -3: "CUDA error",
 
 EXPORTS = ("bsx_version", "bsx_status_string", "bsx_estimate_workspace_bytes",
            "bsx_xattn_estimate", "bsx_bsa_prefill", "bsx_merge_attn",
-           "bsx_map_mask_to_cpu_blocks", "bsx_last_error", "bsx_xattn_estimate_noalloc",
+           "bsx_map_mask_to_cpu_blocks", "bsx_last_error", "bsx_last_error_code",
+           "bsx_xattn_estimate_noalloc",
            "bsx_cpu_block_mask", "bsx_chunk_prefill", "bsx_bsa_prefill_split",
            "bsx_quantize_e4m3", "bsx_chunk_step_host", "bsx_debug_drop_ring_item")
 BSX_STEP_OFFLOAD, BSX_STEP_E4M3_ESTIMATE, BSX_STEP_FUSED = 2, 4, 8
@@ -94,7 +95,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.bsx_cpu_block_mask.restype = i32
         lib.bsx_cpu_block_mask.argtypes = [BsxShape, vp, i32, i32, i32, vp, vp]
         lib.bsx_last_error.restype = i32
-        lib.bsx_last_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+        lib.bsx_last_error.argtypes = [vp]
+        lib.bsx_last_error_code.restype = ctypes.c_uint
+        lib.bsx_last_error_code.argtypes = []
         lib.bsx_debug_drop_ring_item.restype = i32
         lib.bsx_debug_drop_ring_item.argtypes = [i32, i32]
         lib.bsx_chunk_step_host.restype = i32
@@ -316,13 +319,14 @@ def bsx_debug_drop_ring_item(cta: int, item: int) -> None:
     _check("bsx_debug_drop_ring_item", load().bsx_debug_drop_ring_item(cta, item))
 
 
-def bsx_last_error() -> int:
-    """Read and clear the device error word; returns the raw word (0 = none)."""
-    code = ctypes.c_uint(0)
-    status = load().bsx_last_error(ctypes.byref(code))
+def bsx_last_error(stream=None) -> int:
+    """Wait for `stream` (default: torch's current stream), read and clear the
+    device error word; returns the raw word (0 = none)."""
+    lib = load()
+    status = lib.bsx_last_error(_stream(stream))
     if status not in (0, -4):
         raise BsxError("bsx_last_error", status)
-    return int(code.value)
+    return int(lib.bsx_last_error_code())
 
 
 def make_chunk_buffers(q_host, k_host, q_start_pos: int, stride: int,

@@ -74,6 +74,9 @@ constexpr int kMaxKeyBlocks = 8192;  // selection sorts up to this many blocks p
 // consumed by the next tcgen05 attention launch of that thread.
 thread_local bsx::BsaDrop t_drop;
 
+// The raw error word the calling thread's last bsx_last_error read.
+thread_local unsigned t_last_word = 0;
+
 bsx::BsaDrop take_drop() {
   const bsx::BsaDrop d = t_drop;
   t_drop = bsx::BsaDrop();
@@ -244,23 +247,26 @@ int bsx_debug_drop_ring_item(int cta, int item) {
   return BSX_OK;
 }
 
-int bsx_last_error(unsigned int* code) {
-  if (!code) return BSX_ERR_INVALID_ARG;
-  *code = 0;
+int bsx_last_error(void* stream) {
+  t_last_word = 0;
   unsigned* w = err_word();
   if (!w) return BSX_ERR_CUDA;
-  cudaError_t e = cudaDeviceSynchronize();
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_status(e);
   unsigned h = 0;
-  e = cudaMemcpy(&h, w, sizeof(h), cudaMemcpyDeviceToHost);
+  e = cudaMemcpyAsync(&h, w, sizeof(h), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_status(e);
   if (h != 0) {
-    const unsigned zero = 0;
-    e = cudaMemcpy(w, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    e = cudaMemsetAsync(w, 0, sizeof(unsigned), st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_status(e);
   }
-  *code = h;
+  t_last_word = h;
   return h ? BSX_ERR_TIMEOUT : BSX_OK;
 }
+
+unsigned int bsx_last_error_code(void) { return t_last_word; }
 
 }  // extern "C"

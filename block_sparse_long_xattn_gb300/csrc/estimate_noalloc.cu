@@ -6,18 +6,24 @@
 // cudaMalloc, or a real-time loop that may not call an allocator (cudaMalloc
 // and cudaFree can block on the device).  Such a caller may also have no spare
 // buffer to lend as the estimator's scratch.  This entry point takes the same
-// inputs and outputs as bsx_xattn_estimate but uses a scratch array that the
-// library reserves once, at load time, in each device's global memory.
+// inputs and outputs as bsx_xattn_estimate but uses a scratch array of fixed
+// size that lives in the library's own device code.
 //
-// The array is a file-scope __device__ variable of fixed size; every GPU that
-// loads the library keeps it until the process exits.  Host code may not use
-// the variable's name as a device address, so the first call on each device
-// looks its address up with cudaGetSymbolAddress (with that device current)
-// and caches it; that first call should come before any stream capture.
+// The array is a file-scope __device__ variable; every GPU that uses the
+// library keeps it until the process exits.  Host code may not use the
+// variable's name as a device address, so the first call on each device looks
+// its address up with cudaGetSymbolAddress (with that device current) and
+// caches it.  CUDA loads device code lazily: the array is committed on the
+// device by that first lookup, which can therefore fail for lack of device
+// memory; it should come before the caller's engine fills its memory pool and
+// before any stream capture.  The cache belongs to the primary context of
+// each device and does not survive cudaDeviceReset.
 // Calls share the one array: two calls whose kernels overlap on the GPU (on
 // different streams, or from different host threads) race on it.  Nothing in
 // the array needs to start at zero: the estimate writes every scratch cell it
 // later reads.
+#include <stdio.h>
+
 #include <atomic>
 
 #include "../../include/bsxattn.h"
@@ -42,8 +48,11 @@ int scratch_address(void** out) {
     return BSX_ERR_CUDA;
   void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
   if (!p) {
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p)
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) {
+      fprintf(stderr, "bsxattn: scratch lookup failed: %s\n", cudaGetErrorString(e));
       return BSX_ERR_CUDA;
+    }
     g_scratch_addr[dev].store(p, std::memory_order_release);
   }
   *out = p;

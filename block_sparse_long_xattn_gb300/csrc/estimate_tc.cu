@@ -19,15 +19,14 @@
 //   lse_part[b][h][kb][i] = ln sum_{J in kb, J <= I} exp(s[I,J] / (sqrt(d) S)).
 // The selection kernel turns these into the softmax block sums.
 //
-// Persistent clusters of two CTAs (one CTA per SM) walk pair tiles (b, h,
-// row-tile pair, key tile) in order: the two CTAs compute row tiles 2 rp and
-// 2 rp + 1 against the same key tile, each loading half of it and
-// multicasting that half into both CTAs, so the key operand crosses from L2
-// once per pair (the operand stream from L2, not the tensor pipe, bounds
-// this kernel).  A stage is refilled only when the MMAs of both CTAs have
-// released it.
+// Persistent CTAs (one per SM) walk tiles (b, h, row tile, key tile) in
+// order, each CTA taking every gridDim-th tile, so the CTAs resident together
+// work on the key tiles of one or two heads and share them through L2.  Every
+// CTA loads its own Q and key tiles with plain TMA copies.
 // Warp 0: TMA producer (4-stage ring); warp 1: MMA issuer; warps 2..5:
 // epilogue.  Every wait is bounded and records the device error word.
+#include <algorithm>
+
 #include "launchers.h"
 #include "tc_common.cuh"
 
@@ -50,11 +49,10 @@ constexpr uint32_t kTmemCols = 512;      // two 128 x 256 fp32 accumulators
 
 enum Site : unsigned { kSiteEmpty = 1, kSiteFull, kSiteAccEmpty, kSiteAccFull };
 
-// Work units are pairs of 128-row tiles against one 256-key tile: the two
-// CTAs of a cluster take row tiles 2 rp and 2 rp + 1 of the same (b, h) and
-// share the key tile (each loads half and multicasts it to both).
+// Work units are (b, h, row tile, key tile): 128 reshaped rows against 256
+// reshaped keys, in that order (key tiles fastest).
 struct Tiles {
-  int Hq, R, p_s, n_rt, n_rp, per_bh, total;
+  int Hq, R, p_s, n_rt, per_bh, total;
 };
 
 // Key tiles needed by row tile rt: every 256-key tile holding a key J <= the
@@ -64,24 +62,18 @@ __device__ __host__ __forceinline__ int key_tiles(const Tiles& T, int rt) {
   return (T.p_s + i_max) / kN + 1;
 }
 
-// Key tiles of row-tile pair rp: those of its later tile (later rows see
-// more keys); the earlier tile's extra key tile, if any, is fully masked.
-__device__ __host__ __forceinline__ int pair_key_tiles(const Tiles& T, int rp) {
-  return key_tiles(T, min(2 * rp + 1, T.n_rt - 1));
-}
-
-__device__ __forceinline__ void tile_coords(const Tiles& T, int t, int& b, int& h, int& rp,
+__device__ __forceinline__ void tile_coords(const Tiles& T, int t, int& b, int& h, int& rt,
                                             int& kt) {
   const int bh = t / T.per_bh;
   int rem = t - bh * T.per_bh;
   b = bh / T.Hq;
   h = bh - b * T.Hq;
-  rp = 0;
-  while (rp < T.n_rp - 1) {
-    const int n = pair_key_tiles(T, rp);
+  rt = 0;
+  while (rt < T.n_rt - 1) {
+    const int n = key_tiles(T, rt);
     if (rem < n) break;
     rem -= n;
-    ++rp;
+    ++rt;
   }
   kt = rem;
 }
@@ -112,14 +104,12 @@ __global__ void __launch_bounds__(kThreads, 1) estimate_tc_kernel(
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = T.Hq / Hkv;
-  // clusters of two CTAs (consecutive blockIdx.x) walk the pair tiles
-  const int rank = (int)cluster_ctarank();
-  const int cl = (int)blockIdx.x >> 1, ncl = (int)gridDim.x >> 1;
+  const int cl = (int)blockIdx.x, ncl = (int)gridDim.x;
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full(s), 1);
-      mbar_init(empty(s), 2);  // both CTAs' MMAs must be done with the stage
+      mbar_init(empty(s), 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(acc_full(s), 1);
@@ -134,10 +124,8 @@ __global__ void __launch_bounds__(kThreads, 1) estimate_tc_kernel(
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-  // the peer may multicast into this CTA's stages and arrive on its barriers
-  // only once they are initialised
   tc_fence_before();
-  cluster_sync();
+  __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -149,9 +137,8 @@ __global__ void __launch_bounds__(kThreads, 1) estimate_tc_kernel(
       int it = 0;
       bool ok = true;
       for (int t = cl; ok && t < T.total; t += ncl) {
-        int b, h, rp, kt;
-        tile_coords(T, t, b, h, rp, kt);
-        const int rt = 2 * rp + rank;  // past the last tile: TMA fills zeros
+        int b, h, rt, kt;
+        tile_coords(T, t, b, h, rt, kt);
         const int hk = h / G;
         for (int ch = 0; ch < NCH; ++ch, ++it) {
           const int s = it % kStages;
@@ -165,9 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1) estimate_tc_kernel(
           const uint32_t a_dst = sb + s * kStageBytes;
           mbar_arrive_expect_tx(full(s), kStageBytes);
           tma_load_5d(a_dst, &tm_q, full(s), c0, h, S - 1 - phase, rt * kM, b);
-          // this CTA's half of the key tile, into both CTAs of the cluster
-          tma_load_5d_mc(a_dst + kABytes + rank * (kBBytes / 2), &tm_k, full(s), c0, hk, phase,
-                         kt * kN + rank * (kN / 2), b, 0x3);
+          tma_load_5d(a_dst + kABytes, &tm_k, full(s), c0, hk, phase, kt * kN, b);
         }
       }
       for (int s = 0; s < kStages && s < it; ++s)
@@ -217,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1) estimate_tc_kernel(
             else
               mma_bf16(acc, da + 2 * k, db + 2 * k, idesc, (ch > 0 || k > 0) ? 1u : 0u);
           }
-          mma_commit_mc(empty(s), 0x3);  // the stage is free in both CTAs
+          mma_commit(empty(s));
         }
         __syncwarp();
       }
@@ -239,9 +224,8 @@ __global__ void __launch_bounds__(kThreads, 1) estimate_tc_kernel(
                           kSiteAccFull))
         break;
       tc_fence_after();
-      int b, h, rp, kt;
-      tile_coords(T, t, b, h, rp, kt);
-      const int rt = 2 * rp + rank;
+      int b, h, rt, kt;
+      tile_coords(T, t, b, h, rt, kt);
       const int i = rt * kM + row;              // reshaped row within the chunk
       const int Ig = T.p_s + i;                 // global reshaped row
       const bool valid = i < T.R;
@@ -274,9 +258,8 @@ __global__ void __launch_bounds__(kThreads, 1) estimate_tc_kernel(
     }
   }
 
-  // no CTA leaves while its peer may still write into it
   tc_fence_before();
-  cluster_sync();
+  __syncthreads();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -305,7 +288,7 @@ cudaError_t launch_sd(const Problem& p, const void* q, const void* k, float* lse
                               (uint64_t)p.B};
     const uint64_t strides[4] = {(uint64_t)D * es, (uint64_t)p.Hkv * D * es,
                                  (uint64_t)S * p.Hkv * D * es, (uint64_t)p.Lk * p.Hkv * D * es};
-    const uint32_t box[5] = {cw, 1, 1, (uint32_t)(kN / 2), 1};  // half a key tile
+    const uint32_t box[5] = {cw, 1, 1, (uint32_t)kN, 1};
     if (!encode(&mk, k, 5, dims, strides, box)) return cudaErrorInvalidValue;
   }
   Tiles T;
@@ -313,9 +296,8 @@ cudaError_t launch_sd(const Problem& p, const void* q, const void* k, float* lse
   T.R = R;
   T.p_s = p.q_start_pos / S;
   T.n_rt = (R + kM - 1) / kM;
-  T.n_rp = (T.n_rt + 1) / 2;
   T.per_bh = 0;
-  for (int rp = 0; rp < T.n_rp; ++rp) T.per_bh += pair_key_tiles(T, rp);
+  for (int rt = 0; rt < T.n_rt; ++rt) T.per_bh += key_tiles(T, rt);
   T.total = p.B * p.Hq * T.per_bh;
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -327,28 +309,15 @@ cudaError_t launch_sd(const Problem& p, const void* q, const void* k, float* lse
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const float scale_log2 = 1.4426950408889634f / (sqrtf((float)D) * (float)S);
-  // persistent clusters of two CTAs, as many as fit at once (one CTA per SM)
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3((unsigned)(sms & ~1));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int ncl = 0;
-  e = cudaOccupancyMaxActiveClusters(&ncl, estimate_tc_kernel<S, D, F8>, &cfg);
+  // persistent: one CTA per SM (the kernel's shared memory allows no more)
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, estimate_tc_kernel<S, D, F8>,
+                                                    kThreads, smem);
   if (e != cudaSuccess) return e;
-  if (ncl < 1) return cudaErrorInvalidConfiguration;
-  if (ncl > T.total) ncl = T.total;
-  cfg.gridDim = dim3((unsigned)(2 * ncl));
-  e = cudaLaunchKernelEx(&cfg, estimate_tc_kernel<S, D, F8>, mq, mk, T, p.Hkv, p.nkb,
-                         scale_log2, lse_part, err);
-  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  const int grid = std::min(sms * per_sm, T.total);
+  estimate_tc_kernel<S, D, F8><<<grid, kThreads, smem, st>>>(mq, mk, T, p.Hkv, p.nkb,
+                                                             scale_log2, lse_part, err);
   return cudaGetLastError();
 }
 

@@ -148,15 +148,23 @@ int bsx_quantize_e4m3(const void* src, uint8_t* dst, long long n, void* stream);
  * call an allocator) and have no buffer to lend as scratch.
  *
  * Same arguments, outputs and results as bsx_xattn_estimate, minus
- * `workspace`/`workspace_bytes`.  The scratch is a 32 MiB array the library
- * reserves in global memory of every device that loads it, kept until the
- * process exits.  A problem whose bsx_estimate_workspace_bytes() exceeds
- * 32 MiB (33554432 bytes) returns BSX_ERR_WORKSPACE with nothing enqueued.
- * The first call on a device looks up the array's device address (with that
- * device current) and caches it; make that first call before any stream
- * capture.  All calls share the array: calls whose work overlaps on the GPU
- * (other streams, other host threads) race on it and must be serialised by
- * the caller.  This call allocates nothing.
+ * `workspace`/`workspace_bytes`.  The scratch is a fixed 32 MiB array in
+ * the library's own device code, held in global memory of every device that
+ * uses it until the process exits.  A problem whose
+ * bsx_estimate_workspace_bytes() exceeds 32 MiB (33554432 bytes) returns
+ * BSX_ERR_WORKSPACE with nothing enqueued.
+ * The first call on a device (with that device current) looks up the
+ * array's device address and caches it.  CUDA loads the library's device
+ * code lazily, so that first call is also when the 32 MiB are committed on
+ * the device: it can fail for lack of device memory (BSX_ERR_CUDA, the CUDA
+ * error printed to stderr).  Make it before the host engine fills its memory
+ * pool, and before any stream capture.  The cached address belongs to the
+ * device's primary context: after cudaDeviceReset, or from another driver
+ * context, it is stale and must not be used.  All calls share the array:
+ * calls whose work overlaps on the GPU (other streams, other host threads)
+ * race on it and must be serialised by the caller.  Nothing in it needs to
+ * start at zero (every cell read is first written by the same call).  This
+ * call allocates nothing.
  */
 int bsx_xattn_estimate_noalloc(bsx_shape s, const void* q, const void* k,
                                int q_len, int q_start_pos, int stride,
@@ -367,13 +375,24 @@ int bsx_chunk_step_host(bsx_shape s, const void* q_host, const void* k_host,
 int bsx_debug_drop_ring_item(int cta, int item);
 
 /*
- * Read and clear the device error word of the current device.  Waits for
- * the device to finish its work (this call is a diagnostic, not part of the
- * hot path).  *code receives the raw word (0 = no error; otherwise the
- * kernel and the wait that gave up).  Returns BSX_OK, BSX_ERR_TIMEOUT when
- * the word was set, or BSX_ERR_CUDA.
+ * Asynchronous error status of the device.  Waits
+ * for `stream` (a cudaStream_t; NULL is the legacy default stream, which also
+ * waits for the blocking streams), then reads and clears the device error
+ * word of the current device: the word in which a kernel records the first
+ * bounded device wait that expired (the word is per device, so it reports
+ * kernels of any stream that finished before the read; synchronise those
+ * streams first to cover them).  Returns BSX_OK when the word was clear,
+ * BSX_ERR_TIMEOUT when it was set, BSX_ERR_CUDA when a CUDA call failed
+ * (the message goes to stderr).  Not for the hot path: it synchronises.
  */
-int bsx_last_error(unsigned int* code);
+int bsx_last_error(void* stream);
+
+/*
+ * The raw error word read by the calling host thread's last bsx_last_error
+ * call (0 = none; otherwise bit 31 set, bits 0..7 the kernel: 1 = tcgen05
+ * attention, 2 = tcgen05 estimator, bits 8..15 the wait that gave up).
+ */
+unsigned int bsx_last_error_code(void);
 
 #ifdef __cplusplus
 }

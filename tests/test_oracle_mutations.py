@@ -4,7 +4,9 @@ duration of the test) and asserts that at least one pin from
 tests/test_oracle_pins.py then fails.  The mistakes are the kind a restatement
 of the pages could make: a stride reshape in the wrong direction, a dropped
 factor of the softmax scale, a strict causal rule, a wrong GQA head mapping,
-a selection that drops the crossing block or ignores the forced mass, an
+a selection that drops the crossing block or ignores the forced mass, a
+selection margin that is always 0 or taken over inclusive sums, a gap not
+divided by the row total, an
 attention scale of 1/d (block-sparse or offload), a merge that weights by
 LSE instead of exp(LSE), a CPU-block group shifted by one, an offload mask
 without the diagonal block.
@@ -18,7 +20,8 @@ from oracle import xattn_oracle as O
 from tests import test_oracle_pins as pins
 
 BLOCK = 128
-_offload_block_mask = O.offload_block_mask   # the unmutated function
+_offload_block_mask = O.offload_block_mask   # the unmutated functions
+_select_row = O.select_row
 
 
 def _q_forward(q_head, stride):
@@ -94,6 +97,37 @@ def _select_ignoring_forced_mass(a_row, forced, causal_end, threshold):
         else:
             break
     rs.total = total
+    return rs
+
+
+def _select_margin_zero(a_row, forced, causal_end, threshold):
+    rs = _select_row(a_row, forced, causal_end, threshold)
+    rs.margin = 0.0                             # every row would look near the threshold
+    return rs
+
+
+def _select_gap_not_normalised(a_row, forced, causal_end, threshold):
+    rs = _select_row(a_row, forced, causal_end, threshold)
+    rs.gap = rs.gap * rs.total                  # the raw mass difference, not / T
+    return rs
+
+
+def _select_margin_inclusive(a_row, forced, causal_end, threshold):
+    rs = _select_row(a_row, forced, causal_end, threshold)
+    vals = np.asarray(a_row, np.float64)[:causal_end]
+    total = float(vals.sum())
+    forced = sorted(set(f for f in forced if 0 <= f < causal_end))
+    if threshold >= 1.0 or total <= 0:
+        return rs
+    c = float(sum(vals[f] for f in forced))
+    margin = math.inf
+    for kb in sorted((kb for kb in range(causal_end) if kb not in forced),
+                     key=lambda kb: (-vals[kb], kb)):
+        margin = min(margin, abs(c + vals[kb] - threshold * total) / total)  # inclusive sum
+        if c >= threshold * total:
+            break
+        c += vals[kb]
+    rs.margin = margin
     return rs
 
 
@@ -187,6 +221,15 @@ def _selection_pins():
     pins.test_selection_forced_mass_counts()
 
 
+def _margin_gap_pins():
+    pins.test_selection_margin_and_gap_worked_example()
+    pins.test_selection_margin_and_gap_scaled_row_with_forced_block()
+    pins.test_selection_margin_counts_the_forced_mass_alone()
+    pins.test_selection_margin_and_gap_without_a_cut()
+    for seed in range(30):
+        pins.test_selection_margin_and_gap_brute_force(seed)
+
+
 def _bsa_pins():
     for P, dens in ((0, 1.0), (0, 0.5), (384, 0.4), (256, 1.0)):
         pins.test_bsa_matches_torch_attention(P, dens)
@@ -204,6 +247,11 @@ MUTATIONS = {
     "GQA head mapping h % Hkv": ("estimate_block_sums", _gqa_modulo_block_sums, _block_sum_pins),
     "crossing block dropped": ("select_row", _select_dropping_crossing, _selection_pins),
     "forced mass not counted": ("select_row", _select_ignoring_forced_mass, _selection_pins),
+    "selection margin always 0": ("select_row", _select_margin_zero, _margin_gap_pins),
+    "selection margin over inclusive sums": ("select_row", _select_margin_inclusive,
+                                             _margin_gap_pins),
+    "selection gap not divided by the row total": ("select_row", _select_gap_not_normalised,
+                                                   _margin_gap_pins),
     "key reshape taken reversed": (
         "stride_reshape_k", _k_reversed,
         lambda: (pins.test_reshape_positions_match_guide_example(),

@@ -206,6 +206,89 @@ def test_selection_forced_mass_counts():
     assert rs.selected.tolist() == [True, False, False, True]
 
 
+# margin and gap decide which rows the GPU parity tests exempt from a
+# bit-exact mask comparison (the near-threshold and near-tie rules), so they
+# are pinned like the selection itself: hand-computed rows, then brute force.
+def test_selection_margin_and_gap_worked_example():
+    """The guide's worked example (no forced block, T = 1, threshold 0.9):
+    sorted masses .40 .30 .15 .10 .05, exclusive cumulative sums 0, .40, .70,
+    .85, .95; the closest to the target .9 are .85 and .95, both .05 away.
+    The last selected block holds .10 and the first unselected .05: gap .05."""
+    g = _golden("selection_worked_example.json")
+    rs = O.select_row(np.array(g["row"]), g["forced"], len(g["row"]), g["threshold"])
+    assert abs(rs.margin - 0.05) <= 1e-12
+    assert abs(rs.gap - 0.05) <= 1e-12
+    assert abs(rs.total - 1.0) <= 1e-12
+
+
+def test_selection_margin_and_gap_scaled_row_with_forced_block():
+    """A row with total T = 4 and block 0 forced (mass .4): the others sorted
+    are 2.0, 0.8, 0.6, 0.2; exclusive sums (forced mass first) 0.4, 2.4, 3.2
+    against the target 0.7 * 4 = 2.8, so blocks 1 and 2 are taken and block 3
+    is the first left out.  margin = min(|0.4-2.8|, |2.4-2.8|, |3.2-2.8|)/4 =
+    0.1; gap = (0.8 - 0.6)/4 = 0.05."""
+    A = np.array([0.4, 2.0, 0.8, 0.6, 0.2])
+    rs = O.select_row(A, [0], 5, 0.7)
+    assert rs.selected.tolist() == [True, True, True, False, False]
+    assert abs(rs.margin - 0.1) <= 1e-12
+    assert abs(rs.gap - 0.05) <= 1e-12
+    assert abs(rs.total - 4.0) <= 1e-12
+
+
+def test_selection_margin_counts_the_forced_mass_alone():
+    """Forced mass .5 sits .02 below the target .52: the first exclusive sum
+    (the forced mass alone) is the closest one, margin .02; the block taken
+    next (.3) is the last selected and .2 the first unselected, gap .1."""
+    A = np.array([0.5, 0.3, 0.2])
+    rs = O.select_row(A, [0], 3, 0.52)
+    assert rs.selected.tolist() == [True, True, False]
+    assert abs(rs.margin - 0.02) <= 1e-12
+    assert abs(rs.gap - 0.1) <= 1e-12
+
+
+def test_selection_margin_and_gap_without_a_cut():
+    """No non-forced block: no exclusive sum to measure, margin and gap are
+    infinite.  Every block taken (exclusive sums .1, .5, .8 all below the
+    target .99999): no first unselected block, gap infinite, and the margin
+    is that of the last exclusive sum, .99999 - .8 = .19999."""
+    rs = O.select_row(np.array([0.7, 0.3]), [0, 1], 2, 0.9)
+    assert math.isinf(rs.margin) and math.isinf(rs.gap)
+    rs = O.select_row(np.array([0.1, 0.2, 0.3, 0.4]), [0], 4, 0.99999)
+    assert rs.selected.all()
+    assert math.isinf(rs.gap)
+    assert abs(rs.margin - 0.19999) <= 1e-12
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_selection_margin_and_gap_brute_force(seed):
+    """On random rows: margin = the smallest |c - tau*T| / T over the
+    exclusive cumulative sums c of every candidate in sorted order (forced
+    mass first), found by scanning all of them; gap = (smallest mass among the
+    selected non-forced blocks - largest mass among the unselected causal
+    blocks) / T."""
+    rng = np.random.default_rng(1000 + seed)
+    n = int(rng.integers(3, 14))
+    vals = rng.random(n) ** 2 * float(rng.choice([0.25, 1.0, 7.0]))
+    forced = sorted({0, n - 1})
+    tau = float(rng.choice([0.5, 0.8, 0.9, 0.95]))
+    rs = O.select_row(vals, forced, n, tau)
+    T = vals.sum()
+    free = sorted((kb for kb in range(n) if kb not in forced), key=lambda kb: (-vals[kb], kb))
+    c = vals[forced].sum()
+    dists = []
+    for kb in free:
+        dists.append(abs(c - tau * T) / T)
+        c += vals[kb]
+    assert abs(rs.margin - min(dists)) <= 1e-12
+    sel_free = [kb for kb in free if rs.selected[kb]]
+    unsel = [kb for kb in free if not rs.selected[kb]]
+    if sel_free and unsel:
+        want = (min(vals[sel_free]) - max(vals[unsel])) / T
+        assert abs(rs.gap - want) <= 1e-12
+    else:
+        assert math.isinf(rs.gap)
+
+
 def test_estimate_mask_structure_and_tau1():
     w = make_workload(seed=9, B=1, Hq=4, Hkv=2, d=32, Lk=1024, q_start_pos=512,
                       alpha=3.0, n_hot=1, dtype="bf16")

@@ -2,22 +2,21 @@
 
 bsx_xattn_estimate_noalloc serves callers that may not allocate device memory
 and have no buffer to lend as scratch (for instance a plugin whose host engine
-owns all device memory): it uses a fixed 32 MiB scratch array the library
-reserves on each device.  Its results must equal those of bsx_xattn_estimate
+owns all device memory): it uses a fixed 32 MiB scratch array held in the
+library's device code.  Its results must equal those of bsx_xattn_estimate
 with a caller workspace, call after call, since every call reuses (and must
 fully rewrite) the same scratch.  This file sorts last so that a run stopping
 at the first failure has already run every other test.
 """
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
 from block_sparse_long_xattn_gb300 import _lib as L
 from block_sparse_long_xattn_gb300 import bsx_xattn_estimate
 from block_sparse_long_xattn_gb300.inputs import make_workload
-from tests.helpers import A_TOL_REL, to_dev
+from tests.helpers import to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -54,9 +53,9 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
         m = torch.full(shape, 7, dtype=torch.uint8, device="cuda")
         assert _noalloc(lib, q, k, w.q_start_pos, S, tau, m, A) == 0
         torch.cuda.synchronize()
-        np.testing.assert_array_equal(m.cpu().numpy(), m_ref.cpu().numpy())
-        err = (A - A_ref).abs().max().item()
-        assert err <= A_TOL_REL * (128 // S), err
+        # the same kernels on the same inputs: bit-identical results
+        assert torch.equal(m, m_ref)
+        assert torch.equal(A, A_ref)
         assert L.bsx_last_error() == 0
 
 
