@@ -18,6 +18,7 @@ independent replica; the path has no cross-GPU exchange).
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                     [--step chunk|fused|offload|prefill|chunked]
     python bench.py --sweep              # density sweep, one JSON line per point
+    python bench.py --sparse             # the sparse-regime workloads, one line each
     python bench.py --impl reference     # the fp64 CPU oracle, timed on a sample
 """
 from __future__ import annotations
@@ -44,6 +45,12 @@ DEFAULT_WORKLOAD = "llama8b-32k-chunk4096"
 METRIC = "chunked-prefill tokens/s/layer at 32K ctx; % of bf16 TC / HBM roofline"
 UNIT = "tokens/s/layer"
 DOMINANT = "bsa_prefill"
+# Dense bf16 tensor-core figures for the clock-normalised and datasheet
+# fractions: a tcgen05 kind::f16 MMA of M128 N128 K16 retires in 64 SM cycles
+# (8192 flop per cycle per SM, measured in isolation on this part), and the
+# datasheet's dense bf16 figure for the whole GPU.
+MMA_FLOP_PER_CLK_SM = 8192
+DATASHEET_BF16_TFLOPS = 2250.0
 BSA_SOURCES = ("bsa_tc.cu", "bsa_simt.cu", "common.cuh", "tc_common.cuh")
 
 
@@ -403,17 +410,31 @@ def run_gpu(args):
     for n in bsa_names:
         kernels[f"{n}_tflops"] = flops[n] / (t_phase[n] / 1e3) / 1e12
 
+    # the step's roofline: every launch at its own bound (estimate at the
+    # larger of its tensor and HBM times, attention at the tensor peak, merge
+    # and map at the copy bandwidth), summed; tokens/s at that time against
+    # the measured tokens/s
+    merge_bytes = 3 * oh.numel() * oh.element_size() + 3 * lh.numel() * 4
+    roof_ms = {"estimate": max(est_fl / (tc_peak * 1e12), est_bytes / (hbm_peak * 1e9)) * 1e3}
+    for n in bsa_names:
+        roof_ms[n] = flops[n] / (tc_peak * 1e12) * 1e3
+    if "merge_map" in t_phase or "merge" in t_phase:
+        roof_ms["merge"] = merge_bytes / (hbm_peak * 1e9) * 1e3
+    if "merge_map" in t_phase and P >= cpu_tokens:
+        roof_ms["map"] = mask.numel() / (hbm_peak * 1e9) * 1e3
+    if "cpu_blocks" in t_phase:
+        roof_ms["cpu_blocks"] = 2 * mask.numel() / (hbm_peak * 1e9) * 1e3
+    roof_step_ms = sum(roof_ms.values())
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    at_clock = (MMA_FLOP_PER_CLK_SM * n_sm * clocks["sm_mhz"] * 1e6 / 1e12
+                if clocks.get("sm_mhz") else None)
+
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic (seeded planted-direction N(0,1) inputs)",
-        "config": {"workload": args.workload, "step": args.step, "B": B, "Hq": Hq,
-                   "Hkv": Hkv, "d": d, "q_len": Lq, "q_start_pos": P, "Lk": Lk, "stride": S,
-                   "threshold": tau, "cpu_block_tokens": cpu_tokens,
-                   "parallelism": f"replicas{world}",
-                   "l2": "flushed (256 MiB write) between timed steps", "seed": args.seed,
-                   "estimator_operands": args.estimator},
+        "config": config_dict(args, world),
         "roofline": {"kernel": DOMINANT, "bound": "tensor", "achieved": achieved,
                      "peak": tc_peak, "unit": "TFLOP/s", "frac": achieved / tc_peak,
                      "traffic": traffic, "peak_source": peak_src,
@@ -422,9 +443,21 @@ def run_gpu(args):
                      # whether the cap was reached: clocks.reasons)
                      "peak_sustained": tc_sustained,
                      "frac_vs_sustained": achieved / tc_sustained if tc_sustained else None,
-                     "flops_per_launch": bsa_flops_launch, "ms_per_launch": bsa_ms},
+                     "flops_per_launch": bsa_flops_launch, "ms_per_launch": bsa_ms,
+                     # the same launch against the tensor pipe's own rate at
+                     # the median SM clock of the timed region, and against
+                     # the datasheet's dense bf16 figure
+                     "peak_at_clock": at_clock,
+                     "frac_at_clock": achieved / at_clock if at_clock else None,
+                     "frac_of_datasheet": achieved / DATASHEET_BF16_TFLOPS},
         "kernels": kernels,
         "density": density,
+        # tokens/s as a fraction of its roofline: the step's launches each at
+        # their own bound (roofline_ms_per_launch), summed, against the step
+        "tokens_roofline_frac": roof_step_ms / ms_step,
+        "tokens_roofline": {"value": B * Lq / (roof_step_ms / 1e3), "unit": UNIT,
+                            "roofline_ms_per_step": roof_step_ms,
+                            "roofline_ms_per_launch": roof_ms},
         "e2e": {"value": tokens / (ms_e2e / 1e3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
                 "steps": n_e2e, "ms_per_step_serial": float(np.mean(serial_ms)),
@@ -434,7 +467,9 @@ def run_gpu(args):
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline and args.step == "chunk":
-        result["cpu_baseline"] = oracle_baseline(w, S, tau, args.cpu_heads)
+        result["cpu_baseline"], ests, heads = oracle_baseline(w, S, tau, args.cpu_heads,
+                                                              keep_estimates=True)
+        result["near_threshold_rows"] = mask_rows_vs_oracle(mask.cpu().numpy(), ests, heads)
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:
@@ -579,11 +614,7 @@ def run_chunked(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic (seeded planted-direction N(0,1) inputs)",
-        "config": {"workload": args.workload, "step": "chunked", "B": B, "Hq": Hq, "Hkv": Hkv,
-                   "d": d, "seq_len": L, "chunk": chunk, "chunks": n_chunks, "stride": S,
-                   "threshold": tau, "cpu_block_tokens": cpu_tokens,
-                   "parallelism": f"replicas{world}",
-                   "l2": "flushed (256 MiB write) between timed steps", "seed": args.seed},
+        "config": config_dict(args, world),
         "roofline": {"kernel": DOMINANT, "bound": "tensor", "achieved": achieved,
                      "peak": tc_peak, "unit": "TFLOP/s", "frac": achieved / tc_peak,
                      "traffic": None, "peak_source": peak_src, "peak_sustained": tc_sustained,
@@ -698,6 +729,103 @@ def run_sweep(args):
         raise SystemExit("device error word set after the sweep")
 
 
+def run_sparse(args):
+    """The sparse regime: the chunk step (estimate, attention on history and
+    current chunk in one launch, merge, map) on each sparse workload (the 32K
+    and 128K chunk shapes with a strong planted direction; the estimator
+    selects about 6-50% of the causal blocks).  One JSON line per workload:
+    the mask density, the step's tokens/s and its roofline fraction, the
+    attention launch's TFLOP/s over the selected blocks and its fractions.
+    Device-resident inputs, L2 flushed between timed steps."""
+    import torch
+
+    import block_sparse_long_xattn_gb300 as bsx
+    from block_sparse_long_xattn_gb300.inputs import SPARSE_CONFIGS
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    hbm_peak, tc_peak, tc_sustained, peak_src = _peaks()
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    names = [args.workload] if args.workload in SPARSE_CONFIGS else list(SPARSE_CONFIGS)
+    for name in names:
+        c = dict(CONFIGS[name])
+        S, tau = c.pop("stride"), c.pop("threshold")
+        w = make_workload(seed=args.seed, **c)
+        B, Lq, Hq, d = w.q.shape
+        P, Lk = w.q_start_pos, w.k.shape[1]
+        cur, nkb = P // 128, Lk // 128
+        q, k, v = (torch.from_numpy(x).to(torch.bfloat16).to(dev) for x in (w.q, w.k, w.v))
+        del w
+        mask = torch.empty((B, Hq, Lq // 128, nkb), dtype=torch.uint8, device=dev)
+        ws = torch.empty(bsx.bsx_estimate_workspace_bytes(bsx.shape_of(q, k), Lq, P, S),
+                         dtype=torch.uint8, device=dev)
+        oh, oc = torch.empty_like(q), torch.empty_like(q)
+        lh = torch.empty((B, Hq, Lq), dtype=torch.float32, device=dev)
+        lc = torch.empty_like(lh)
+        keep = torch.empty((B, P // 1024), dtype=torch.uint8, device=dev)
+        est_fl = estimate_flops(c, Lq, P, S)
+        est_bytes = (q.numel() + k.numel()) * q.element_size() + mask.numel()
+        merge_bytes = 3 * oh.numel() * oh.element_size() + 3 * lh.numel() * 4
+        causal_blocks = sum(cur + qb + 1 for qb in range(Lq // 128)) * B * Hq
+
+        def step(ev=None):
+            if ev:
+                ev[0].record(stream)
+            bsx.bsx_xattn_estimate(q, k, P, S, tau, mask=mask, workspace=ws, stream=stream)
+            if ev:
+                ev[1].record(stream)
+            bsx.bsx_bsa_prefill_split(q, k, v, mask, P, o_hist=oh, lse_hist=lh,
+                                      o_curr=oc, lse_curr=lc, stream=stream)
+            if ev:
+                ev[2].record(stream)
+            bsx.bsx_merge_attn(oh, lh, oc, lc, stream=stream)
+            bsx.bsx_map_mask_to_cpu_blocks(mask, P, 1024, keep=keep, stream=stream)
+            if ev:
+                ev[3].record(stream)
+
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        m = mask.cpu().numpy()
+        density = float(m.astype(bool).sum()) / causal_blocks
+        fl = bsa_flops(m, P, 0, cur, d) + bsa_flops(m, P, cur, nkb, d)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
+               for _ in range(args.steps)]
+        with ClockSampler(0) as clk:
+            t0 = time.time()
+            for i in range(args.steps):
+                flush.zero_()
+                step(evs[i])
+            torch.cuda.synchronize()
+            clk.mark(t0, time.time())
+        clocks = clk.summary()
+        t = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(3)] for e in evs])
+        t_est, t_bsa, t_rest = (float(x) for x in t.mean(axis=0))
+        ms = t_est + t_bsa + t_rest
+        bsa_tf = fl / (t_bsa / 1e3) / 1e12
+        roof_ms = (max(est_fl / (tc_peak * 1e12), est_bytes / (hbm_peak * 1e9))
+                   + fl / (tc_peak * 1e12) + (merge_bytes + m.size) / (hbm_peak * 1e9)) * 1e3
+        at_clock = (MMA_FLOP_PER_CLK_SM * n_sm * clocks["sm_mhz"] * 1e6 / 1e12
+                    if clocks.get("sm_mhz") else None)
+        print(json.dumps({
+            "sparse": name, "alpha": c["alpha"], "n_hot": c["n_hot"], "stride": S,
+            "threshold": tau, "density": density, "ms_per_step": ms,
+            "tokens_per_s_layer": B * Lq / (ms / 1e3), "tokens_roofline_frac": roof_ms / ms,
+            "bsa_ms": t_bsa, "bsa_flops": fl, "bsa_tflops": bsa_tf,
+            "bsa_frac": bsa_tf / tc_peak,
+            "bsa_frac_at_clock": bsa_tf / at_clock if at_clock else None,
+            "estimate_ms": t_est, "estimate_tflops": est_fl / (t_est / 1e3) / 1e12,
+            "estimate_tc_frac": est_fl / (t_est / 1e3) / 1e12 / tc_peak,
+            "merge_map_ms": t_rest, "steps": args.steps, "warmup": args.warmup,
+            "peak_source": peak_src, "clocks": clocks}), flush=True)
+        del q, k, v, ws, oh, oc
+        torch.cuda.empty_cache()
+    if bsx.bsx_last_error() != 0:
+        raise SystemExit("device error word set after the sparse runs")
+
+
 # ---------------------------------------------------------------------------
 def _oracle_threads():
     try:
@@ -710,26 +838,73 @@ def _oracle_threads():
     return os.cpu_count() or 1
 
 
-def oracle_baseline(w, stride, tau, n_heads):
+def oracle_baseline(w, stride, tau, n_heads, keep_estimates=False):
     """Time the fp64 oracle's chunk step on a sample of q-heads and scale it to
-    the whole chunk (heads are independent)."""
+    the whole chunk (heads are independent).  With keep_estimates, also
+    return the oracle's estimate of each sampled head and the head list."""
     from oracle import xattn_oracle as O
     G = w.q.shape[2] // w.k.shape[2]
     heads = list(range(0, w.q.shape[2], G))[:n_heads]
+    ests = []
     t0 = time.perf_counter()
     for h in heads:
         kv = h // G
-        O.chunk_step(w.q[:, :, h:h + 1], w.k[:, :, kv:kv + 1], w.v[:, :, kv:kv + 1],
-                     w.q_start_pos, stride, tau, 1024)
+        est, _, _, _ = O.chunk_step(w.q[:, :, h:h + 1], w.k[:, :, kv:kv + 1],
+                                    w.v[:, :, kv:kv + 1], w.q_start_pos, stride, tau, 1024)
+        ests.append(est)
     dt = time.perf_counter() - t0
     per_step = dt / len(heads) * w.q.shape[2]
-    return {"value": w.q.shape[0] * w.q.shape[1] / per_step, "unit": UNIT,
+    base = {"value": w.q.shape[0] * w.q.shape[1] / per_step, "unit": UNIT,
             "cores": _oracle_threads(), "kind": "oracle",
             "sample": f"chunk step for {len(heads)} of {w.q.shape[2]} q-heads "
                       f"({dt:.1f} s), scaled by the head count"}
+    if keep_estimates:
+        return base, ests, heads
+    return base
+
+
+def mask_rows_vs_oracle(mask_gpu, ests, heads, margin_tol=1e-4):
+    """The GPU mask rows of the sampled heads against the oracle's: rows,
+    rows near the threshold (some exclusive cumulative mass within 1e-4 of the
+    target, relative to the row total: exempt from the bit-exact rule), and
+    the other rows that differ (0 when the masks agree)."""
+    rows = near = differ = 0
+    for h, est in zip(heads, ests):
+        g = mask_gpu[:, h].astype(bool)
+        o = est.mask[:, 0]
+        is_near = est.margin[:, 0] <= margin_tol
+        same = (g == o).all(axis=-1)
+        rows += g.shape[0] * g.shape[1]
+        near += int(is_near.sum())
+        differ += int((~same & ~is_near).sum())
+    return {"heads": heads, "rows": rows, "near_threshold": near,
+            "other_rows_differing": differ, "margin_tol": margin_tol}
+
+
+def config_dict(args, world):
+    """The workload description both arms print."""
+    cfg = dict(CONFIGS[args.workload])
+    B, Hq, Hkv, d = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["d"]
+    out = {"workload": args.workload, "step": args.step, "B": B, "Hq": Hq, "Hkv": Hkv,
+           "d": d, "stride": cfg["stride"], "threshold": cfg["threshold"],
+           "cpu_block_tokens": 1024, "parallelism": f"replicas{world}",
+           "l2": "flushed (256 MiB write) between timed steps", "seed": args.seed,
+           "estimator_operands": args.estimator}
+    if "chunk" in cfg and args.step == "chunked":
+        out.update({"seq_len": cfg["Lk"], "chunk": cfg["chunk"],
+                    "chunks": cfg["Lk"] // cfg["chunk"]})
+    else:
+        out.update({"q_len": cfg["Lk"] - cfg["q_start_pos"], "q_start_pos": cfg["q_start_pos"],
+                    "Lk": cfg["Lk"]})
+    return out
 
 
 def run_reference(args):
+    """The fp64 oracle as the reference arm.  One step = the oracle's chunk
+    step on one q-head of the workload (a bounded sample: a whole chunk of 32
+    heads would take minutes); ms_per_step is that step's measured time, and
+    value scales it to the whole chunk by the head count (heads are
+    independent)."""
     rank, world, _ = _env_rank()
     if rank != 0:
         return
@@ -737,21 +912,23 @@ def run_reference(args):
     S, tau = cfg.pop("stride"), cfg.pop("threshold")
     cfg.pop("chunk", None)
     w = make_workload(seed=args.seed, **cfg)
-    # each step: the oracle's chunk step on one q-head (a bounded sample),
-    # scaled to the whole chunk by the head count
     for _ in range(args.warmup):
         oracle_baseline(w, S, tau, 1)
     vals = [oracle_baseline(w, S, tau, 1) for _ in range(args.steps)]
-    ms = float(np.mean([w.q.shape[1] / v["value"] * 1e3 for v in vals]))
-    value = w.q.shape[0] * w.q.shape[1] / (ms / 1e3)
+    Hq = w.q.shape[2]
+    # each sample's tokens/s was scaled by Hq; undo it for the step's own time
+    ms = float(np.mean([w.q.shape[1] / v["value"] * 1e3 for v in vals])) / Hq
+    value = w.q.shape[0] * w.q.shape[1] / (ms * Hq / 1e3)
     base = dict(vals[-1])
     base["value"] = value
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "step_is": f"the oracle's chunk step on 1 of {Hq} q-heads",
+        "value_scaling": f"value = tokens per chunk / (ms_per_step x {Hq} q-heads)",
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic (seeded planted-direction N(0,1) inputs)",
-        "config": {"workload": args.workload, "parallelism": "cpu oracle, rank 0 only"},
+        "config": config_dict(args, world),
         "cpu_baseline": base,
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
@@ -783,12 +960,17 @@ def main():
     ap.add_argument("--nvtx", action="store_true",
                     help="wrap each phase of the step in an NVTX range (for a profiler's "
                          "timeline; adds host work to the timed region)")
+    ap.add_argument("--sparse", action="store_true",
+                    help="the sparse-regime workloads (32K and 128K chunks, 6-50%% of the "
+                         "causal blocks selected), one JSON line each; with --workload "
+                         "naming one of them, that one only")
     ap.add_argument("--sweep", action="store_true",
                     help="density sweep on the 32K / 4096-chunk shapes (thresholds 0.8-1.0 "
                          "on alpha 0, 2, 4): one JSON line per point")
     args = ap.parse_args()
     if args.steps is None:
-        args.steps = (50 if args.sweep else 200) if args.impl == "gb300" else 20
+        args.steps = (50 if (args.sweep or args.sparse) else 200) \
+            if args.impl == "gb300" else 20
     if args.warmup < 3 and args.impl == "gb300":
         ap.error("at least 3 warm-up steps")
     if args.step == "prefill" and args.workload == DEFAULT_WORKLOAD:
@@ -802,6 +984,8 @@ def main():
         run_reference(args)
     elif args.sweep:
         run_sweep(args)
+    elif args.sparse:
+        run_sparse(args)
     elif args.step == "chunked":
         run_chunked(args)
     else:

@@ -13,10 +13,10 @@
 // taken while the cumulative mass, forced mass included, is below
 // threshold * sum(A).  The crossing block is kept (the section's worked
 // example); threshold >= 1 keeps every causal block.  One CTA per (b, h, qb):
-// a bitonic sort of packed (A, kb) keys in shared memory, then a block-wide
-// exclusive scan of the sorted masses.  Rows of at most 1024 key blocks take
-// select_warp_kernel instead: one warp per (b, h, qb), everything in
-// registers and warp shuffles.
+// rows of at most 1024 key blocks take select_cta_kernel (everything in
+// registers, warp shuffles and a few shared-memory stages); longer rows take
+// select_kernel (a bitonic sort of packed (A, kb) keys in shared memory, then
+// a block-wide exclusive scan of the sorted masses).
 #include "common.cuh"
 #include "launchers.h"
 
@@ -229,225 +229,235 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// The same computation with one warp per (b, h, qb) row, for rows of at most
-// 32 * KPL key blocks.  Element i of the row (key block i before sorting,
-// sorted position i after) lives in lane i % 32, register i / 32, so every
-// compare-exchange of the bitonic network is either a warp shuffle (partner
-// distance below 32) or a swap between two registers of one lane; no block
-// barrier is needed anywhere.
-constexpr int kWarpsPerCta = 4;
-
-// One bitonic stage between registers t and t + TJ of every lane (element
-// i = t * 32 + lane; partner distance 32 * TJ); descending runs where
-// (i & k) == 0.
-template <int KPL, int TJ>
-__device__ __forceinline__ void bitonic_regs(unsigned long long (&key)[KPL], int k, int lane) {
-  if constexpr (TJ < KPL) {
-#pragma unroll
-    for (int t = 0; t < KPL; ++t) {
-      if ((t & TJ) == 0) {
-        const int i = t * 32 + lane;  // lower index of the pair
-        const bool desc = (i & k) == 0;
-        const unsigned long long x = key[t], y = key[t | TJ];
-        const bool swap = desc ? (x < y) : (x > y);
-        key[t] = swap ? y : x;
-        key[t | TJ] = swap ? x : y;
-      }
-    }
-  }
-}
-
-template <int RB, int KPL>
-__global__ void __launch_bounds__(32 * kWarpsPerCta, (KPL <= 8 && RB <= 16) ? 4 : 2) select_warp_kernel(
+// The same computation for rows of at most 256 * E key blocks, one CTA of 256
+// threads per (b, h, qb) row, with no phase that runs on a single warp:
+//  1. every thread loads the partials of its key blocks kb = e * 256 + tid
+//     (128/S consecutive floats each, all loads in flight at once) and
+//     stores them transposed, vals[i][kb], in shared memory;
+//  2. each reshaped row i is reduced by 256/RB threads (a max, then a sum of
+//     exponentials, each followed by a shuffle reduction inside the group):
+//     row_lse[i];
+//  3. each thread sums its key blocks' probabilities over the rows: A[kb];
+//     one block reduction gives the row total T;
+//  4. a bitonic sort of packed (A, ~kb) 64-bit keys, descending, position
+//     p = tid * E + e: partner distances below E are register swaps, below
+//     32 E warp shuffles, the others go through shared memory (two buffers,
+//     one barrier per stage);
+//  5. an exclusive scan of the sorted masses (per thread, then per warp by
+//     shuffles, then across warps), and every candidate whose exclusive mass
+//     plus the forced mass is below threshold * T is selected.
+template <int RB, int E>
+__global__ void __launch_bounds__(kSelThreads) select_cta_kernel(
     const float* __restrict__ lse_part, int Hq, int nqb, int nkb, int R, int cur,
     float threshold, uint8_t* __restrict__ mask, float* __restrict__ block_sums) {
-  constexpr int N = 32 * KPL;  // padded row length (a power of two)
-  __shared__ __align__(16) uint8_t sel_all[kWarpsPerCta][N];
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const int row_id = blockIdx.x * kWarpsPerCta + wid;  // (h, qb) flattened
-  if (row_id >= Hq * nqb) return;
-  const int qb = row_id % nqb;
-  const int h = row_id / nqb;
-  const int b = blockIdx.y;
-  uint8_t* sel = sel_all[wid];
+  constexpr int NT = kSelThreads;
+  constexpr int N = NT * E;                  // padded row length (a power of two)
+  constexpr int GR = NT / RB;                // threads per row in step 2 (8, 16 or 32)
+  constexpr int LD = N + (GR < 32 ? GR : 0);  // row stride: the row groups of a warp
+                                              // read disjoint banks
+  constexpr int NW = NT / 32;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  float* vals = reinterpret_cast<float*>(smem_raw);                              // [RB][LD]
+  unsigned long long* kbuf = reinterpret_cast<unsigned long long*>(vals + RB * LD);  // [2][N]
+  uint8_t* sel = reinterpret_cast<uint8_t*>(kbuf + 2 * N);                       // [N]
+  __shared__ float row_lse[RB];
+  __shared__ float red[NW];
+  __shared__ float forced[2];
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int qb = blockIdx.x % nqb, h = blockIdx.x / nqb, b = blockIdx.y;
   const int diag = cur + qb;
   const int ncausal = diag + 1;
   const float* base = lse_part + ((long long)(b * Hq + h) * nkb) * R + qb * RB;
 
-  // ---- row maxima, then row sums -> row LSE ----
-  float acc[RB];
+  // ---- 1. partials, transposed into shared memory ----
 #pragma unroll
-  for (int i = 0; i < RB; ++i) acc[i] = -INFINITY;
-#pragma unroll 4
-  for (int kb = lane; kb < ncausal; kb += 32) {
-    const float4* q = reinterpret_cast<const float4*>(base + (long long)kb * R);
+  for (int e = 0; e < E; ++e) {
+    const int kb = e * NT + tid;
+    float4 v[RB / 4];
+    const float4* src = reinterpret_cast<const float4*>(base + (long long)kb * R);
 #pragma unroll
-    for (int c = 0; c < RB / 4; ++c) {
-      const float4 v = __ldg(q + c);
-      acc[4 * c + 0] = fmaxf(acc[4 * c + 0], v.x);
-      acc[4 * c + 1] = fmaxf(acc[4 * c + 1], v.y);
-      acc[4 * c + 2] = fmaxf(acc[4 * c + 2], v.z);
-      acc[4 * c + 3] = fmaxf(acc[4 * c + 3], v.w);
-    }
-  }
-  float rmax[RB];
-#pragma unroll
-  for (int i = 0; i < RB; ++i) {
-    rmax[i] = warp_max(acc[i]);
-    acc[i] = 0.f;
-  }
-#pragma unroll 4
-  for (int kb = lane; kb < ncausal; kb += 32) {
-    const float4* q = reinterpret_cast<const float4*>(base + (long long)kb * R);
+    for (int c = 0; c < RB / 4; ++c)
+      v[c] = kb < ncausal ? __ldg(src + c) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
 #pragma unroll
     for (int c = 0; c < RB / 4; ++c) {
-      const float4 v = __ldg(q + c);
-      acc[4 * c + 0] += __expf(v.x - rmax[4 * c + 0]);
-      acc[4 * c + 1] += __expf(v.y - rmax[4 * c + 1]);
-      acc[4 * c + 2] += __expf(v.z - rmax[4 * c + 2]);
-      acc[4 * c + 3] += __expf(v.w - rmax[4 * c + 3]);
+      vals[(4 * c + 0) * LD + kb] = v[c].x;
+      vals[(4 * c + 1) * LD + kb] = v[c].y;
+      vals[(4 * c + 2) * LD + kb] = v[c].z;
+      vals[(4 * c + 3) * LD + kb] = v[c].w;
     }
+    sel[kb] = 0;
   }
-  float rlse[RB];
-#pragma unroll
-  for (int i = 0; i < RB; ++i) rlse[i] = rmax[i] + logf(warp_sum(acc[i]));
+  __syncthreads();
 
-  // ---- block sums A[kb], kb = t * 32 + lane ----
-  float a[KPL];
+  // ---- 2. row LSE: GR threads per row ----
+  {
+    const int i = tid / GR, j = tid % GR;
+    const float* rowp = vals + i * LD;
+    float m = -INFINITY;
+#pragma unroll
+    for (int c = j; c < N; c += GR) m = fmaxf(m, rowp[c]);
+#pragma unroll
+    for (int o = GR / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float sum = 0.f;
+#pragma unroll
+    for (int c = j; c < N; c += GR) sum += __expf(rowp[c] - m);
+#pragma unroll
+    for (int o = GR / 2; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (j == 0) row_lse[i] = m + logf(sum);
+  }
+  __syncthreads();
+
+  // ---- 3. block sums A[kb] and the row total ----
+  float a[E];
   float part = 0.f;
 #pragma unroll
-  for (int t = 0; t < KPL; ++t) {
-    const int kb = t * 32 + lane;
-    float v = 0.f;
+  for (int e = 0; e < E; ++e) {
+    const int kb = e * NT + tid;
+    float x = 0.f;
     if (kb < ncausal) {
-      const float4* q = reinterpret_cast<const float4*>(base + (long long)kb * R);
 #pragma unroll
-      for (int c = 0; c < RB / 4; ++c) {
-        const float4 w = __ldg(q + c);
-        v += __expf(w.x - rlse[4 * c + 0]) + __expf(w.y - rlse[4 * c + 1]) +
-             __expf(w.z - rlse[4 * c + 2]) + __expf(w.w - rlse[4 * c + 3]);
-      }
+      for (int i = 0; i < RB; ++i) x += __expf(vals[i * LD + kb] - row_lse[i]);
     }
-    a[t] = v;
-    part += v;
-    if (block_sums && kb < nkb) block_sums[(((long long)b * Hq + h) * nqb + qb) * nkb + kb] = v;
+    a[e] = x;
+    part += x;
+    if (block_sums && kb < nkb) block_sums[(((long long)b * Hq + h) * nqb + qb) * nkb + kb] = x;
+    if (kb == 0) forced[0] = x;
+    if (kb == diag) forced[1] = x;
   }
-  const float total = warp_sum(part);
+  part = warp_sum(part);
+  if (lane == 0) red[warp] = part;
+  __syncthreads();
+  float total = 0.f;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) total += red[w];
 
   uint8_t* mrow = mask + (((long long)b * Hq + h) * nqb + qb) * nkb;
   if (threshold >= 1.0f) {
-    for (int kb = lane; kb < nkb; kb += 32) mrow[kb] = kb < ncausal ? 1 : 0;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int kb = e * NT + tid;
+      if (kb < nkb) mrow[kb] = kb < ncausal ? 1 : 0;
+    }
     return;
   }
 
-  // ---- bitonic sort of (A, kb) keys, descending (ties: lower kb first) ----
-  unsigned long long key[KPL];
+  // ---- 4. bitonic sort of (A, kb) keys, descending (ties: lower kb first) ----
+  unsigned long long key[E];
 #pragma unroll
-  for (int t = 0; t < KPL; ++t) {
-    const int kb = t * 32 + lane;
-    key[t] = (kb < ncausal && kb != 0 && kb != diag)
-                 ? ((unsigned long long)__float_as_uint(a[t]) << 32) |
+  for (int e = 0; e < E; ++e) {
+    const int kb = e * NT + tid;
+    key[e] = (kb < ncausal && kb != 0 && kb != diag)
+                 ? ((unsigned long long)__float_as_uint(a[e]) << 32) |
                        (unsigned long long)(0xFFFFFFFFu - (unsigned)kb)
                  : 0ull;
   }
-  // For 1024-key rows the stage loops stay rolled and only the per-register
-  // work is unrolled: their fully unrolled network overflows the instruction
-  // cache.  Register distances (partner 32 or more elements away) dispatch
-  // to bodies with a compile-time distance, so no register is indexed at
-  // run time; for 256-key rows everything unrolls.
-  auto stage = [&](int k, int j) {
-    if (j >= 32) {
-      switch (j >> 5) {
-        case 1: bitonic_regs<KPL, 1>(key, k, lane); break;
-        case 2: bitonic_regs<KPL, 2>(key, k, lane); break;
-        case 4: bitonic_regs<KPL, 4>(key, k, lane); break;
-        case 8: bitonic_regs<KPL, 8>(key, k, lane); break;
-        default: bitonic_regs<KPL, 16>(key, k, lane); break;
-      }
-    } else {
-      const bool lower = (lane & j) == 0;
+  int buf = 0;
 #pragma unroll
-      for (int t = 0; t < KPL; ++t) {
-        const int i = t * 32 + lane;
-        const bool desc = (i & k) == 0;
-        const unsigned long long y = __shfl_xor_sync(0xffffffffu, key[t], j);
-        const unsigned long long x = key[t];
-        // the lower index keeps the larger key in a descending run
-        const bool take_max = (lower == desc);
-        key[t] = take_max ? (x > y ? x : y) : (x < y ? x : y);
+  for (int k = 2; k <= N; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (j < E) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          if ((e & j) == 0) {
+            const int p = tid * E + e;  // lower position of the pair
+            const bool desc = (p & k) == 0;
+            const unsigned long long x = key[e], y = key[e | j];
+            const bool swap = desc ? (x < y) : (x > y);
+            key[e] = swap ? y : x;
+            key[e | j] = swap ? x : y;
+          }
+        }
+      } else if (j < 32 * E) {
+        const bool lower = (tid & (j / E)) == 0;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int p = tid * E + e;
+          const bool desc = (p & k) == 0;
+          const unsigned long long y = __shfl_xor_sync(0xffffffffu, key[e], j / E);
+          const unsigned long long x = key[e];
+          key[e] = (lower == desc) ? (x > y ? x : y) : (x < y ? x : y);
+        }
+      } else {
+        unsigned long long* kb_ = kbuf + buf * N;
+#pragma unroll
+        for (int e = 0; e < E; ++e) kb_[tid * E + e] = key[e];
+        __syncthreads();
+        const bool lower = (tid & (j / E)) == 0;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int p = tid * E + e;
+          const bool desc = (p & k) == 0;
+          const unsigned long long y = kb_[p ^ j];
+          const unsigned long long x = key[e];
+          key[e] = (lower == desc) ? (x > y ? x : y) : (x < y ? x : y);
+        }
+        buf ^= 1;
       }
     }
-  };
-  if constexpr (KPL <= 8) {
-#pragma unroll
-    for (int k = 2; k <= N; k <<= 1)
-#pragma unroll
-      for (int j = k >> 1; j > 0; j >>= 1) stage(k, j);
-  } else {
-#pragma unroll 1
-    for (int k = 2; k <= N; k <<= 1)
-#pragma unroll 1
-      for (int j = k >> 1; j > 0; j >>= 1) stage(k, j);
   }
 
-  // ---- exclusive scan of the sorted masses; keep while below the target ----
-  const int nforced = diag == 0 ? 1 : 2;
-  const int ncand = ncausal - nforced;
-  // A of the diagonal block, recomputed by every lane the way its owner did
-  // (selecting it from the owner's registers would need a runtime index)
-  float a_diag = 0.f;
-  {
-    const float4* q = reinterpret_cast<const float4*>(base + (long long)diag * R);
+  // ---- 5. exclusive scan of the sorted masses; keep while below the target ----
+  float pre[E];
+  float tsum = 0.f;
 #pragma unroll
-    for (int c = 0; c < RB / 4; ++c) {
-      const float4 w = __ldg(q + c);
-      a_diag += __expf(w.x - rlse[4 * c + 0]) + __expf(w.y - rlse[4 * c + 1]) +
-                __expf(w.z - rlse[4 * c + 2]) + __expf(w.w - rlse[4 * c + 3]);
-    }
+  for (int e = 0; e < E; ++e) {
+    pre[e] = tsum;
+    tsum += __uint_as_float((unsigned)(key[e] >> 32));
   }
-  const float forced_mass = __shfl_sync(0xffffffffu, a[0], 0) + (diag != 0 ? a_diag : 0.f);
+  float incl = tsum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  __syncthreads();  // every thread is past its reads of red[]
+  if (lane == 31) red[warp] = incl;
+  __syncthreads();
+  float before = incl - tsum;  // exclusive within the warp
+#pragma unroll
+  for (int w = 0; w < NW; ++w)
+    if (w < warp) before += red[w];
+  const float forced_mass = forced[0] + (diag != 0 ? forced[1] : 0.f);
   const float target = threshold * total;
-  for (int kb = lane; kb < N; kb += 32) sel[kb] = 0;
-  __syncwarp();
-  float carry = 0.f;  // mass of the sorted positions before register t
 #pragma unroll
-  for (int t = 0; t < KPL; ++t) {
-    const int i = t * 32 + lane;
-    const float v = i < ncand ? __uint_as_float((unsigned)(key[t] >> 32)) : 0.f;
-    float incl = v;
+  for (int e = 0; e < E; ++e) {
+    if (key[e] != 0ull && forced_mass + (before + pre[e]) < target)
+      sel[0xFFFFFFFFu - (unsigned)(key[e] & 0xFFFFFFFFull)] = 1;
+  }
+  __syncthreads();
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float n = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += n;
-    }
-    const float excl = carry + incl - v;
-    if (i < ncand && forced_mass + excl < target)
-      sel[0xFFFFFFFFu - (unsigned)(key[t] & 0xFFFFFFFFull)] = 1;
-    carry += __shfl_sync(0xffffffffu, incl, 31);
+  for (int e = 0; e < E; ++e) {
+    const int kb = e * NT + tid;
+    if (kb < nkb) mrow[kb] = (kb < ncausal && (kb == 0 || kb == diag || sel[kb])) ? 1 : 0;
   }
-  __syncwarp();
-  for (int kb = lane; kb < nkb; kb += 32) {
-    uint8_t m = sel[kb];
-    if (kb == 0 || kb == diag) m = 1;
-    mrow[kb] = kb < ncausal ? m : 0;
-  }
+}
+
+template <int RB, int E>
+cudaError_t launch_cta(const Problem& p, float threshold, const float* lse_part,
+                       uint8_t* mask, float* block_sums, cudaStream_t st) {
+  constexpr int N = kSelThreads * E;
+  constexpr int GR = kSelThreads / RB;
+  constexpr int LD = N + (GR < 32 ? GR : 0);
+  const size_t smem = (size_t)RB * LD * 4 + (size_t)2 * N * 8 + N;
+  cudaError_t e = cudaFuncSetAttribute(select_cta_kernel<RB, E>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int R = p.q_len / (kBlock / RB);
+  dim3 grid(p.Hq * p.nqb, p.B);
+  select_cta_kernel<RB, E><<<grid, kSelThreads, smem, st>>>(
+      lse_part, p.Hq, p.nqb, p.nkb, R, p.q_start_pos / kBlock, threshold, mask, block_sums);
+  return cudaGetLastError();
 }
 
 template <int RB>
 cudaError_t launch_rb(const Problem& p, float threshold, const float* lse_part,
                       uint8_t* mask, float* block_sums, cudaStream_t st) {
   const int R = p.q_len / (kBlock / RB);
-  const int rows = p.B * p.Hq * p.nqb;
-  if (p.nkb <= 1024) {
-    dim3 grid((rows / p.B + kWarpsPerCta - 1) / kWarpsPerCta, p.B);
-    if (p.nkb <= 256)
-      select_warp_kernel<RB, 8><<<grid, 32 * kWarpsPerCta, 0, st>>>(
-          lse_part, p.Hq, p.nqb, p.nkb, R, p.q_start_pos / kBlock, threshold, mask, block_sums);
-    else
-      select_warp_kernel<RB, 32><<<grid, 32 * kWarpsPerCta, 0, st>>>(
-          lse_part, p.Hq, p.nqb, p.nkb, R, p.q_start_pos / kBlock, threshold, mask, block_sums);
-    return cudaGetLastError();
-  }
+  if (p.nkb <= 256) return launch_cta<RB, 1>(p, threshold, lse_part, mask, block_sums, st);
+  if (p.nkb <= 512) return launch_cta<RB, 2>(p, threshold, lse_part, mask, block_sums, st);
+  if (p.nkb <= 1024) return launch_cta<RB, 4>(p, threshold, lse_part, mask, block_sums, st);
   int n_pad = 1;
   while (n_pad < p.nkb) n_pad <<= 1;
   const size_t smem = (size_t)n_pad * 8 + (size_t)p.nkb * 4 + (size_t)p.nkb + 16;
