@@ -79,7 +79,7 @@ __global__ void __launch_bounds__(kEstThreads) estimate_simt_kernel(
       float l = 0.f;
 #pragma unroll
       for (int j = 0; j < RB; ++j) l += expf(x[j] - m);
-      lse_part[(((long long)b * Hq + h) * nkb + kb) * R + qb * RB + i] = m + logf(l);
+      lse_part[((((long long)b * Hq + h) * (R / RB) + qb) * nkb + kb) * RB + i] = m + logf(l);
     }
   }
 }

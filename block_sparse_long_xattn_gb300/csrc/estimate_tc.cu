@@ -16,7 +16,8 @@
 // the causal rule J <= I (global reshaped indices, the chunk starting at row
 // q_start_pos/S; xattn_bsa.py select_blocks Step 0), and for every key block
 // (128/S consecutive keys) at or before the row's diagonal write
-//   lse_part[b][h][kb][i] = ln sum_{J in kb, J <= I} exp(s[I,J] / (sqrt(d) S)).
+//   lse_part[b][h][qb][kb][r] = ln sum_{J in kb, J <= I} exp(s[I,J] / (sqrt(d) S))
+// for row I = q_start_pos/S + qb * (128/S) + r.
 // The selection kernel turns these into the softmax block sums.
 //
 // Persistent CTAs (one per SM) walk tiles (b, h, row tile, key tile) in
@@ -229,7 +230,11 @@ __global__ void __launch_bounds__(kThreads, 1) estimate_tc_kernel(
       const int i = rt * kM + row;              // reshaped row within the chunk
       const int Ig = T.p_s + i;                 // global reshaped row
       const bool valid = i < T.R;
-      float* out = lse_part + ((long long)(b * T.Hq + h) * nkb) * T.R + i;
+      // lse_part[b][h][qb][kb][r] for row i = qb * RB + r: the RB rows of a
+      // query block are contiguous per key block, and a query block's rows
+      // for all key blocks form one contiguous run that selection reads
+      float* out = lse_part +
+                   ((long long)(b * T.Hq + h) * (T.R / RB) + i / RB) * nkb * RB + (i % RB);
 #pragma unroll 1
       for (int cc = 0; cc < kN / 32; ++cc) {
         float v[32];
@@ -249,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1) estimate_tc_kernel(
             float sum = 0.f;
 #pragma unroll
             for (int e = 0; e < RB; ++e) sum += fast_exp2(v[g * RB + e] - m);
-            out[(long long)(Jg / RB) * T.R] = (m + __log2f(sum)) * 0.69314718055994531f;
+            out[Jg] = (m + __log2f(sum)) * 0.69314718055994531f;  // (Jg / RB) * RB
           }
         }
       }

@@ -1,7 +1,9 @@
 // a2-a4: row normalisation, block sums and threshold block selection.
 //
-// Input: lse_part[b][h][kb][I] = ln sum_{J in kb, J <= I} exp(s[I,J] / (sqrt(d) S))
-// for the reshaped query rows I of the chunk (written by the estimate kernels).
+// Input: lse_part[b][h][qb][kb][r] = ln sum_{J in kb, J <= I} exp(s[I,J] / (sqrt(d) S))
+// for the reshaped query rows I = q_start_pos/S + qb * 128/S + r of the chunk
+// (written by the estimate kernels): one query block's partials are one
+// contiguous run of nkb * 128/S floats.
 // Then for one query block qb with rows I in qb:
 //   LSE_I   = ln sum_kb exp(lse_part[kb][I])                 (row softmax denominator)
 //   A[kb]   = sum_{I in qb} exp(lse_part[kb][I] - LSE_I)      (block sum of probabilities)
@@ -43,7 +45,7 @@ __device__ __forceinline__ float block_reduce_sum(float v, float* red) {
 
 template <int RB>  // reshaped rows per 128-token block, 128 / stride
 __global__ void __launch_bounds__(kSelThreads) select_kernel(
-    const float* __restrict__ lse_part, int Hq, int nkb, int R, int cur,
+    const float* __restrict__ lse_part, int Hq, int nkb, int cur,
     float threshold, uint8_t* __restrict__ mask, float* __restrict__ block_sums,
     int n_pad) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -60,14 +62,14 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int diag = cur + qb;
   const int ncausal = diag + 1;
-  const float* base = lse_part + ((long long)(b * Hq + h) * nkb) * R + qb * RB;
+  const float* base = lse_part + ((long long)(b * Hq + h) * gridDim.x + qb) * nkb * RB;
 
   // ---- row maxima over key blocks ----
   float acc[RB];
 #pragma unroll
   for (int i = 0; i < RB; ++i) acc[i] = -INFINITY;
   for (int kb = tid; kb < ncausal; kb += kSelThreads) {
-    const float4* p = reinterpret_cast<const float4*>(base + (long long)kb * R);
+    const float4* p = reinterpret_cast<const float4*>(base + (long long)kb * RB);
 #pragma unroll
     for (int c = 0; c < RB / 4; ++c) {
       const float4 v = __ldg(p + c);
@@ -97,7 +99,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
 #pragma unroll
   for (int i = 0; i < RB; ++i) acc[i] = 0.f;
   for (int kb = tid; kb < ncausal; kb += kSelThreads) {
-    const float4* p = reinterpret_cast<const float4*>(base + (long long)kb * R);
+    const float4* p = reinterpret_cast<const float4*>(base + (long long)kb * RB);
 #pragma unroll
     for (int c = 0; c < RB / 4; ++c) {
       const float4 v = __ldg(p + c);
@@ -129,7 +131,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
   for (int kb = tid; kb < nkb; kb += kSelThreads) {
     float a = 0.f;
     if (kb < ncausal) {
-      const float4* p = reinterpret_cast<const float4*>(base + (long long)kb * R);
+      const float4* p = reinterpret_cast<const float4*>(base + (long long)kb * RB);
 #pragma unroll
       for (int c = 0; c < RB / 4; ++c) {
         const float4 v = __ldg(p + c);
@@ -248,7 +250,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
 //     plus the forced mass is below threshold * T is selected.
 template <int RB, int E>
 __global__ void __launch_bounds__(kSelThreads) select_cta_kernel(
-    const float* __restrict__ lse_part, int Hq, int nqb, int nkb, int R, int cur,
+    const float* __restrict__ lse_part, int Hq, int nqb, int nkb, int cur,
     float threshold, uint8_t* __restrict__ mask, float* __restrict__ block_sums) {
   constexpr int NT = kSelThreads;
   constexpr int N = NT * E;                  // padded row length (a power of two)
@@ -268,14 +270,14 @@ __global__ void __launch_bounds__(kSelThreads) select_cta_kernel(
   const int qb = blockIdx.x % nqb, h = blockIdx.x / nqb, b = blockIdx.y;
   const int diag = cur + qb;
   const int ncausal = diag + 1;
-  const float* base = lse_part + ((long long)(b * Hq + h) * nkb) * R + qb * RB;
+  const float* base = lse_part + ((long long)(b * Hq + h) * nqb + qb) * nkb * RB;
 
   // ---- 1. partials, transposed into shared memory ----
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     const int kb = e * NT + tid;
     float4 v[RB / 4];
-    const float4* src = reinterpret_cast<const float4*>(base + (long long)kb * R);
+    const float4* src = reinterpret_cast<const float4*>(base + (long long)kb * RB);
 #pragma unroll
     for (int c = 0; c < RB / 4; ++c)
       v[c] = kb < ncausal ? __ldg(src + c) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
@@ -444,17 +446,15 @@ cudaError_t launch_cta(const Problem& p, float threshold, const float* lse_part,
   cudaError_t e = cudaFuncSetAttribute(select_cta_kernel<RB, E>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const int R = p.q_len / (kBlock / RB);
   dim3 grid(p.Hq * p.nqb, p.B);
   select_cta_kernel<RB, E><<<grid, kSelThreads, smem, st>>>(
-      lse_part, p.Hq, p.nqb, p.nkb, R, p.q_start_pos / kBlock, threshold, mask, block_sums);
+      lse_part, p.Hq, p.nqb, p.nkb, p.q_start_pos / kBlock, threshold, mask, block_sums);
   return cudaGetLastError();
 }
 
 template <int RB>
 cudaError_t launch_rb(const Problem& p, float threshold, const float* lse_part,
                       uint8_t* mask, float* block_sums, cudaStream_t st) {
-  const int R = p.q_len / (kBlock / RB);
   if (p.nkb <= 256) return launch_cta<RB, 1>(p, threshold, lse_part, mask, block_sums, st);
   if (p.nkb <= 512) return launch_cta<RB, 2>(p, threshold, lse_part, mask, block_sums, st);
   if (p.nkb <= 1024) return launch_cta<RB, 4>(p, threshold, lse_part, mask, block_sums, st);
@@ -467,7 +467,7 @@ cudaError_t launch_rb(const Problem& p, float threshold, const float* lse_part,
   if (e != cudaSuccess) return e;
   dim3 grid(p.nqb, p.Hq, p.B);
   select_kernel<RB><<<grid, kSelThreads, smem, st>>>(
-      lse_part, p.Hq, p.nkb, R, p.q_start_pos / kBlock, threshold, mask,
+      lse_part, p.Hq, p.nkb, p.q_start_pos / kBlock, threshold, mask,
       block_sums, n_pad);
   return cudaGetLastError();
 }

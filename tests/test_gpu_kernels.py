@@ -104,6 +104,55 @@ def test_bsa_prefill(case, cols):
     assert np.all(o_g[np.transpose(~fin, (0, 2, 1))] == 0.0)
 
 
+def _pairing_mask(P, Lq, Hq, seed):
+    """Rows of mixed lengths next to each other: head 0 has one long row (more
+    than 128 selected blocks: many laps of the K/V ring) between two short
+    ones; head 1 short rows that start at different blocks; head 2 long rows;
+    head 3 short rows and one row holding only its diagonal block (an empty
+    history part).  The tile count is odd."""
+    rng = np.random.default_rng(seed)
+    nqb, cur = Lq // 128, P // 128
+    nkb = cur + nqb
+    m = np.zeros((1, Hq, nqb, nkb), np.uint8)
+    for h in range(Hq):
+        for qb in range(nqb):
+            diag = cur + qb
+            if h == 2 or (h == 0 and qb == 1):
+                m[0, h, qb, :diag + 1] = rng.random(diag + 1) < 0.95
+            else:
+                lo = {1: 3 + 7 * (qb & 1), 3: 10 - 7 * (qb & 1)}.get(h, 0)
+                k = 2 if (h == 3 and qb == 2) else 30
+                m[0, h, qb, lo + rng.choice(diag - lo, size=k, replace=False)] = 1
+            m[0, h, qb, diag] = 1
+    if Hq > 3:
+        m[0, 3, 2, :cur + 2] = 0                  # only the diagonal block
+    return m
+
+
+def test_bsa_mixed_row_lengths():
+    P, Lq, Hq = 20480, 384, 4
+    Lk = P + Lq
+    nkb, cur = Lk // 128, P // 128
+    w = make_workload(seed=61, B=1, Hq=Hq, Hkv=2, d=128, Lk=Lk, q_start_pos=P,
+                      alpha=2.0, n_hot=8, dtype="bf16")
+    m = _pairing_mask(P, Lq, Hq, 5)
+    assert (m.sum(axis=-1) > 128).any() and (m.sum(axis=-1) <= 128).any()
+    q, k, v = (to_dev(x, "bf16") for x in (w.q, w.k, w.v))
+    mask = torch.from_numpy(m).cuda()
+    oh, lh, oc, lc = bsx_bsa_prefill_split(q, k, v, mask, P)
+    oa, la = bsx_bsa_prefill(q, k, v, mask, P)
+    torch.cuda.synchronize()
+    for (o, lse), (kb0, kb1) in (((oh, lh), (0, cur)), ((oc, lc), (cur, nkb)),
+                                 ((oa, la), (0, nkb))):
+        o_ref, lse_ref = O.bsa_prefill(w.q, w.k, w.v, m, P, kb0, kb1)
+        o_g, lse_g = o.float().cpu().numpy(), lse.cpu().numpy()
+        fin = np.isfinite(lse_ref)
+        assert np.array_equal(np.isfinite(lse_g), fin)
+        assert np.abs(o_g - o_ref).max() <= O_TOL["bf16"]
+        assert np.abs(lse_g[fin] - lse_ref[fin]).max() <= LSE_TOL
+    assert bsx_last_error() == 0
+
+
 @pytest.mark.parametrize("dt", ["bf16", "f32"])
 @pytest.mark.parametrize("d", [64, 128])
 def test_merge(dt, d):
