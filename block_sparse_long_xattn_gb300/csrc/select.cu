@@ -237,8 +237,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
 //     (128/S consecutive floats each, all loads in flight at once) and
 //     stores them transposed, vals[i][kb], in shared memory;
 //  2. each reshaped row i is reduced by 256/RB threads (a max, then a sum of
-//     exponentials, each followed by a shuffle reduction inside the group):
-//     row_lse[i];
+//     exponentials written back over the partials, each followed by a
+//     shuffle reduction inside the group): row_inv[i] = 1 / sum;
 //  3. each thread sums its key blocks' probabilities over the rows: A[kb];
 //     one block reduction gives the row total T;
 //  4. a bitonic sort of packed (A, ~kb) 64-bit keys, descending, position
@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(kSelThreads) select_cta_kernel(
   float* vals = reinterpret_cast<float*>(smem_raw);                              // [RB][LD]
   unsigned long long* kbuf = reinterpret_cast<unsigned long long*>(vals + RB * LD);  // [2][N]
   uint8_t* sel = reinterpret_cast<uint8_t*>(kbuf + 2 * N);                       // [N]
-  __shared__ float row_lse[RB];
+  __shared__ float row_inv[RB];
   __shared__ float red[NW];
   __shared__ float forced[2];
 
@@ -292,10 +292,11 @@ __global__ void __launch_bounds__(kSelThreads) select_cta_kernel(
   }
   __syncthreads();
 
-  // ---- 2. row LSE: GR threads per row ----
+  // ---- 2. row softmax: GR threads per row; each exponential exp(x - m) is
+  // written back over its partial, and the row keeps 1 / sum ----
   {
     const int i = tid / GR, j = tid % GR;
-    const float* rowp = vals + i * LD;
+    float* rowp = vals + i * LD;
     float m = -INFINITY;
 #pragma unroll
     for (int c = j; c < N; c += GR) m = fmaxf(m, rowp[c]);
@@ -303,14 +304,18 @@ __global__ void __launch_bounds__(kSelThreads) select_cta_kernel(
     for (int o = GR / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     float sum = 0.f;
 #pragma unroll
-    for (int c = j; c < N; c += GR) sum += __expf(rowp[c] - m);
+    for (int c = j; c < N; c += GR) {
+      const float e = __expf(rowp[c] - m);
+      rowp[c] = e;
+      sum += e;
+    }
 #pragma unroll
     for (int o = GR / 2; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (j == 0) row_lse[i] = m + logf(sum);
+    if (j == 0) row_inv[i] = 1.f / sum;
   }
   __syncthreads();
 
-  // ---- 3. block sums A[kb] and the row total ----
+  // ---- 3. block sums A[kb] = sum_i exp(x - m_i) / sum_i, and the row total ----
   float a[E];
   float part = 0.f;
 #pragma unroll
@@ -319,7 +324,7 @@ __global__ void __launch_bounds__(kSelThreads) select_cta_kernel(
     float x = 0.f;
     if (kb < ncausal) {
 #pragma unroll
-      for (int i = 0; i < RB; ++i) x += __expf(vals[i * LD + kb] - row_lse[i]);
+      for (int i = 0; i < RB; ++i) x = fmaf(vals[i * LD + kb], row_inv[i], x);
     }
     a[e] = x;
     part += x;
