@@ -76,3 +76,45 @@ def test_estimate_flops_counts_the_causal_reshaped_pairs():
         pairs = sum(1 for I in range(P // S, (P + q_len) // S) for J in range((P + q_len) // S)
                     if J <= I)
         assert bench.estimate_flops(cfg, q_len, P, S) == 2.0 * 64 * S * pairs * 3 * 2
+
+
+def test_mask_rows_vs_oracle_counts_near_and_differing_rows():
+    """The bench's parity record for the oracle's sampled heads: rows whose
+    margin is within 1e-4 count as near the threshold (exempt), any other
+    row that differs from the oracle's mask is counted as differing."""
+    from types import SimpleNamespace
+    import numpy as np
+    B, Hq, nqb, nkb = 1, 8, 3, 5
+    gpu = np.zeros((B, Hq, nqb, nkb), np.uint8)
+    ests, heads = [], [0, 4]
+    for h in heads:
+        m = np.zeros((B, 1, nqb, nkb), bool)
+        m[0, 0, :, 0] = True
+        margin = np.full((B, 1, nqb), 0.5)
+        ests.append(SimpleNamespace(mask=m, margin=margin))
+        gpu[0, h, :, 0] = 1
+    # head 0, row 1: differs but is near the threshold; head 4, row 2: differs
+    ests[0].margin[0, 0, 1] = 5e-5
+    gpu[0, 0, 1, 3] = 1
+    gpu[0, 4, 2, 2] = 1
+    r = bench.mask_rows_vs_oracle(gpu, ests, heads)
+    assert r["rows"] == 2 * nqb
+    assert r["near_threshold"] == 1
+    assert r["other_rows_differing"] == 1
+
+
+def test_both_arms_print_the_same_config():
+    """The GPU arm and the reference arm describe the workload with one dict,
+    so a driver comparing the two lines sees the same configuration."""
+    from types import SimpleNamespace
+    for wl, step in (("llama8b-32k-chunk4096", "chunk"), ("llama8b-64k-chunked", "chunked"),
+                     ("llama8b-128k-rho10", "chunk")):
+        args = SimpleNamespace(workload=wl, step=step, seed=0, estimator="bf16")
+        c = bench.config_dict(args, 1)
+        assert c["workload"] == wl and c["parallelism"] == "replicas1"
+        cfg = bench.CONFIGS[wl]
+        assert c["stride"] == cfg["stride"] and c["threshold"] == cfg["threshold"]
+        if step == "chunked":
+            assert c["seq_len"] == cfg["Lk"] and c["chunks"] == cfg["Lk"] // cfg["chunk"]
+        else:
+            assert c["q_len"] + c["q_start_pos"] == c["Lk"] == cfg["Lk"]
