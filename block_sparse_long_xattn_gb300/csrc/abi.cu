@@ -4,6 +4,8 @@
 #include <math.h>
 #include <stdio.h>
 
+#include <atomic>
+
 #include "../../include/bsxattn.h"
 #include "common.cuh"
 #include "launchers.h"
@@ -15,19 +17,23 @@ namespace {
 __device__ unsigned g_bsx_err_word = 0;
 
 constexpr int kMaxDevices = 64;
-unsigned* g_err_ptr[kMaxDevices] = {nullptr};
+std::atomic<unsigned*> g_err_ptr[kMaxDevices];
 
 // Device address of the error word for the current device (looked up once
-// per device; host code cannot use the symbol itself as an address).
+// per device; host code cannot use the symbol itself as an address).  The
+// cached address belongs to the device's primary context (the runtime API's
+// context) and does not survive cudaDeviceReset.
 unsigned* err_word() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  if (!g_err_ptr[dev]) {
+  unsigned* w = g_err_ptr[dev].load(std::memory_order_acquire);
+  if (!w) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_bsx_err_word) != cudaSuccess) return nullptr;
-    g_err_ptr[dev] = static_cast<unsigned*>(p);
+    w = static_cast<unsigned*>(p);
+    g_err_ptr[dev].store(w, std::memory_order_release);
   }
-  return g_err_ptr[dev];
+  return w;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
