@@ -278,8 +278,19 @@ def run_gpu(args):
     if args.step == "chunk":
         phases = [("estimate", est), ("bsa_split", bsa_split(mask)), ("merge_map", merge_map)]
         launches = 5
+    elif args.step in ("fused", "prefill") and not e4m3:
+        # bsx_chunk_prefill: one launch (estimate, selection and attention in
+        # one kernel where it applies; else the three launches it falls back to)
+        wsf = torch.empty(bsx.bsx_chunk_prefill_workspace_bytes(bsx.shape_of(dq, dk), Lq, P, S),
+                          dtype=torch.uint8, device=dev)
+
+        def fused_step(q, k, v):
+            bsx.bsx_chunk_prefill(q, k, v, P, S, tau, mask=mask, o=oh, lse=lh, workspace=wsf,
+                                  stream=stream)
+        phases = [("fused_step", fused_step)]
+        launches = 1 if (w.dtype == "bf16" and nkb <= 1024) else 3
     elif args.step in ("fused", "prefill"):
-        # the launches bsx_chunk_prefill enqueues, timed one by one
+        # e4m3 estimator operands: the estimate and one attention launch
         phases = [("estimate", est), ("bsa_all", bsa(mask, 0, nkb, oh, lh))]
         launches = 3
     elif args.step == "offload":
@@ -307,9 +318,15 @@ def run_gpu(args):
     bsa_mask = (omask if args.step == "offload" else mask).cpu().numpy()
     causal_blocks = sum(cur + qb + 1 for qb in range(Lq // 128)) * B * Hq
     density = float(mask.cpu().numpy().astype(bool).sum()) / causal_blocks
-    ranges = {"bsa_split": ((0, cur), (cur, nkb)), "bsa_all": ((0, nkb),)}
+    if e4m3:
+        launches += 2   # the two quantize launches of each step
+    ranges = {"bsa_split": ((0, cur), (cur, nkb)), "bsa_all": ((0, nkb),),
+              "fused_step": ((0, nkb),)}
     flops = {n: sum(bsa_flops(bsa_mask, P, r0, r1, d) for r0, r1 in ranges[n])
              for n, _ in phases if n in ranges}
+    est_fl = estimate_flops(cfg, Lq, P, S)
+    if "fused_step" in flops:   # one kernel: the estimate's MMAs and the attention's
+        flops["fused_step"] += est_fl
 
     np_ = len(phases)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(np_ + 1)]
@@ -396,17 +413,17 @@ def run_gpu(args):
     achieved = bsa_flops_launch / (bsa_ms / 1e3) / 1e12
     traffic = _traffic_per_launch("bsa_prefill") if args.step == "chunk" and \
         args.workload == DEFAULT_WORKLOAD else None
-    est_fl = estimate_flops(cfg, Lq, P, S)
     est_bytes = (dq.numel() + dk.numel()) * dq.element_size() + mask.numel()
-    est_ms = t_phase["estimate"]
 
     kernels = {f"{n}_ms": t for n, t in t_phase.items()}
-    kernels.update({
-        "estimate_tflops": est_fl / (est_ms / 1e3) / 1e12,
-        "estimate_tc_frac": est_fl / (est_ms / 1e3) / 1e12 / tc_peak,
-        "estimate_gbs": est_bytes / (est_ms / 1e3) / 1e9,
-        "estimate_hbm_frac": est_bytes / (est_ms / 1e3) / 1e9 / hbm_peak,
-    })
+    if "estimate" in t_phase:
+        est_ms = t_phase["estimate"]
+        kernels.update({
+            "estimate_tflops": est_fl / (est_ms / 1e3) / 1e12,
+            "estimate_tc_frac": est_fl / (est_ms / 1e3) / 1e12 / tc_peak,
+            "estimate_gbs": est_bytes / (est_ms / 1e3) / 1e9,
+            "estimate_hbm_frac": est_bytes / (est_ms / 1e3) / 1e9 / hbm_peak,
+        })
     for n in bsa_names:
         kernels[f"{n}_tflops"] = flops[n] / (t_phase[n] / 1e3) / 1e12
 
@@ -415,7 +432,9 @@ def run_gpu(args):
     # and map at the copy bandwidth), summed; tokens/s at that time against
     # the measured tokens/s
     merge_bytes = 3 * oh.numel() * oh.element_size() + 3 * lh.numel() * 4
-    roof_ms = {"estimate": max(est_fl / (tc_peak * 1e12), est_bytes / (hbm_peak * 1e9)) * 1e3}
+    roof_ms = {}
+    if "estimate" in t_phase:
+        roof_ms["estimate"] = max(est_fl / (tc_peak * 1e12), est_bytes / (hbm_peak * 1e9)) * 1e3
     for n in bsa_names:
         roof_ms[n] = flops[n] / (tc_peak * 1e12) * 1e3
     if "merge_map" in t_phase or "merge" in t_phase:
@@ -435,7 +454,8 @@ def run_gpu(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic (seeded planted-direction N(0,1) inputs)",
         "config": config_dict(args, world),
-        "roofline": {"kernel": DOMINANT, "bound": "tensor", "achieved": achieved,
+        "roofline": {"kernel": "fused_step" if "fused_step" in t_phase else DOMINANT,
+                     "bound": "tensor", "achieved": achieved,
                      "peak": tc_peak, "unit": "TFLOP/s", "frac": achieved / tc_peak,
                      "traffic": traffic, "peak_source": peak_src,
                      # the same launch against the cuBLAS figure sustained under
@@ -946,8 +966,8 @@ def main():
     ap.add_argument("--step", default="chunk",
                     choices=["chunk", "fused", "offload", "prefill", "chunked"],
                     help="chunk: estimate, BSA on history and current chunk, merge, map "
-                         "(the default); fused: estimate + one BSA launch over all key "
-                         "blocks; offload: the pages' CPU-block-dense history; prefill: "
+                         "(the default); fused: bsx_chunk_prefill, estimate, selection "
+                         "and attention over all key blocks in one kernel; offload: the pages' CPU-block-dense history; prefill: "
                          "fused on a whole-sequence workload; chunked: the chunk step on "
                          "every chunk of a whole sequence in order (64K in 16 chunks)")
     ap.add_argument("--estimator", default="bf16", choices=["bf16", "e4m3"],

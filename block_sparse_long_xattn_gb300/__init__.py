@@ -18,9 +18,11 @@ from ._lib import (  # noqa: F401
     bsx_bsa_prefill,
     bsx_bsa_prefill_split,
     bsx_chunk_prefill,
+    bsx_chunk_prefill_workspace_bytes,
     bsx_chunk_step_host,
     bsx_cpu_block_mask,
     bsx_debug_drop_ring_item,
+    bsx_debug_fused_skip_row,
     bsx_estimate_workspace_bytes,
     bsx_last_error,
     bsx_map_mask_to_cpu_blocks,

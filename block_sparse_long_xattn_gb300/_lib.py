@@ -27,7 +27,8 @@ EXPORTS = ("bsx_version", "bsx_status_string", "bsx_estimate_workspace_bytes",
            "bsx_map_mask_to_cpu_blocks", "bsx_last_error", "bsx_last_error_code",
            "bsx_xattn_estimate_noalloc",
            "bsx_cpu_block_mask", "bsx_chunk_prefill", "bsx_bsa_prefill_split",
-           "bsx_quantize_e4m3", "bsx_chunk_step_host", "bsx_debug_drop_ring_item")
+           "bsx_quantize_e4m3", "bsx_chunk_step_host", "bsx_debug_drop_ring_item",
+           "bsx_chunk_prefill_workspace_bytes", "bsx_debug_fused_skip_row")
 BSX_STEP_OFFLOAD, BSX_STEP_E4M3_ESTIMATE, BSX_STEP_FUSED = 2, 4, 8
 
 
@@ -89,6 +90,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.bsx_merge_attn.argtypes = [BsxShape, i32, vp, vp, vp, vp, vp]
         lib.bsx_map_mask_to_cpu_blocks.restype = i32
         lib.bsx_map_mask_to_cpu_blocks.argtypes = [BsxShape, vp, i32, i32, i32, i32, vp, vp]
+        lib.bsx_chunk_prefill_workspace_bytes.restype = sz
+        lib.bsx_chunk_prefill_workspace_bytes.argtypes = [BsxShape, i32, i32, i32]
         lib.bsx_chunk_prefill.restype = i32
         lib.bsx_chunk_prefill.argtypes = [BsxShape, vp, vp, vp, i32, i32, i32, f32, vp, vp,
                                           vp, vp, sz, vp]
@@ -98,6 +101,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.bsx_last_error.argtypes = [vp]
         lib.bsx_last_error_code.restype = ctypes.c_uint
         lib.bsx_last_error_code.argtypes = []
+        lib.bsx_debug_fused_skip_row.restype = i32
+        lib.bsx_debug_fused_skip_row.argtypes = [i32]
         lib.bsx_debug_drop_ring_item.restype = i32
         lib.bsx_debug_drop_ring_item.argtypes = [i32, i32]
         lib.bsx_chunk_step_host.restype = i32
@@ -261,7 +266,7 @@ def bsx_chunk_prefill(q, k, v, q_start_pos: int, stride: int, threshold: float, 
         o = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, Hq, q_len), dtype=torch.float32, device=q.device)
-    need = lib.bsx_estimate_workspace_bytes(shape, q_len, q_start_pos, stride)
+    need = lib.bsx_chunk_prefill_workspace_bytes(shape, q_len, q_start_pos, stride)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     _check("bsx_chunk_prefill", lib.bsx_chunk_prefill(
@@ -319,6 +324,19 @@ def bsx_debug_drop_ring_item(cta: int, item: int) -> None:
     _check("bsx_debug_drop_ring_item", load().bsx_debug_drop_ring_item(cta, item))
 
 
+def bsx_debug_fused_skip_row(row: int) -> None:
+    """Failure-path test hook: the calling thread's next fused chunk step never
+    marks selection row `row` ready, so that row's attention CTA's bounded
+    wait runs out and the error word records it (see bsxattn.h)."""
+    _check("bsx_debug_fused_skip_row", load().bsx_debug_fused_skip_row(row))
+
+
+def bsx_chunk_prefill_workspace_bytes(shape: BsxShape, q_len: int, q_start_pos: int,
+                                      stride: int) -> int:
+    """Device workspace bytes of bsx_chunk_prefill (0 for invalid arguments)."""
+    return int(load().bsx_chunk_prefill_workspace_bytes(shape, q_len, q_start_pos, stride))
+
+
 def bsx_last_error(stream=None) -> int:
     """Wait for `stream` (default: torch's current stream), read and clear the
     device error word; returns the raw word (0 = none)."""
@@ -341,8 +359,11 @@ def make_chunk_buffers(q_host, k_host, q_start_pos: int, stride: int,
     dt = q_host.dtype
     u8 = torch.uint8
     n_cpu = q_start_pos // cpu_block_tokens
-    need = load().bsx_estimate_workspace_bytes(BsxShape(B, Hq, Hkv, d, _dtype_code(q_host)),
-                                               q_len, q_start_pos, stride)
+    shape = BsxShape(B, Hq, Hkv, d, _dtype_code(q_host))
+    need = load().bsx_estimate_workspace_bytes(shape, q_len, q_start_pos, stride)
+    if fused:  # the step may run as one fused kernel: room for its control block
+        need = max(need, load().bsx_chunk_prefill_workspace_bytes(shape, q_len, q_start_pos,
+                                                                  stride))
     mshape = (B, Hq, q_len // 128, Lk // 128)
     return {
         "q": torch.empty(q_host.shape, dtype=dt, device=device),

@@ -83,6 +83,12 @@ thread_local bsx::BsaDrop t_drop;
 // The raw error word the calling thread's last bsx_last_error read.
 thread_local unsigned t_last_word = 0;
 
+// Failure-path test hook of the fused chunk step (bsx_debug_fused_skip_row):
+// armed per host thread, consumed by its next fused step.
+thread_local int t_skip_row = -1;
+
+size_t round_up_256(size_t n) { return (n + 255) / 256 * 256; }
+
 bsx::BsaDrop take_drop() {
   const bsx::BsaDrop d = t_drop;
   t_drop = bsx::BsaDrop();
@@ -218,6 +224,15 @@ int bsx_map_mask_to_cpu_blocks(bsx_shape s, const uint8_t* mask, int q_len,
                                      static_cast<cudaStream_t>(stream)));
 }
 
+size_t bsx_chunk_prefill_workspace_bytes(bsx_shape s, int q_len, int q_start_pos,
+                                         int stride) {
+  const size_t est = bsx_estimate_workspace_bytes(s, q_len, q_start_pos, stride);
+  if (est == 0) return 0;
+  bsx::Problem p;
+  if (make_problem(s, q_len, q_start_pos, &p, true) != BSX_OK) return 0;
+  return round_up_256(est) + bsx::fused_ctl_bytes(p, stride);
+}
+
 int bsx_chunk_prefill(bsx_shape s, const void* q, const void* k, const void* v, int q_len,
                       int q_start_pos, int stride, float threshold, uint8_t* mask, void* o,
                       float* lse, void* workspace, size_t workspace_bytes, void* stream) {
@@ -225,9 +240,26 @@ int bsx_chunk_prefill(bsx_shape s, const void* q, const void* k, const void* v, 
   bsx::Problem p;
   int rc = make_problem(s, q_len, q_start_pos, &p);
   if (rc != BSX_OK) return rc;
-  if (!v || !o || !lse || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+  if (stride != 4 && stride != 8 && stride != 16) return BSX_ERR_UNSUPPORTED;
+  if (!(threshold > 0.0f) || isnan(threshold)) return BSX_ERR_INVALID_ARG;
+  if (!q || !k || !v || !mask || !o || !lse) return BSX_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return BSX_ERR_INVALID_ARG;
   if (p.nkb > kMaxKeyBlocks) return BSX_ERR_UNSUPPORTED;
+  const size_t need = bsx_chunk_prefill_workspace_bytes(s, q_len, q_start_pos, stride);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return BSX_ERR_WORKSPACE;
+  if (bsx::fused_step_supported(p, stride)) {
+    // one kernel: estimate, selection and attention (the control block after
+    // the partials)
+    const size_t off = round_up_256(bsx_estimate_workspace_bytes(s, q_len, q_start_pos, stride));
+    unsigned* ctl = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + off);
+    const int skip = t_skip_row;
+    t_skip_row = -1;
+    return cuda_status(bsx::launch_fused_step(p, q, k, v, stride, threshold,
+                                              static_cast<float*>(workspace), ctl, need - off,
+                                              mask, o, lse, err_word(), skip,
+                                              static_cast<cudaStream_t>(stream)));
+  }
   rc = bsx_xattn_estimate(s, q, k, q_len, q_start_pos, stride, threshold, mask, nullptr,
                           workspace, workspace_bytes, stream);
   if (rc != BSX_OK) return rc;
@@ -250,6 +282,11 @@ int bsx_debug_drop_ring_item(int cta, int item) {
   if (cta >= 0 && item < 0) return BSX_ERR_INVALID_ARG;
   t_drop.cta = cta < 0 ? -1 : cta;
   t_drop.item = cta < 0 ? -1 : item;
+  return BSX_OK;
+}
+
+int bsx_debug_fused_skip_row(int row) {
+  t_skip_row = row < 0 ? -1 : row;
   return BSX_OK;
 }
 

@@ -1,69 +1,14 @@
-// a5 on tcgen05 tensor cores: block-sparse causal attention with LSE (bf16).
-//
-// docs/xattention_algorithm_guide.md "BSA (Block Sparse Attention)": causal
-// FlashAttention restricted to the selected 128x128 tiles of a per-head block
-// mask (block size fixed at 128); xattn_bsa.py compute_chunked_prefill takes O
-// and LSE from the history part and the current-chunk part and merges them.
-//
-// One CTA per (128-row q-tile, q-head, batch); 10 warps with fixed roles:
-//   warp 0      TMA producer: Q and the first selected K tile (both copied
-//               before the block count), then the K and V tiles of every selected
-//               key block, found by scanning the mask row, into a ring of
-//               tile-sized slots in the order the MMAs consume them (K_0, K_1,
-//               V_0, K_2, V_1, ...).  A K slot is freed as soon as its S MMA
-//               completes and a V slot after its P V MMA.
-//   warp 1      tcgen05 issuer (one elected lane): S(j) = Q K_j^T into TMEM
-//               buffer j % 2, and O_{j%2} += P(j) V_j with P(j) read from that
-//               same buffer.
-//   warps 2..9  two softmax groups of four warps; group g takes the blocks
-//               j = g, g + 2, ... with one query row per thread (TMEM lane =
-//               row): read S, mask the diagonal block causally, P =
-//               exp2(x - m) as bf16 pairs written back over the consumed S
-//               columns, row sums; the running max m is raised (and O_g
-//               rescaled) only on a group's first block and when a block's
-//               row sum would exceed 2^32.  At the end the two partial
-//               results (O_g, m_g, l_g) are merged per row; LSE goes to
-//               global memory directly, O through the finished Q buffer and
-//               one TMA store per 64-feature region.
-// Each group's chain S(j) -> softmax -> P V(j) -> S(j + 2) interleaves with
-// the other group's on the tensor pipe, and no per-block exchange between
-// warps is needed.  TMEM: S/P buffers in columns 0-255, O_0 and O_1 after.
-// Every wait is bounded (2 s of wall time); on expiry the CTA records the wait
-// in the device error word, drains its in-flight copies and MMAs, frees TMEM
-// and exits.
+// a5 on tcgen05 tensor cores: block-sparse causal attention with LSE (bf16),
+// one or two key-block ranges of the same queries in one launch.  The method
+// and the CTA's structure are described in bsa_tc.cuh.
+#include "bsa_tc.cuh"
 #include "launchers.h"
-#include "tc_common.cuh"
 
 namespace bsx {
 namespace {
 
 using namespace tc;
-
-constexpr int kThreads = 320;   // producer, MMA issuer, 8 softmax warps
-constexpr int kRegion = 128 * 128;  // bytes of one 128-row x 64-feature bf16 tile
-// Largest row sum of one block's P accepted without raising the running max
-// first (2^32: P and the fp32 sums stay far from overflow).
-constexpr float kMaxBlockSum = 4294967296.0f;
-
-enum Site : unsigned {
-  kSiteKvEmpty = 1, kSiteQFull, kSiteKvFull, kSitePFull, kSiteSFull, kSiteODoneFinal,
-  kSiteXchg, kSiteStage
-};
-
-template <int D>
-struct Layout {
-  static constexpr int kRegions = D / 64;
-  static constexpr int kTile = kRegions * kRegion;        // Q, K or V tile bytes
-  static constexpr int kSlots = D == 128 ? 5 : 8;         // K/V ring slots of kTile bytes
-  static constexpr int kQ = 0;
-  static constexpr int kRing = kQ + kTile;
-  static constexpr int kBars = kRing + kSlots * kTile;    // mbarriers (8 B each)
-  static constexpr int kNumBars = 32;
-  static constexpr int kMisc = kBars + 8 * kNumBars;      // tmem slot, n, flags
-  static constexpr int kXchg = kMisc + 64;                // [2 groups][m, l][128 rows] fp32
-  static constexpr int kBytes = kXchg + 2 * 2 * 128 * 4;
-  static constexpr uint32_t kTmemCols = 512;              // S/P 0, S/P 1, O_0, O_1
-};
+using namespace bsa;
 
 // One launch computes up to two key-block ranges of the same queries, each
 // into its own O and LSE (the history and the current chunk of a chunk step).
@@ -86,7 +31,6 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o0,
     const __grid_constant__ CUtensorMap tm_o1, const uint8_t* __restrict__ mask, int q_len,
     int Lk, int Hq, int Hkv, int cur, float scale_log2, const BsaParts parts, unsigned* err) {
-  using L = Layout<D>;
   // One linear grid, decoded here so that the dispatch order is explicit:
   // part 0 before part 1, then batch, then heads, query tiles fastest.  The
   // CTAs resident together then cover a few heads of one GQA group or two,
@@ -108,420 +52,10 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t sb = smem_u32(smem);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
-  int* n_sm = reinterpret_cast<int*>(smem + L::kMisc + 4);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 8);
-
-  // barrier addresses
-  const uint32_t bar0 = smem_u32(bars);
-  const uint32_t q_full = bar0 + 0;
-  auto slot_full = [&](int s) { return bar0 + 8 * (1 + s); };
-  auto slot_empty = [&](int s) { return bar0 + 8 * (1 + L::kSlots + s); };
-  constexpr int kB2 = 1 + 2 * L::kSlots;
-  auto s_full = [&](int g) { return bar0 + 8 * (kB2 + g); };    // S(j) ready, g = j % 2
-  auto p_full = [&](int g) { return bar0 + 8 * (kB2 + 2 + g); };  // P(j) written
-  auto o_done = [&](int g) { return bar0 + 8 * (kB2 + 4 + g); };  // P V(j) complete
-  const uint32_t mma_final = bar0 + 8 * (kB2 + 6);
-  const uint32_t xbar = bar0 + 8 * (kB2 + 7);                    // end-of-row merge
-  const uint32_t stage_full = bar0 + 8 * (kB2 + 8);              // O tile staged for the store
-
-  const int nkb = Lk / kBlock;
-  const int hk = h / (Hq / Hkv);
-  const int diag = cur + qb;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint8_t* mrow = mask + (((long long)b * Hq + h) * nqb + qb) * nkb;
-  const int kb_last = min(kb_end, diag + 1);
-  const bool drop_here = (int)blockIdx.x == parts.drop_cta;
-  int kb_first = kb_last;  // producer: key block of the K tile copied before the count
-
-  if (tid == 0) {
-    mbar_init(q_full, 1);
-    for (int s = 0; s < L::kSlots; ++s) {
-      mbar_init(slot_full(s), 1);
-      mbar_init(slot_empty(s), 1);
-    }
-    for (int g = 0; g < 2; ++g) {
-      mbar_init(s_full(g), 1);
-      mbar_init(p_full(g), 128);
-      mbar_init(o_done(g), 1);
-    }
-    mbar_init(xbar, 256);
-    mbar_init(stage_full, 256);
-    mbar_init(mma_final, 1);
-    *abort_flag = 0;
-    *n_sm = 0;
-    fence_barrier_init();
-    fence_proxy_async_smem();
-    // Q and the first selected K tile do not depend on the block count, so
-    // their copies start now and their latency overlaps the count's
-    tma_prefetch_map(&tm_q);
-    tma_prefetch_map(&tm_k);
-    tma_prefetch_map(&tm_v);
-    mbar_arrive_expect_tx(q_full, L::kTile);
-    for (int r = 0; r < L::kRegions; ++r)
-      tma_load_4d(sb + L::kQ + r * kRegion, &tm_q, q_full, r * 64, h, qb * 128, b);
-    if (!(drop_here && parts.drop_item == 0)) {
-      int kb = kb_begin;
-      while (kb < kb_last && !__ldg(mrow + kb)) ++kb;
-      if (kb < kb_last) {
-        mbar_arrive_expect_tx(slot_full(0), L::kTile);
-        for (int r = 0; r < L::kRegions; ++r)
-          tma_load_4d(sb + L::kRing + r * kRegion, &tm_k, slot_full(0), r * 64, hk, kb * 128, b);
-        kb_first = kb;
-      }
-    }
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
-    tmem_relinquish();
-  }
-
-  // ---- count the selected key blocks of this row ----
-  int cnt = 0;
-  for (int kb = kb_begin + tid; kb < kb_last; kb += kThreads) cnt += mrow[kb] ? 1 : 0;
-  cnt = __reduce_add_sync(0xffffffffu, cnt);
-  __syncthreads();  // n_sm initialised
-  if (lane == 0 && cnt) atomicAdd(n_sm, cnt);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const int n = *n_sm;
-  // the diagonal block, when selected, is the last block of the row
-  const bool diag_last = diag >= kb_begin && diag < kb_end && mrow[diag] != 0;
-  const uint32_t tmem_s0 = tmem, tmem_o0 = tmem + 256;
-
-  if (n == 0) {
-    // no visible key: O = 0, LSE = -inf
-    for (int e = tid; e < 128 * D / 8; e += kThreads) {
-      const int r = e / (D / 8), c = e % (D / 8);
-      reinterpret_cast<uint4*>(o + (((long long)b * q_len + qb * 128 + r) * Hq + h) * D)[c] =
-          make_uint4(0, 0, 0, 0);
-    }
-    for (int r = tid; r < 128; r += kThreads)
-      lse[((long long)b * Hq + h) * q_len + qb * 128 + r] = -INFINITY;
-    if (tid == 0) drain_wait(q_full, 0);  // the early Q copy lands before the CTA exits
-  } else if (warp == 0) {
-    // ------------------------------ producer ------------------------------
-    if (lane == 0) {
-      // Ring items in the order the tensor pipe consumes them,
-      //   K_0, K_1, V_0, K_2, V_1, ..., K_{n-1}, V_{n-2}, V_{n-1},
-      // item i in slot i % kSlots, so that the ring is a plain FIFO.  K_0
-      // was copied before the count (unless the test hook drops item 0).
-      const bool k0_copied = kb_first < kb_last;
-      int issued = k0_copied ? 1 : 0;
-      int kb = k0_copied ? kb_first : kb_begin - 1;
-      int kb_even = k0_copied ? kb_first : 0, kb_odd = 0;  // key blocks of the two most recent K items
-      bool ok = true;
-      for (int i = issued; ok && i < 2 * n; ++i) {
-        const bool is_k = i == 0 || ((i & 1) && (i + 1) / 2 < n);
-        int blk;
-        if (is_k) {
-          blk = (i + 1) / 2;
-          do {
-            ++kb;
-          } while (kb < kb_last && !__ldg(mrow + kb));
-          if (kb >= kb_last) break;  // cannot happen: n counts these blocks
-          if (blk & 1) kb_odd = kb; else kb_even = kb;
-        } else {
-          blk = i == 2 * n - 1 ? n - 1 : (i - 2) / 2;
-        }
-        if (drop_here && i == parts.drop_item) break;
-        const int s = i % L::kSlots;
-        if (i >= L::kSlots &&
-            !mbar_wait(slot_empty(s), ((i / L::kSlots) - 1) & 1, abort_flag, err, kErrBsaTc,
-                       kSiteKvEmpty)) {
-          ok = false;
-          break;
-        }
-        const uint32_t dst = sb + L::kRing + s * L::kTile;
-        mbar_arrive_expect_tx(slot_full(s), L::kTile);
-        const CUtensorMap* map = is_k ? &tm_k : &tm_v;
-        for (int r = 0; r < L::kRegions; ++r)
-          tma_load_4d(dst + r * kRegion, map, slot_full(s), r * 64, hk,
-                      ((blk & 1) ? kb_odd : kb_even) * 128, b);
-        issued = i + 1;
-      }
-      // copies still in flight must land before the CTA may exit
-      drain_wait(q_full, 0);
-      for (int s = 0; s < L::kSlots && s < issued; ++s)
-        drain_wait(slot_full(s), ((issued - 1 - s) / L::kSlots) & 1);
-    }
-  } else if (warp == 1) {
-    // ------------------------------ MMA issuer ----------------------------
-    // The whole warp runs the loop, so that slot addresses and descriptors are
-    // warp-uniform values; one elected lane issues the tcgen05 instructions.
-    // (A single-lane issuer sharing its scheduler with ALU-bound softmax warps
-    // cannot keep the tensor pipe fed.)  The tensor pipe accepts only a few
-    // MMAs ahead, so the work between two batches is kept small: the order is
-    //   S(0), S(1), [P V(0), S(2)], [P V(1), S(3)], ..., [P V(n-1)]
-    // and each bracketed pair follows one group of waits (P(j), V_j, K_{j+2}).
-    // Every lane keeps its own wait result and runs the same number of
-    // iterations and __syncwarp()s; only the issuing lane's result decides
-    // whether it issues, so a timed-out wait needs no warp vote.
-    constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0, 0);
-    constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);
-    const bool leader = elect_one_sync();
-    auto wait = [&](bool ok, uint32_t bar, uint32_t parity, unsigned site) -> bool {
-      return ok && mbar_wait(bar, parity, abort_flag, err, kErrBsaTc, site);
-    };
-    // ring position of K_m and V_j (the producer's order)
-    auto kpos = [&](int m) { return m == 0 ? 0 : 2 * m - 1; };
-    auto vpos = [&](int j) { return j == n - 1 ? 2 * n - 1 : 2 * j + 2; };
-    // The start-address field of a shared-memory descriptor is (address >> 4)
-    // in its low bits; shared addresses are below 256 KB, so adding
-    // (offset >> 4) to a descriptor moves it by `offset` bytes.
-    const uint64_t dq = smem_desc_sw128(sb + L::kQ, 16, 1024);
-    const uint64_t dk0 = smem_desc_sw128(sb + L::kRing, 16, 1024);
-    const uint64_t dv0 = smem_desc_sw128(sb + L::kRing, kRegion, 1024);
-    // S(m) = Q K_m^T into TMEM buffer m % 2 (K_m already waited for)
-    auto issue_s = [&](int m) {
-      const int s = kpos(m) % L::kSlots;
-      const uint64_t dk = dk0 + (uint64_t)((s * L::kTile) >> 4);
-      const uint32_t d_tmem = tmem_s0 + (m & 1) * 128;
-#pragma unroll
-      for (int k = 0; k < D / 16; ++k) {  // 16 features per MMA
-        const uint32_t off = ((k >> 2) * kRegion + (k & 3) * 32) >> 4;
-        mma_bf16(d_tmem, dq + off, dk + off, idesc_qk, k > 0 ? 1u : 0u);
-      }
-      mma_commit(s_full(m & 1));
-      mma_commit(slot_empty(s));
-    };
-    bool ok = wait(true, q_full, 0, kSiteQFull);
-    for (int m = 0; m < 2 && m < n; ++m) {
-      ok = wait(ok, slot_full(kpos(m) % L::kSlots), (kpos(m) / L::kSlots) & 1, kSiteKvFull);
-      tc_fence_after();
-      if (leader && ok) issue_s(m);
-      __syncwarp();
-    }
-    for (int j = 0; j < n; ++j) {
-      const int g = j & 1;
-      const int iv = vpos(j), sv = iv % L::kSlots;
-      const bool next_s = j + 2 < n;
-      const int ik = kpos(j + 2), sk = ik % L::kSlots;
-      // the three probes are issued back to back so that their latencies
-      // overlap; the bounded waits run only if one of them found its phase
-      // still open
-      bool ready = false;
-      if (ok) {
-        const bool r0 = mbar_try_wait(p_full(g), (j >> 1) & 1);
-        const bool r1 = mbar_try_wait(slot_full(sv), (iv / L::kSlots) & 1);
-        const bool r2 = !next_s || mbar_try_wait(slot_full(sk), (ik / L::kSlots) & 1);
-        ready = r0 & r1 & r2;
-      }
-      if (!ready) {
-        ok = wait(ok, p_full(g), (j >> 1) & 1, kSitePFull);
-        ok = wait(ok, slot_full(sv), (iv / L::kSlots) & 1, kSiteKvFull);
-        if (next_s) ok = wait(ok, slot_full(sk), (ik / L::kSlots) & 1, kSiteKvFull);
-      }
-      tc_fence_after();
-      if (leader && ok) {
-        // O_g += P(j) V_j with P(j) read from TMEM buffer g (it overwrote S(j))
-        const uint64_t dv = dv0 + (uint64_t)((sv * L::kTile) >> 4);
-        const uint32_t p_tmem = tmem_s0 + g * 128;
-        const uint32_t o_tmem = tmem_o0 + g * D;
-#pragma unroll
-        for (int k = 0; k < 8; ++k)  // 16 keys per MMA: 8 TMEM columns of bf16 pairs
-          mma_bf16_tmem_a(o_tmem, p_tmem + k * 8, dv + (uint64_t)((k * 2048) >> 4), idesc_pv,
-                          (j >= 2 || k > 0) ? 1u : 0u);
-        mma_commit(o_done(g));
-        mma_commit(slot_empty(sv));
-        // S(j+2) overwrites buffer g after P V(j) has read it: the tensor
-        // pipe runs the MMAs in issue order
-        if (next_s) issue_s(j + 2);
-      }
-      __syncwarp();
-    }
-    // every MMA issued above completes before TMEM is released
-    if (leader) mma_commit(mma_final);
-    __syncwarp();
-    drain_wait(mma_final, 0);
-  } else {
-    // ------------------------------ softmax -------------------------------
-    const int quad = warp & 3;           // TMEM lane quadrant this warp may access
-    const int grp = (warp - 2) >> 2;     // takes blocks j = grp, grp + 2, ...
-    const int row = quad * 32 + lane;    // query row within the tile
-    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    const uint32_t sbuf = tmem_s0 + lane_base + grp * 128;
-    const uint32_t obuf = tmem_o0 + lane_base + grp * D;
-    float m_run = -INFINITY, l_run = 0.f;
-    bool ok = true;
-    for (int j = grp; j < n; j += 2) {
-      if (!mbar_wait_warp(s_full(grp), (j >> 1) & 1, abort_flag, err, kErrBsaTc, kSiteSFull)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      // S(j) into registers, the diagonal block masked causally (key column c
-      // is visible to row r iff c <= r)
-      auto load_s = [&](float* x) {
-        tmem_ld128(sbuf, x);
-        if (diag_last && j == n - 1) {
-#pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c > row) x[c] = -INFINITY;
-        }
-      };
-      // P = exp2(x * scale - m_run) as bf16 pairs, and the row sum.  The
-      // exponent argument and the sum use the packed two-wide fp32 FMA/add:
-      // the softmax warps share their schedulers with the MMA issuer and the
-      // producer, and the launch runs under the power cap, so every
-      // instruction saved counts.
-      uint32_t pk[64];
-      float2 ps[2];
-      float alpha = 1.f;
-      const float2 sc2 = make_float2(scale_log2, scale_log2);
-      auto exps = [&](const float* x) {
-        ps[0] = make_float2(0.f, 0.f);
-        ps[1] = make_float2(0.f, 0.f);
-        const float2 nm2 = make_float2(-m_run, -m_run);
-#pragma unroll
-        for (int c = 0; c < 128; c += 2) {
-          const float2 t = __ffma2_rn(make_float2(x[c], x[c + 1]), sc2, nm2);
-          const float2 p = make_float2(fast_exp2(t.x), fast_exp2(t.y));
-          ps[(c >> 1) & 1] = __fadd2_rn(ps[(c >> 1) & 1], p);
-          __nv_bfloat162 b2 = __floats2bfloat162_rn(p.x, p.y);
-          pk[c >> 1] = *reinterpret_cast<uint32_t*>(&b2);
-        }
-      };
-      // After the group's first block the running max is not raised before
-      // the exponentials: the block is exponentiated against the current
-      // m_run, which is correct for any m_run (O and l carry the same scale)
-      // as long as no P overflows.  A row sum within kMaxBlockSum bounds
-      // every P of the row; beyond it (or inf/NaN) the warp takes the slow
-      // path: the row max, the new m_run, the exponentials again and O_g
-      // rescaled.  That drops the max pass from almost every block.
-      bool slow = j < 2;
-      if (!slow) {
-        float x[128];
-        load_s(x);
-        exps(x);
-        const float sblk = (ps[0].x + ps[0].y) + (ps[1].x + ps[1].y);
-        slow = __any_sync(0xffffffffu, !(sblk <= kMaxBlockSum));
-      }
-      if (slow) {
-        float x[128];
-        load_s(x);  // S(j) is still in TMEM: P has not been written over it
-        // row max in eight independent chains of three-way max
-        float mx[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) mx[e] = x[e];
-#pragma unroll
-        for (int c = 8; c < 128; c += 16)
-#pragma unroll
-          for (int e = 0; e < 8; ++e) mx[e] = fmax3(mx[e], x[c + e], x[c + 8 + e]);
-        const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
-                               fmaxf(mx[6], mx[7])) * scale_log2;
-        if (mt > m_run) {
-          alpha = fast_exp2(m_run - mt);  // 0 on the group's first block
-          m_run = mt;
-        }
-        exps(x);
-        // O_g is rescaled between P V(j-2) and P V(j).  P V(j-2) is
-        // complete: the tensor pipe ran it before S(j), which we have read.
-        if (j >= 2) {
-#pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) {
-            float t[32];
-            tmem_ld32(obuf + cc * 32, t);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) t[e] *= alpha;
-            tmem_st32(obuf + cc * 32, t);
-          }
-        }
-      }
-      l_run = l_run * alpha + ((ps[0].x + ps[0].y) + (ps[1].x + ps[1].y));
-      tmem_st64(sbuf, reinterpret_cast<const float*>(pk));  // P(j) over S(j)
-      tc_fence_before();
-      mbar_arrive(p_full(grp));
-    }
-    // ---- merge the two groups' partial results per row ----
-    float* xm = reinterpret_cast<float*>(smem + L::kXchg);   // [group][m, l][row]
-    xm[(grp * 2 + 0) * 128 + row] = m_run;
-    xm[(grp * 2 + 1) * 128 + row] = l_run;
-    const int j_last = ((n - 1 - grp) >= 0) ? n - 1 - ((n - 1 - grp) & 1) : -1;
-    if (ok && j_last >= 0 &&
-        !mbar_wait_warp(o_done(grp), (j_last >> 1) & 1, abort_flag, err, kErrBsaTc,
-                        kSiteODoneFinal))
-      ok = false;
-    mbar_arrive(xbar);
-    if (!mbar_wait_warp(xbar, 0, abort_flag, err, kErrBsaTc, kSiteXchg)) ok = false;
-    if (ok) {
-      tc_fence_after();
-      const float m0 = xm[0 * 128 + row], l0 = xm[1 * 128 + row];
-      const float m1 = xm[2 * 128 + row], l1 = xm[3 * 128 + row];
-      const float m = fmaxf(m0, m1);
-      // group 1 has no block when n == 1 (uniform over the CTA, so the
-      // warp-collective TMEM loads below stay convergent)
-      const bool has1 = n >= 2;
-      const float w0 = fast_exp2(m0 - m);
-      const float w1 = has1 ? fast_exp2(m1 - m) : 0.f;
-      const float l = l0 * w0 + l1 * w1;
-      const float inv = 1.f / l;
-      const float f0 = w0 * inv, f1 = w1 * inv;
-      // This group writes output columns [grp * D/2, grp * D/2 + D/2) of its
-      // row into the Q buffer (every MMA is complete), in the 128-byte
-      // swizzled layout of the tensor map's box: feature f of row r sits in
-      // region f / 64, 16-byte chunk ((f % 64) / 8) ^ (r % 8) of the row's
-      // 128 bytes.  One TMA store then writes the tile.
-      uint8_t* stage = smem + L::kQ;
-#pragma unroll
-      for (int cc = 0; cc < D / 64; ++cc) {
-        const int col = grp * (D / 2) + cc * 32;
-        float t0[32], t1[32];
-        tmem_ld32(tmem_o0 + lane_base + col, t0);
-        if (has1) {
-          tmem_ld32(tmem_o0 + lane_base + D + col, t1);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) t0[e] = t0[e] * f0 + t1[e] * f1;
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) t0[e] *= f0;
-        }
-#pragma unroll
-        for (int e = 0; e < 32; e += 8) {
-          uint4 pk4;
-          __nv_bfloat162 a0 = __floats2bfloat162_rn(t0[e + 0], t0[e + 1]);
-          __nv_bfloat162 a1 = __floats2bfloat162_rn(t0[e + 2], t0[e + 3]);
-          __nv_bfloat162 a2 = __floats2bfloat162_rn(t0[e + 4], t0[e + 5]);
-          __nv_bfloat162 a3 = __floats2bfloat162_rn(t0[e + 6], t0[e + 7]);
-          pk4.x = *reinterpret_cast<uint32_t*>(&a0);
-          pk4.y = *reinterpret_cast<uint32_t*>(&a1);
-          pk4.z = *reinterpret_cast<uint32_t*>(&a2);
-          pk4.w = *reinterpret_cast<uint32_t*>(&a3);
-          const int f = col + e;
-          *reinterpret_cast<uint4*>(stage + (f >> 6) * kRegion + row * 128 +
-                                    ((((f & 63) >> 3) ^ (row & 7)) << 4)) = pk4;
-        }
-      }
-      if (grp == 0)
-        lse[((long long)b * Hq + h) * q_len + qb * 128 + row] =
-            (m + __log2f(l)) * 0.69314718055994531f;
-    }
-    // the staged tile is visible to the async proxy once every softmax
-    // thread has arrived; one thread stores it and waits until the copy has
-    // read shared memory (the CTA's shared memory must outlive the read)
-    fence_proxy_async_smem();
-    mbar_arrive(stage_full);
-    if (tid == 64 && ok &&
-        mbar_wait(stage_full, 0, abort_flag, err, kErrBsaTc, kSiteStage)) {
-      const CUtensorMap* tmo = part ? &tm_o1 : &tm_o0;
-      for (int r = 0; r < L::kRegions; ++r)
-        tma_store_4d(tmo, sb + L::kQ + r * kRegion, r * 64, h, qb * 128, b);
-      bulk_commit_group();
-      bulk_wait_group_read0();
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    __syncwarp();
-    tc_fence_after();
-    tmem_dealloc(tmem, L::kTmemCols);
-  }
+  const BsaArgs a{&tm_q, &tm_k, &tm_v, mask, q_len, Lk, Hq, Hkv, nqb, cur, scale_log2, err};
+  const BsaTile tile{b, h, qb, kb_begin, kb_end, o, lse, part ? &tm_o1 : &tm_o0,
+                     (int)blockIdx.x == parts.drop_cta, parts.drop_item, nullptr, nullptr};
+  bsa_cta<D, false>(a, tile, smem);
 }
 
 template <int D>

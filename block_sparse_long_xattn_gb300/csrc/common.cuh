@@ -13,6 +13,7 @@ constexpr int kBlock = 128;  // BSA block size (fixed at 128 tokens)
 enum ErrKernel : unsigned {
   kErrBsaTc = 1,
   kErrEstimateTc = 2,
+  kErrFused = 3,  // the fused chunk step's waits for other CTAs' results
 };
 __device__ __forceinline__ void record_error(unsigned* err, unsigned kernel,
                                              unsigned site) {

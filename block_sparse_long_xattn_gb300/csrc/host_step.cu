@@ -6,10 +6,23 @@
 
 #include "../../include/bsxattn.h"
 #include "common.cuh"
+#include "launchers.h"
 
 namespace {
 
 bool a16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// BSX_STEP_FUSED without the offload mask or e4m3 estimate operands runs as
+// bsx_chunk_prefill, one kernel where the problem allows it.
+bool one_kernel(const bsx_shape& s, int q_len, int P, int stride, int flags) {
+  if (!(flags & BSX_STEP_FUSED) || (flags & (BSX_STEP_OFFLOAD | BSX_STEP_E4M3_ESTIMATE)))
+    return false;
+  bsx::Problem p{};
+  p.dtype = s.dtype;
+  p.d = s.d;
+  p.nkb = (P + q_len) / 128;
+  return bsx::fused_step_supported(p, stride);
+}
 
 int cuda_fail(cudaError_t e) {
   fprintf(stderr, "bsxattn: CUDA error %s\n", cudaGetErrorString(e));
@@ -47,9 +60,13 @@ int validate(const bsx_shape& s, const void* qh, const void* kh, const void* vh,
     if (s.dtype != BSX_BF16 || s.d != 128) return BSX_ERR_UNSUPPORTED;
     if (!a16(dev->q8) || !a16(dev->k8)) return BSX_ERR_INVALID_ARG;
   }
-  const size_t need = bsx_estimate_workspace_bytes(
-      bsx_shape{s.B, s.Hq, s.Hkv, s.d, (flags & BSX_STEP_E4M3_ESTIMATE) ? BSX_F8E4M3 : s.dtype},
-      q_len, P, stride);
+  const size_t need =
+      one_kernel(s, q_len, P, stride, flags)
+          ? bsx_chunk_prefill_workspace_bytes(s, q_len, P, stride)
+          : bsx_estimate_workspace_bytes(
+                bsx_shape{s.B, s.Hq, s.Hkv, s.d,
+                          (flags & BSX_STEP_E4M3_ESTIMATE) ? BSX_F8E4M3 : s.dtype},
+                q_len, P, stride);
   if (need == 0 || !a16(dev->workspace) || dev->workspace_bytes < need) return BSX_ERR_WORKSPACE;
   return BSX_OK;
 }
@@ -80,6 +97,22 @@ struct CallEvents {
 cudaError_t follow(cudaStream_t dst, cudaStream_t src, cudaEvent_t ev) {
   cudaError_t e = cudaEventRecord(ev, src);
   return e == cudaSuccess ? cudaStreamWaitEvent(dst, ev, 0) : e;
+}
+
+// Read-back of O, LSE (and the keep flags) on `dn`, after the step's launches
+// on `st`; then `done` is recorded on `dn`.
+int read_back(const bsx_shape& s, const bsx_chunk_buffers* dev, int n_cpu, bool map,
+              size_t o_bytes, size_t lse_bytes, void* o_host, float* lse_host,
+              uint8_t* keep_host, cudaStream_t st, cudaStream_t dn, cudaEvent_t done,
+              cudaEvent_t ev) {
+  cudaError_t e = dn != st ? follow(dn, st, ev) : cudaSuccess;
+  if (e == cudaSuccess) e = cudaMemcpyAsync(o_host, dev->o, o_bytes, cudaMemcpyDeviceToHost, dn);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(lse_host, dev->lse, lse_bytes, cudaMemcpyDeviceToHost, dn);
+  if (e == cudaSuccess && keep_host && map)
+    e = cudaMemcpyAsync(keep_host, dev->keep, (size_t)s.B * n_cpu, cudaMemcpyDeviceToHost, dn);
+  if (e == cudaSuccess && done) e = cudaEventRecord(done, dn);
+  return e == cudaSuccess ? BSX_OK : cuda_fail(e);
 }
 
 }  // namespace
@@ -129,6 +162,19 @@ extern "C" int bsx_chunk_step_host(bsx_shape s, const void* q_host, const void* 
   if (e == cudaSuccess && up != st) e = cudaEventRecord(ev.ev[1], up);
   if (e != cudaSuccess) return cuda_fail(e);
 
+  if (one_kernel(s, q_len, P, stride, flags)) {
+    // estimate, selection and attention in one launch, which reads V as well
+    if (up != st && cudaStreamWaitEvent(st, ev.ev[1], 0) != cudaSuccess) return BSX_ERR_CUDA;
+    rc = bsx_chunk_prefill(s, dev->q, dev->k, dev->v, q_len, P, stride, threshold, dev->mask,
+                           dev->o, dev->lse, dev->workspace, dev->workspace_bytes, st);
+    if (rc == BSX_OK && map)
+      rc = bsx_map_mask_to_cpu_blocks(s, dev->mask, q_len, P, cpu_block_tokens,
+                                      flags & BSX_FORCE_FIRST_LAST, dev->keep, st);
+    if (rc != BSX_OK) return rc;
+    return read_back(s, dev, n_cpu, map, q_elems * elt, lse_bytes, o_host, lse_host,
+                     keep_host, st, dn, done, ev.ev[2]);
+  }
+
   // estimate (on e4m3 copies of the uploaded Q and K when asked)
   const void* qe = dev->q;
   const void* ke = dev->k;
@@ -174,14 +220,6 @@ extern "C" int bsx_chunk_step_host(bsx_shape s, const void* q_host, const void* 
                                     dev->keep, st);
   if (rc != BSX_OK) return rc;
 
-  // read-back, after the step's launches
-  e = dn != st ? follow(dn, st, ev.ev[2]) : cudaSuccess;
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(o_host, dev->o, q_elems * elt, cudaMemcpyDeviceToHost, dn);
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(lse_host, dev->lse, lse_bytes, cudaMemcpyDeviceToHost, dn);
-  if (e == cudaSuccess && keep_host && map)
-    e = cudaMemcpyAsync(keep_host, dev->keep, (size_t)s.B * n_cpu, cudaMemcpyDeviceToHost, dn);
-  if (e == cudaSuccess && done) e = cudaEventRecord(done, dn);
-  return e == cudaSuccess ? BSX_OK : cuda_fail(e);
+  return read_back(s, dev, n_cpu, map, q_elems * elt, lse_bytes, o_host, lse_host,
+                   keep_host, st, dn, done, ev.ev[2]);
 }

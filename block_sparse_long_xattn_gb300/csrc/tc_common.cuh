@@ -108,6 +108,32 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Bounded wait, by one thread, for a counter in global memory written by
+// other CTAs: *p >= need (acquire: what was written before the matching
+// release is visible after it).  Gives up when *gabort is set, or after 2 s
+// of wall time, when it sets *gabort and records (kernel, site).
+__device__ __forceinline__ bool wait_counter(const unsigned* p, unsigned need, unsigned* gabort,
+                                             unsigned* err, unsigned kernel, unsigned site) {
+  if (ld_acquire_gpu(p) >= need) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (ld_acquire_gpu(p) >= need) return true;
+    if (ld_acquire_gpu(gabort) != 0) return false;
+    if ((it & 15u) == 0 && global_timer_ns() - t0 > 2000000000ull) {
+      atomicExch(gabort, 1u);
+      record_error(err, kernel, site);
+      return false;
+    }
+    __nanosleep(64);
+  }
+}
+
 // mbar_wait with one result for the whole (converged) warp: warps that go on
 // to warp-collective tcgen05 loads and stores must leave a wait together,
 // never some lanes through the timeout and others through the phase.  One

@@ -210,14 +210,43 @@ int bsx_bsa_prefill_split(bsx_shape s, const void* q, const void* k, const void*
                           void* stream);
 
 /*
+ * Bytes of device workspace bsx_chunk_prefill needs: the estimate partials
+ * of bsx_estimate_workspace_bytes(), rounded up to 256 bytes; then a control
+ * block of 4 * (4 + B * Hq * (ceil(R / 128) + q_len / 128)) bytes rounded up
+ * to 256 (the fused launch's counters and ready flags), with R = q_len /
+ * stride; then 4 * B * Hq * n_kt * R bytes rounded up to 256, n_kt =
+ * (q_start_pos / stride + R - 1) / 256 + 1 (each reshaped row's
+ * log-sum-exp over each 256-key tile, which the fused selection reads).
+ * Returns 0 for invalid arguments.
+ */
+size_t bsx_chunk_prefill_workspace_bytes(bsx_shape s, int q_len, int q_start_pos,
+                                         int stride);
+
+/*
  * One chunk of XAttention prefill with the KV resident on the device:
  * bsx_xattn_estimate followed by bsx_bsa_prefill over every key block
- * [0, Lk/128) in one launch.  By the merge identity this equals attending to
- * the history and the current chunk separately and merging them by LSE (the
- * structure of xattn_bsa.py compute_chunked_prefill), without the second
- * launch and the merge.  Outputs: mask (as bsx_xattn_estimate), o, lse (as
- * bsx_bsa_prefill).  Arguments are validated before anything is enqueued;
- * workspace as for bsx_xattn_estimate.
+ * [0, Lk/128).  By the merge identity this equals attending to the history
+ * and the current chunk separately and merging them by LSE (the structure of
+ * xattn_bsa.py compute_chunked_prefill), without the merge.
+ *
+ * docs/xattention_algorithm_guide.md "算法流程": estimate, select, attend, in
+ * that order, for one chunk.  In bf16 with at most 1024 key blocks (Lk <=
+ * 131072) the three stages run as ONE kernel launch (preceded by a 4-byte-
+ * granular memset of the control block on the same stream): CTAs take
+ * roles in the order they start -- estimate workers, which also select each
+ * row once its estimate tiles are complete, then one attention CTA per
+ * 128-row query tile, which waits for its row's mask; every such wait is
+ * bounded (a wait that gives up sets the device error word, kernel id 3, and
+ * ends the other waits; bsx_last_error).  Otherwise (f32, or more key blocks)
+ * the estimate and the attention are separate launches.  The mask, o and lse
+ * are those of the separate calls (the fused selection adds its row sums in
+ * another order, which can only change near-threshold rows).
+ *
+ * Outputs: mask (as bsx_xattn_estimate), o, lse (as bsx_bsa_prefill).
+ * Arguments are validated before anything is enqueued.  workspace (device,
+ * 16-byte aligned) of at least bsx_chunk_prefill_workspace_bytes() bytes,
+ * overwritten; else BSX_ERR_WORKSPACE.  Calls that overlap on the GPU need
+ * separate workspaces.
  */
 int bsx_chunk_prefill(bsx_shape s, const void* q, const void* k, const void* v,
                       int q_len, int q_start_pos, int stride, float threshold,
@@ -295,7 +324,9 @@ typedef struct {
   uint8_t* keep;          /* [B,q_start_pos/cpu_block_tokens] or NULL (no flags) */
   uint8_t* q8;            /* [B,q_len,Hq,d] e4m3; BSX_STEP_E4M3_ESTIMATE only */
   uint8_t* k8;            /* [B,Lk,Hkv,d]   e4m3; BSX_STEP_E4M3_ESTIMATE only */
-  void* workspace;        /* bsx_estimate_workspace_bytes(s, ...) bytes */
+  void* workspace;        /* bsx_estimate_workspace_bytes(s, ...) bytes, or
+                             bsx_chunk_prefill_workspace_bytes() for a step
+                             that runs as bsx_chunk_prefill (BSX_STEP_FUSED) */
   size_t workspace_bytes;
   void* done;             /* a cudaEvent_t, or NULL; see bsx_chunk_step_host */
 } bsx_chunk_buffers;
@@ -326,7 +357,10 @@ typedef struct {
  * BSX_STEP_FUSED replaces the split attention and the merge by one
  * bsx_bsa_prefill over every key block into (dev->o, dev->lse), as
  * bsx_chunk_prefill does (with q_start_pos = 0: whole-sequence prefill);
- * dev->o_curr and dev->lse_curr are then not used and may be NULL.
+ * dev->o_curr and dev->lse_curr are then not used and may be NULL.  Without
+ * BSX_STEP_OFFLOAD and BSX_STEP_E4M3_ESTIMATE the step then IS
+ * bsx_chunk_prefill (one kernel where that call runs one, after all three
+ * uploads), and dev->workspace must hold bsx_chunk_prefill_workspace_bytes().
  * With BSX_STEP_OFFLOAD and q_start_pos >= cpu_block_tokens, dev->keep is
  * required.
  *
@@ -359,8 +393,9 @@ int bsx_chunk_step_host(bsx_shape s, const void* q_host, const void* k_host,
 /*
  * Test hook for the failure path (not for production use).  Arms, for the
  * calling host thread only, the next bf16 bsx_bsa_prefill or
- * bsx_bsa_prefill_split launch (including those made by bsx_chunk_prefill
- * and bsx_chunk_step_host): in CTA `cta` of that launch (its linear grid
+ * bsx_bsa_prefill_split launch (including those made by bsx_chunk_step_host,
+ * and by bsx_chunk_prefill when it does not run as one fused kernel): in CTA
+ * `cta` of that launch (its linear grid
  * index; CTA 0 is the last 128-row query tile of head 0 of batch 0 in the
  * first key-block range) the copy producer stops before K/V ring item
  * `item` (items in the order the tensor pipe consumes them: K_0, K_1, V_0,
@@ -373,6 +408,19 @@ int bsx_chunk_step_host(bsx_shape s, const void* q_host, const void* k_host,
  * cta >= 0 with item < 0.
  */
 int bsx_debug_drop_ring_item(int cta, int item);
+
+/*
+ * Test hook for the failure path of the fused chunk step (not for production
+ * use).  Arms, for the calling host thread only, its next bsx_chunk_prefill
+ * that runs as one kernel: selection row `row` (row = (b * Hq + h) * (q_len /
+ * 128) + qb) writes its mask but never marks it ready, so that row's
+ * attention CTA's bounded wait runs out (about 2 s); it then writes o = 0 and
+ * lse = -inf for its rows, and the device error word records kernel id 3
+ * (the fused step), wait site 1 (bsx_last_error).  The other rows are not
+ * affected.  The call consumes the setting; row < 0 disarms it.  Returns
+ * BSX_OK.
+ */
+int bsx_debug_fused_skip_row(int row);
 
 /*
  * Asynchronous error status of the device.  Waits
@@ -390,7 +438,11 @@ int bsx_last_error(void* stream);
 /*
  * The raw error word read by the calling host thread's last bsx_last_error
  * call (0 = none; otherwise bit 31 set, bits 0..7 the kernel: 1 = tcgen05
- * attention, 2 = tcgen05 estimator, bits 8..15 the wait that gave up).
+ * attention, 2 = tcgen05 estimator (both also inside the fused chunk step),
+ * 3 = the fused chunk step's hand-over between its stages; bits 8..15 the
+ * wait that gave up; for kernel 3: 1 = an attention CTA's wait for its
+ * row's mask, 2 = a selection's wait for its estimate tiles, 3 = a worker's
+ * tile-id ring).
  */
 unsigned int bsx_last_error_code(void);
 

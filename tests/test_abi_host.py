@@ -53,6 +53,48 @@ def test_workspace_formula(lib):
     assert lib.bsx_estimate_workspace_bytes(s, 4096, 0, 3) == 0      # bad stride
 
 
+def test_chunk_prefill_workspace_formula(lib):
+    s = L.BsxShape(1, 32, 8, 128, L.BSX_BF16)
+    # the partials (rounded up to 256 bytes), then the fused launch's control
+    # block: 4 counters, tiles_done per (b, h, 128-row tile of reshaped rows),
+    # row_ready per (b, h, q-block), 4 bytes each, rounded up to 256; then one
+    # float per (b, h, 256-key tile of the last row tile, reshaped row),
+    # rounded up to 256
+    est = 32 * 256 * 512 * 4
+    ctl = (4 + 32 * (512 // 128 + 4096 // 128)) * 4
+    n_kt = (28672 // 8 + 512 - 1) // 256 + 1            # 16 key tiles at 32K
+    assert lib.bsx_chunk_prefill_workspace_bytes(s, 4096, 28672, 8) == \
+        est + (ctl + 255) // 256 * 256 + 32 * n_kt * 512 * 4
+    tiny = L.BsxShape(1, 1, 1, 64, L.BSX_BF16)
+    assert lib.bsx_estimate_workspace_bytes(tiny, 128, 0, 16) == 32
+    assert lib.bsx_chunk_prefill_workspace_bytes(tiny, 128, 0, 16) == 256 + 256 + 256
+    assert lib.bsx_chunk_prefill_workspace_bytes(s, 4000, 0, 8) == 0   # q_len not /128
+    assert lib.bsx_chunk_prefill_workspace_bytes(s, 4096, 0, 3) == 0   # bad stride
+
+
+def test_chunk_prefill_rejects_bad_arguments(lib):
+    s = L.BsxShape(1, 4, 2, 128, L.BSX_BF16)
+    p = ctypes.c_void_p(64)
+    need = lib.bsx_chunk_prefill_workspace_bytes(s, 512, 1024, 8)
+
+    def call(shape=s, stride=8, tau=0.9, v=p, ws=need, wp=p):
+        return lib.bsx_chunk_prefill(shape, p, p, v, 512, 1024, stride, tau, p, p, p, wp, ws,
+                                     None)
+    assert call(stride=3) == -2
+    assert call(tau=float("nan")) == -1
+    assert call(tau=0.0) == -1
+    assert call(v=None) == -1
+    assert call(v=ctypes.c_void_p(72)) == -1                        # misaligned
+    assert call(shape=L.BsxShape(1, 3, 2, 128, 1)) == -1            # Hq % Hkv
+    assert call(ws=need - 1) == -5                                  # no room for the control block
+    assert call(wp=None) == -5
+
+
+def test_debug_fused_skip_row_hook(lib):
+    assert lib.bsx_debug_fused_skip_row(3) == 0          # arm ...
+    assert lib.bsx_debug_fused_skip_row(-1) == 0         # ... and disarm (no launch here)
+
+
 NULL = None
 
 
@@ -151,6 +193,8 @@ def test_chunk_step_host_rejects_bad_arguments(lib):
     assert _host_step(lib, flags=4, drop=("k8",)) == -1               # e4m3 needs its copies
     assert _host_step(lib, flags=4, shape=L.BsxShape(1, 4, 2, 64, 1)) == -2  # e4m3: d = 128
     assert _host_step(lib, ws=16) == -5                               # workspace too small
+    est_only = lib.bsx_estimate_workspace_bytes(L.BsxShape(1, 4, 2, 128, 1), 256, 1024, 8)
+    assert _host_step(lib, flags=8, ws=est_only) == -5                # fused: + control block
 
 
 def test_debug_drop_hook_arguments(lib):

@@ -25,8 +25,8 @@ import pytest
 import torch
 
 from block_sparse_long_xattn_gb300 import (
-    bsx_bsa_prefill, bsx_bsa_prefill_split, bsx_last_error, bsx_map_mask_to_cpu_blocks,
-    bsx_merge_attn, bsx_quantize_e4m3, bsx_xattn_estimate)
+    bsx_bsa_prefill, bsx_bsa_prefill_split, bsx_chunk_prefill, bsx_last_error,
+    bsx_map_mask_to_cpu_blocks, bsx_merge_attn, bsx_quantize_e4m3, bsx_xattn_estimate)
 from block_sparse_long_xattn_gb300.inputs import (CONFIGS, SPARSE_CONFIGS, make_workload,
                                                   round_to_e4m3)
 from oracle import xattn_oracle as O
@@ -204,6 +204,35 @@ def test_sparse_regime_full_size(name):
     estimator) at the 32K and 128K chunk sizes: every mask row, every CTA."""
     assert name in SPARSE_CONFIGS
     _run_single_chunk(name)
+
+
+@pytest.mark.parametrize("name", ["llama8b-32k-chunk4096", "llama8b-128k-chunk4096",
+                                  "llama8b-32k-rho10"])
+def test_fused_chunk_step_full_size(name):
+    """bsx_chunk_prefill at full size, the one fused kernel bench.py --step
+    fused times (1024 key blocks at 128K: the largest selection it runs).
+    Every mask row against the oracle (the tie rule with the stand-alone
+    estimator's block sums, whose rounding the fused selection shares); O /
+    LSE of every attention CTA on the kernel's own mask."""
+    c, S, tau, _ = _cfg(name)
+    w = make_workload(seed=0, **c)
+    P = w.q_start_pos
+    q, k, v = (to_dev(x, w.dtype) for x in (w.q, w.k, w.v))
+    mask, o, lse = bsx_chunk_prefill(q, k, v, P, S, tau)
+    torch.cuda.synchronize()
+    assert bsx_last_error() == 0
+    assert bool(torch.isfinite(o.float()).all()) and bool(torch.isfinite(lse).all())
+    B, Lq, Hq, _ = w.q.shape
+    nkb = w.k.shape[1] // 128
+    A = torch.empty((B, Hq, Lq // 128, nkb), dtype=torch.float32, device="cuda")
+    bsx_xattn_estimate(q, k, P, S, tau, block_sums=A)
+    est = O.xattn_estimate(w.q, w.k, P, S, tau)
+    m_g = mask.cpu().numpy()
+    n_rows, n_near, n_tie = check_mask(m_g, est, tau, P, A.cpu().numpy())
+    errs = _check_rows(w, m_g, o, lse, P, range(Hq), 0, nkb)
+    _record(f"{name} fused", rows=n_rows, near_threshold=n_near, tie_swaps=n_tie,
+            density=_density(est.mask, P), gpu_density=_density(m_g, P),
+            o_lse_max_err=[float(x) for x in errs])
 
 
 def test_llama8b_64k_chunked_sequence():

@@ -268,24 +268,76 @@ def test_bsa_running_max_grows_every_block(d):
     assert np.abs(lse.cpu().numpy() - lse_ref).max() <= LSE_TOL * max(1.0, np.abs(lse_ref).max() / 100)
 
 
-def test_fused_chunk_prefill_equals_split_and_oracle():
-    """bsx_chunk_prefill (estimate + BSA over every key block, no merge) equals
-    the oracle's estimate + attention over all columns (rows of near-threshold
-    masks excepted: there BSA runs on the oracle's mask in a second call)."""
-    P, S, tau = 768, 8, 0.9
-    w = make_workload(seed=91, B=1, Hq=8, Hkv=2, d=128, Lk=P + 512, q_start_pos=P,
-                      alpha=3.0, n_hot=2, dtype="bf16")
+FUSED_CASES = [
+    # (B, Hq, Hkv, d, Lk, P, stride, tau, alpha, n_hot)
+    (1, 8, 2, 128, 1280, 768, 8, 0.9, 3.0, 2),
+    (2, 4, 1, 64, 768, 256, 4, 0.9, 2.0, 1),        # batch 2, d 64, stride 4
+    (1, 4, 2, 128, 2048, 1536, 16, 0.9, 4.0, 3),    # stride 16
+    (1, 2, 2, 128, 512, 0, 8, 0.8, 0.0, 0),         # whole-sequence prefill
+    (1, 4, 1, 128, 1152, 1024, 8, 0.99, 3.0, 2),    # a chunk of one block
+    (1, 4, 2, 128, 1024, 512, 8, 1.0, 3.0, 2),      # threshold 1: every causal block
+    (1, 2, 1, 64, 40960, 40704, 8, 0.9, 3.0, 4),    # 320 key blocks: the 1024-key select
+]
+
+
+@pytest.mark.parametrize("case", FUSED_CASES)
+def test_fused_chunk_prefill(case):
+    """bsx_chunk_prefill as one kernel (estimate workers, in-kernel selection,
+    attention CTAs waiting on row flags): the mask against the oracle's
+    estimate (near-threshold rule; the tie rule with the stand-alone
+    estimator's block sums, whose rounding the fused selection shares), and
+    O / LSE against the oracle's attention over every key block on the
+    kernel's own mask, every row."""
+    B, Hq, Hkv, d, Lk, P, S, tau, alpha, n_hot = case
+    w = make_workload(seed=91 + Lk + P, B=B, Hq=Hq, Hkv=Hkv, d=d, Lk=Lk, q_start_pos=P,
+                      alpha=alpha, n_hot=n_hot, dtype="bf16")
     q, k, v = (to_dev(x, "bf16") for x in (w.q, w.k, w.v))
     mask, o, lse = bsx_chunk_prefill(q, k, v, P, S, tau)
     torch.cuda.synchronize()
+    assert bsx_last_error() == 0
+    _, A_g = _estimate(w, S, tau)
     est = O.xattn_estimate(w.q, w.k, P, S, tau)
     m_g = mask.cpu().numpy()
-    if np.array_equal(m_g.astype(bool), est.mask):
-        o_ref, lse_ref = O.bsa_prefill(w.q, w.k, w.v, est.mask, P, 0, (P + 512) // 128)
-    else:   # a near-threshold row differs: compare attention on the GPU's own mask
-        o_ref, lse_ref = O.bsa_prefill(w.q, w.k, w.v, m_g, P, 0, (P + 512) // 128)
+    check_mask(m_g, est, tau, P, A_g)
+    if Lk > 8192:   # sampled rows: every query tile, both halves
+        rows = np.array(sorted({r for t in range((Lk - P) // 128)
+                                for r in (t * 128 + 3, t * 128 + 100)}))
+        for h in range(Hq):
+            o_r, l_r = O.bsa_rows(w.q, w.k, w.v, m_g, P, 0, Lk // 128, 0, h, rows)
+            assert np.abs(o.float().cpu().numpy()[0, rows, h] - o_r).max() <= O_TOL["bf16"]
+            assert np.abs(lse.cpu().numpy()[0, h, rows] - l_r).max() <= LSE_TOL
+        return
+    o_ref, lse_ref = O.bsa_prefill(w.q, w.k, w.v, m_g, P, 0, Lk // 128)
     assert np.abs(o.float().cpu().numpy() - o_ref).max() <= O_TOL["bf16"]
     assert np.abs(lse.cpu().numpy() - lse_ref).max() <= LSE_TOL
+
+
+def test_fused_chunk_prefill_many_tiles_per_worker():
+    """32 q-heads over an 8K context: more estimate tiles than SMs, so every
+    worker takes several from the counter and the selection rows wait on
+    tiles of other workers; the fused result equals the separate launches'
+    (the same mask outside near-threshold rows, attention on it within the
+    tolerance) and the oracle's on sampled rows of every query tile."""
+    P, Lq, S, tau = 4096, 4096, 8, 0.9
+    w = make_workload(seed=93, B=1, Hq=32, Hkv=8, d=128, Lk=P + Lq, q_start_pos=P,
+                      alpha=3.0, n_hot=8, dtype="bf16")
+    q, k, v = (to_dev(x, "bf16") for x in (w.q, w.k, w.v))
+    mask, o, lse = bsx_chunk_prefill(q, k, v, P, S, tau)
+    torch.cuda.synchronize()
+    assert bsx_last_error() == 0
+    nkb = (P + Lq) // 128
+    est = O.xattn_estimate(w.q, w.k, P, S, tau)
+    _, A_g = _estimate(w, S, tau)
+    m_g = mask.cpu().numpy()
+    check_mask(m_g, est, tau, P, A_g)
+    o2, lse2 = bsx_bsa_prefill(q, k, v, mask, P)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)   # the same attention code
+    rows = np.array(sorted({t * 128 + (t * 41 + 7) % 128 for t in range(Lq // 128)}))
+    for h in (0, 13, 31):
+        o_r, l_r = O.bsa_rows(w.q, w.k, w.v, m_g, P, 0, nkb, 0, h, rows)
+        assert np.abs(o.float().cpu().numpy()[0, rows, h] - o_r).max() <= O_TOL["bf16"]
+        assert np.abs(lse.cpu().numpy()[0, h, rows] - l_r).max() <= LSE_TOL
 
 
 def test_offload_semantics_chunk_step():
@@ -512,3 +564,41 @@ def test_bounded_wait_timeout_is_reported_and_the_context_survives():
     o_ref, lse_ref = O.bsa_prefill(w.q, w.k, w.v, mask_np, P, 0, nkb)
     assert np.abs(o.float().cpu().numpy() - o_ref).max() <= O_TOL["bf16"]
     assert np.abs(lse.cpu().numpy() - lse_ref).max() <= LSE_TOL
+
+
+def test_fused_step_wait_timeout_is_reported_and_the_context_survives():
+    """Failure detection in the fused chunk step without a fault: selection
+    row 3 is never marked ready, so its attention CTA's bounded wait runs
+    out; the error word names the fused step's row wait, that CTA writes
+    o = 0 / lse = -inf, the other rows are correct, and the next fused step on
+    the same context is correct everywhere."""
+    from block_sparse_long_xattn_gb300 import bsx_debug_fused_skip_row
+    P, Lq, S, tau = 512, 512, 8, 0.9
+    w = make_workload(seed=45, B=1, Hq=2, Hkv=1, d=128, Lk=P + Lq, q_start_pos=P,
+                      alpha=3.0, n_hot=1, dtype="bf16")
+    q, k, v = (to_dev(x, "bf16") for x in (w.q, w.k, w.v))
+    nqb, nkb = Lq // 128, (P + Lq) // 128
+    torch.cuda.synchronize()
+    assert bsx_last_error() == 0
+    bsx_debug_fused_skip_row(3)               # b 0, h 0, qb 3
+    mask, o, lse = bsx_chunk_prefill(q, k, v, P, S, tau)
+    torch.cuda.synchronize()                  # the launch ends: no hang, no fault
+    code = bsx_last_error()
+    assert code & 0x80000000
+    assert code & 0xFF == 3                   # the fused step's hand-over
+    assert (code >> 8) & 0xFF == 1            # an attention CTA's wait for its row
+    o_g, l_g = o.float().cpu().numpy(), lse.cpu().numpy()
+    assert np.all(o_g[0, 3 * 128:4 * 128, 0] == 0) and np.all(np.isneginf(l_g[0, 0, 384:512]))
+    m_g = mask.cpu().numpy()
+    o_ref, lse_ref = O.bsa_prefill(w.q, w.k, w.v, m_g, P, 0, nkb)
+    keep = np.ones(o_g.shape[:3], bool)
+    keep[0, 384:512, 0] = False
+    assert np.abs(o_g - o_ref)[keep].max() <= O_TOL["bf16"]
+    assert np.abs(l_g - lse_ref).transpose(0, 2, 1)[keep].max() <= LSE_TOL
+    mask, o, lse = bsx_chunk_prefill(q, k, v, P, S, tau)
+    torch.cuda.synchronize()
+    assert bsx_last_error() == 0
+    o_ref, lse_ref = O.bsa_prefill(w.q, w.k, w.v, mask.cpu().numpy(), P, 0, nkb)
+    assert np.abs(o.float().cpu().numpy() - o_ref).max() <= O_TOL["bf16"]
+    assert np.abs(lse.cpu().numpy() - lse_ref).max() <= LSE_TOL
+    assert nqb == 4
