@@ -51,7 +51,9 @@ DOMINANT = "bsa_prefill"
 # datasheet's dense bf16 figure for the whole GPU.
 MMA_FLOP_PER_CLK_SM = 8192
 DATASHEET_BF16_TFLOPS = 2250.0
-BSA_SOURCES = ("bsa_tc.cu", "bsa_simt.cu", "common.cuh", "tc_common.cuh")
+BSA_SOURCES = ("bsa_tc.cu", "bsa_tc.cuh", "bsa_simt.cu", "common.cuh", "tc_common.cuh")
+FUSED_SOURCES = ("fused_tc.cuh", "fused_tc.cu", "fused_d128_e2.cu", "estimate_tc.cuh", "bsa_tc.cuh",
+                 "common.cuh", "tc_common.cuh")
 
 
 def _env_rank():
@@ -79,7 +81,7 @@ def _source_sha(names):
     return h.hexdigest()[:16]
 
 
-def _traffic_per_launch(kernel_key):
+def _traffic_per_launch(kernel_key, sources=BSA_SOURCES):
     """DRAM bytes per launch of the dominant kernel from a committed ncu
     summary, or None when it is absent or was taken on different source."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -88,7 +90,7 @@ def _traffic_per_launch(kernel_key):
     with open(path) as f:
         t = json.load(f)
     e = t.get(kernel_key)
-    if not e or e.get("source_sha") != _source_sha(BSA_SOURCES):
+    if not e or e.get("source_sha") != _source_sha(sources):
         return None
     return e.get("bytes_per_launch_full")
 
@@ -411,8 +413,11 @@ def run_gpu(args):
     bsa_ms = float(np.mean([t_phase[n] for n in bsa_names]))        # mean launch
     bsa_flops_launch = float(np.mean([flops[n] for n in bsa_names]))
     achieved = bsa_flops_launch / (bsa_ms / 1e3) / 1e12
-    traffic = _traffic_per_launch("bsa_prefill") if args.step == "chunk" and \
-        args.workload == DEFAULT_WORKLOAD else None
+    traffic = None
+    if args.workload == DEFAULT_WORKLOAD and args.step == "chunk":
+        traffic = _traffic_per_launch("bsa_prefill")
+    elif args.workload == DEFAULT_WORKLOAD and "fused_step" in t_phase:
+        traffic = _traffic_per_launch("fused_step", FUSED_SOURCES)
     est_bytes = (dq.numel() + dk.numel()) * dq.element_size() + mask.numel()
 
     kernels = {f"{n}_ms": t for n, t in t_phase.items()}
