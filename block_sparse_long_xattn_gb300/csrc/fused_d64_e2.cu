@@ -17,8 +17,8 @@ cudaError_t launch_fused_d64_e2(const Problem& p, const void* q, const void* k,
       return launch_sde<8, 64, 2>(p, q, k, v, threshold, lse_part, ctl, ctl_bytes, mask, o,
                                     lse, err, skip_row, st);
     case 16:
-      return launch_sde<16, 64, 2>(p, q, k, v, threshold, lse_part, ctl, ctl_bytes, mask, o,
-                                     lse, err, skip_row, st);
+      return launch_sde<16, 64, 2>(p, q, k, v, threshold, lse_part, ctl, ctl_bytes, mask,
+                                     o, lse, err, skip_row, st);
     default:
       return cudaErrorInvalidValue;
   }

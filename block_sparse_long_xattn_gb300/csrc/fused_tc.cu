@@ -42,15 +42,10 @@ cudaError_t launch_fused_step(const Problem& p, const void* q, const void* k, co
                               unsigned* err, int skip_row, cudaStream_t st) {
   if (!fused_step_supported(p, stride)) return cudaErrorInvalidValue;
   const bool small = p.nkb <= 2 * fused::kSelThreads;  // rows of up to 256 key blocks
-  if (p.d == 64)
-    return small ? launch_fused_d64_e2(p, q, k, v, stride, threshold, lse_part, ctl, ctl_bytes,
-                                       mask, o, lse, err, skip_row, st)
-                 : launch_fused_d64_e8(p, q, k, v, stride, threshold, lse_part, ctl, ctl_bytes,
-                                       mask, o, lse, err, skip_row, st);
-  return small ? launch_fused_d128_e2(p, q, k, v, stride, threshold, lse_part, ctl, ctl_bytes,
-                                      mask, o, lse, err, skip_row, st)
-               : launch_fused_d128_e8(p, q, k, v, stride, threshold, lse_part, ctl, ctl_bytes,
-                                      mask, o, lse, err, skip_row, st);
+  auto launch = p.d == 64 ? (small ? launch_fused_d64_e2 : launch_fused_d64_e8)
+                          : (small ? launch_fused_d128_e2 : launch_fused_d128_e8);
+  return launch(p, q, k, v, stride, threshold, lse_part, ctl, ctl_bytes, mask, o, lse, err,
+                skip_row, st);
 }
 
 }  // namespace bsx
