@@ -760,7 +760,9 @@ def run_sparse(args):
     and 128K chunk shapes with a strong planted direction; the estimator
     selects about 6-50% of the causal blocks).  One JSON line per workload:
     the mask density, the step's tokens/s and its roofline fraction, the
-    attention launch's TFLOP/s over the selected blocks and its fractions.
+    attention launch's TFLOP/s over the selected blocks and its fractions,
+    and the fused step (bsx_chunk_prefill, one kernel) on the same inputs with
+    its fraction (estimate and attention flops over its time).
     Device-resident inputs, L2 flushed between timed steps."""
     import torch
 
@@ -828,6 +830,28 @@ def run_sparse(args):
         clocks = clk.summary()
         t = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(3)] for e in evs])
         t_est, t_bsa, t_rest = (float(x) for x in t.mean(axis=0))
+
+        # the fused step on the same inputs: bsx_chunk_prefill, one kernel
+        # (estimate, selection, attention over every key block; no merge)
+        wsf = torch.empty(bsx.bsx_chunk_prefill_workspace_bytes(bsx.shape_of(q, k), Lq, P, S),
+                          dtype=torch.uint8, device=dev)
+        maskf = torch.empty_like(mask)
+
+        def fused():
+            bsx.bsx_chunk_prefill(q, k, v, P, S, tau, mask=maskf, o=oh, lse=lh, workspace=wsf,
+                                  stream=stream)
+        for _ in range(args.warmup):
+            fused()
+        torch.cuda.synchronize()
+        fl_f = bsa_flops(maskf.cpu().numpy(), P, 0, nkb, d) + est_fl
+        ef = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.zero_()
+            ef[i][0].record(stream)
+            fused()
+            ef[i][1].record(stream)
+        torch.cuda.synchronize()
+        t_fused = float(np.mean([e[0].elapsed_time(e[1]) for e in ef]))
         ms = t_est + t_bsa + t_rest
         bsa_tf = fl / (t_bsa / 1e3) / 1e12
         roof_ms = (max(est_fl / (tc_peak * 1e12), est_bytes / (hbm_peak * 1e9))
@@ -843,9 +867,14 @@ def run_sparse(args):
             "bsa_frac_at_clock": bsa_tf / at_clock if at_clock else None,
             "estimate_ms": t_est, "estimate_tflops": est_fl / (t_est / 1e3) / 1e12,
             "estimate_tc_frac": est_fl / (t_est / 1e3) / 1e12 / tc_peak,
-            "merge_map_ms": t_rest, "steps": args.steps, "warmup": args.warmup,
+            "merge_map_ms": t_rest,
+            "fused_step": {"ms": t_fused, "tokens_per_s_layer": B * Lq / (t_fused / 1e3),
+                           "flops": fl_f, "frac": fl_f / (t_fused / 1e3) / 1e12 / tc_peak,
+                           "frac_at_clock": (fl_f / (t_fused / 1e3) / 1e12 / at_clock
+                                             if at_clock else None)},
+            "steps": args.steps, "warmup": args.warmup,
             "peak_source": peak_src, "clocks": clocks}), flush=True)
-        del q, k, v, ws, oh, oc
+        del q, k, v, ws, wsf, oh, oc
         torch.cuda.empty_cache()
     if bsx.bsx_last_error() != 0:
         raise SystemExit("device error word set after the sparse runs")
