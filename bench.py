@@ -276,8 +276,22 @@ def run_gpu(args):
     def merge_only(q, k, v):
         bsx.bsx_merge_attn(oh, lh, oc, lc, stream=stream)
 
+    one_kernel = w.dtype == "bf16" and nkb <= 1024 and not e4m3
     # phases of one step, timed separately; the BSA phases give the roofline
-    if args.step == "chunk":
+    if args.step == "chunk_kernel" and one_kernel:
+        # bsx_chunk_step: estimate, selection, attention on the history and
+        # on the current chunk, merge and CPU-block flags in one kernel
+        wsc = torch.empty(bsx.bsx_chunk_prefill_workspace_bytes(bsx.shape_of(dq, dk), Lq, P, S),
+                          dtype=torch.uint8, device=dev)
+
+        def chunk_step(q, k, v):
+            bsx.bsx_chunk_step(q, k, v, P, S, tau, cpu_block_tokens=cpu_tokens, mask=mask,
+                               o=oh, lse=lh, o_curr=oc, lse_curr=lc,
+                               keep=keep if P >= cpu_tokens else None, workspace=wsc,
+                               stream=stream)
+        phases = [("chunk_step", chunk_step)]
+        launches = 1
+    elif args.step in ("chunk", "chunk_kernel"):
         phases = [("estimate", est), ("bsa_split", bsa_split(mask)), ("merge_map", merge_map)]
         launches = 5
     elif args.step in ("fused", "prefill") and not e4m3:
@@ -290,7 +304,7 @@ def run_gpu(args):
             bsx.bsx_chunk_prefill(q, k, v, P, S, tau, mask=mask, o=oh, lse=lh, workspace=wsf,
                                   stream=stream)
         phases = [("fused_step", fused_step)]
-        launches = 1 if (w.dtype == "bf16" and nkb <= 1024) else 3
+        launches = 1 if one_kernel else 3
     elif args.step in ("fused", "prefill"):
         # e4m3 estimator operands: the estimate and one attention launch
         phases = [("estimate", est), ("bsa_all", bsa(mask, 0, nkb, oh, lh))]
@@ -323,12 +337,13 @@ def run_gpu(args):
     if e4m3:
         launches += 2   # the two quantize launches of each step
     ranges = {"bsa_split": ((0, cur), (cur, nkb)), "bsa_all": ((0, nkb),),
-              "fused_step": ((0, nkb),)}
+              "fused_step": ((0, nkb),), "chunk_step": ((0, cur), (cur, nkb))}
     flops = {n: sum(bsa_flops(bsa_mask, P, r0, r1, d) for r0, r1 in ranges[n])
              for n, _ in phases if n in ranges}
     est_fl = estimate_flops(cfg, Lq, P, S)
-    if "fused_step" in flops:   # one kernel: the estimate's MMAs and the attention's
-        flops["fused_step"] += est_fl
+    for n in ("fused_step", "chunk_step"):   # one kernel: the estimate's MMAs and the attention's
+        if n in flops:
+            flops[n] += est_fl
 
     np_ = len(phases)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(np_ + 1)]
@@ -414,7 +429,9 @@ def run_gpu(args):
     bsa_flops_launch = float(np.mean([flops[n] for n in bsa_names]))
     achieved = bsa_flops_launch / (bsa_ms / 1e3) / 1e12
     traffic = None
-    if args.workload == DEFAULT_WORKLOAD and args.step == "chunk":
+    if args.workload == DEFAULT_WORKLOAD and "chunk_step" in t_phase:
+        traffic = _traffic_per_launch("chunk_step", FUSED_SOURCES)
+    elif args.workload == DEFAULT_WORKLOAD and "bsa_split" in t_phase:
         traffic = _traffic_per_launch("bsa_prefill")
     elif args.workload == DEFAULT_WORKLOAD and "fused_step" in t_phase:
         traffic = _traffic_per_launch("fused_step", FUSED_SOURCES)
@@ -442,9 +459,9 @@ def run_gpu(args):
         roof_ms["estimate"] = max(est_fl / (tc_peak * 1e12), est_bytes / (hbm_peak * 1e9)) * 1e3
     for n in bsa_names:
         roof_ms[n] = flops[n] / (tc_peak * 1e12) * 1e3
-    if "merge_map" in t_phase or "merge" in t_phase:
+    if "merge_map" in t_phase or "merge" in t_phase or "chunk_step" in t_phase:
         roof_ms["merge"] = merge_bytes / (hbm_peak * 1e9) * 1e3
-    if "merge_map" in t_phase and P >= cpu_tokens:
+    if ("merge_map" in t_phase or "chunk_step" in t_phase) and P >= cpu_tokens:
         roof_ms["map"] = mask.numel() / (hbm_peak * 1e9) * 1e3
     if "cpu_blocks" in t_phase:
         roof_ms["cpu_blocks"] = 2 * mask.numel() / (hbm_peak * 1e9) * 1e3
@@ -459,7 +476,8 @@ def run_gpu(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic (seeded planted-direction N(0,1) inputs)",
         "config": config_dict(args, world),
-        "roofline": {"kernel": "fused_step" if "fused_step" in t_phase else DOMINANT,
+        "roofline": {"kernel": next((n for n in ("chunk_step", "fused_step") if n in t_phase),
+                                    DOMINANT),
                      "bound": "tensor", "achieved": achieved,
                      "peak": tc_peak, "unit": "TFLOP/s", "frac": achieved / tc_peak,
                      "traffic": traffic, "peak_source": peak_src,
@@ -998,9 +1016,10 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(CONFIGS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--step", default="chunk",
-                    choices=["chunk", "fused", "offload", "prefill", "chunked"],
+                    choices=["chunk", "chunk_kernel", "fused", "offload", "prefill", "chunked"],
                     help="chunk: estimate, BSA on history and current chunk, merge, map "
-                         "(the default); fused: bsx_chunk_prefill, estimate, selection "
+                         "(the default); chunk_kernel: the same step as one kernel "
+                         "(bsx_chunk_step); fused: bsx_chunk_prefill, estimate, selection "
                          "and attention over all key blocks in one kernel; offload: the pages' CPU-block-dense history; prefill: "
                          "fused on a whole-sequence workload; chunked: the chunk step on "
                          "every chunk of a whole sequence in order (64K in 16 chunks)")

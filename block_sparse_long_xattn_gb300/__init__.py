@@ -19,6 +19,7 @@ from ._lib import (  # noqa: F401
     bsx_bsa_prefill_split,
     bsx_chunk_prefill,
     bsx_chunk_prefill_workspace_bytes,
+    bsx_chunk_step,
     bsx_chunk_step_host,
     bsx_cpu_block_mask,
     bsx_debug_drop_ring_item,

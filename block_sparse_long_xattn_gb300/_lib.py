@@ -28,7 +28,7 @@ EXPORTS = ("bsx_version", "bsx_status_string", "bsx_estimate_workspace_bytes",
            "bsx_xattn_estimate_noalloc",
            "bsx_cpu_block_mask", "bsx_chunk_prefill", "bsx_bsa_prefill_split",
            "bsx_quantize_e4m3", "bsx_chunk_step_host", "bsx_debug_drop_ring_item",
-           "bsx_chunk_prefill_workspace_bytes", "bsx_debug_fused_skip_row")
+           "bsx_chunk_prefill_workspace_bytes", "bsx_debug_fused_skip_row", "bsx_chunk_step")
 BSX_STEP_OFFLOAD, BSX_STEP_E4M3_ESTIMATE, BSX_STEP_FUSED = 2, 4, 8
 
 
@@ -90,6 +90,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.bsx_merge_attn.argtypes = [BsxShape, i32, vp, vp, vp, vp, vp]
         lib.bsx_map_mask_to_cpu_blocks.restype = i32
         lib.bsx_map_mask_to_cpu_blocks.argtypes = [BsxShape, vp, i32, i32, i32, i32, vp, vp]
+        lib.bsx_chunk_step.restype = i32
+        lib.bsx_chunk_step.argtypes = [BsxShape, vp, vp, vp, i32, i32, i32, f32, i32, vp, vp, vp,
+                                       vp, vp, vp, vp, sz, vp]
         lib.bsx_chunk_prefill_workspace_bytes.restype = sz
         lib.bsx_chunk_prefill_workspace_bytes.argtypes = [BsxShape, i32, i32, i32]
         lib.bsx_chunk_prefill.restype = i32
@@ -276,6 +279,43 @@ def bsx_chunk_prefill(q, k, v, q_start_pos: int, stride: int, threshold: float, 
     return mask, o, lse
 
 
+def bsx_chunk_step(q, k, v, q_start_pos: int, stride: int, threshold: float, *,
+                   cpu_block_tokens: int = 1024, mask=None, o=None, lse=None, o_curr=None,
+                   lse_curr=None, keep=None, with_keep: bool = True, workspace=None,
+                   stream=None):
+    """The chunk step (estimate, attention on history and current chunk, LSE
+    merge, CPU-block flags) -> (mask, o, lse, keep); keep is None when there
+    is no history CPU block or with_keep is False.  o_curr / lse_curr are
+    scratch."""
+    lib = load()
+    B, q_len, Hq, _ = q.shape
+    Lk = k.shape[1]
+    shape = shape_of(q, k)
+    dev = q.device
+    if mask is None:
+        mask = torch.empty((B, Hq, q_len // 128, Lk // 128), dtype=torch.uint8, device=dev)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, q_len), dtype=torch.float32, device=dev)
+    if o_curr is None:
+        o_curr = torch.empty_like(q)
+    if lse_curr is None:
+        lse_curr = torch.empty((B, Hq, q_len), dtype=torch.float32, device=dev)
+    n_cpu = q_start_pos // cpu_block_tokens
+    if keep is None and with_keep and n_cpu > 0:
+        keep = torch.empty((B, n_cpu), dtype=torch.uint8, device=dev)
+    need = lib.bsx_chunk_prefill_workspace_bytes(shape, q_len, q_start_pos, stride)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    _check("bsx_chunk_step", lib.bsx_chunk_step(
+        shape, _ptr(q), _ptr(k), _ptr(v), q_len, q_start_pos, stride, float(threshold),
+        cpu_block_tokens, _ptr(mask), _ptr(o), _ptr(lse), _ptr(o_curr), _ptr(lse_curr),
+        _ptr(keep), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+    return mask, o, lse, keep
+
+
 def bsx_merge_attn(o1, lse1, o2, lse2, *, stream=None):
     """In-place LSE merge of (o2, lse2) into (o1, lse1); returns (o1, lse1)."""
     lib = load()
@@ -360,10 +400,9 @@ def make_chunk_buffers(q_host, k_host, q_start_pos: int, stride: int,
     u8 = torch.uint8
     n_cpu = q_start_pos // cpu_block_tokens
     shape = BsxShape(B, Hq, Hkv, d, _dtype_code(q_host))
-    need = load().bsx_estimate_workspace_bytes(shape, q_len, q_start_pos, stride)
-    if fused:  # the step may run as one fused kernel: room for its control block
-        need = max(need, load().bsx_chunk_prefill_workspace_bytes(shape, q_len, q_start_pos,
-                                                                  stride))
+    # the step may run as one fused kernel: room for its control block
+    need = max(load().bsx_estimate_workspace_bytes(shape, q_len, q_start_pos, stride),
+               load().bsx_chunk_prefill_workspace_bytes(shape, q_len, q_start_pos, stride))
     mshape = (B, Hq, q_len // 128, Lk // 128)
     return {
         "q": torch.empty(q_host.shape, dtype=dt, device=device),

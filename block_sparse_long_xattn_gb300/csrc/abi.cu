@@ -255,15 +255,70 @@ int bsx_chunk_prefill(bsx_shape s, const void* q, const void* k, const void* v, 
     unsigned* ctl = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + off);
     const int skip = t_skip_row;
     t_skip_row = -1;
+    const bsx::FusedOut out{mask, o, lse, nullptr, nullptr, nullptr, 0};
     return cuda_status(bsx::launch_fused_step(p, q, k, v, stride, threshold,
                                               static_cast<float*>(workspace), ctl, need - off,
-                                              mask, o, lse, err_word(), skip,
+                                              out, err_word(), skip,
                                               static_cast<cudaStream_t>(stream)));
   }
   rc = bsx_xattn_estimate(s, q, k, q_len, q_start_pos, stride, threshold, mask, nullptr,
                           workspace, workspace_bytes, stream);
   if (rc != BSX_OK) return rc;
   return bsx_bsa_prefill(s, q, k, v, mask, q_len, q_start_pos, 0, p.nkb, o, lse, stream);
+}
+
+int bsx_chunk_step(bsx_shape s, const void* q, const void* k, const void* v, int q_len,
+                   int q_start_pos, int stride, float threshold, int cpu_block_tokens,
+                   uint8_t* mask, void* o, float* lse, void* o_curr, float* lse_curr,
+                   uint8_t* keep, void* workspace, size_t workspace_bytes, void* stream) {
+  // validate everything before the first launch, so nothing is enqueued on error
+  bsx::Problem p;
+  int rc = make_problem(s, q_len, q_start_pos, &p);
+  if (rc != BSX_OK) return rc;
+  if (stride != 4 && stride != 8 && stride != 16) return BSX_ERR_UNSUPPORTED;
+  if (!(threshold > 0.0f) || isnan(threshold)) return BSX_ERR_INVALID_ARG;
+  if (!q || !k || !v || !mask || !o || !lse || !o_curr || !lse_curr) return BSX_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(o_curr) || !aligned16(lse_curr))
+    return BSX_ERR_INVALID_ARG;
+  const int cur = q_start_pos / 128;
+  if (cur > kMaxKeyBlocks || p.nkb - cur > kMaxKeyBlocks) return BSX_ERR_UNSUPPORTED;
+  const bool map = keep != nullptr && q_start_pos >= cpu_block_tokens;
+  if (keep && (cpu_block_tokens < 128 || cpu_block_tokens % 128 != 0 ||
+               q_start_pos % cpu_block_tokens != 0))
+    return BSX_ERR_INVALID_ARG;
+  const size_t need = bsx_chunk_prefill_workspace_bytes(s, q_len, q_start_pos, stride);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return BSX_ERR_WORKSPACE;
+  if (bsx::fused_step_supported(p, stride)) {
+    // one kernel: estimate, selection (and the CPU-block flags), attention on
+    // the history and on the current chunk, merge
+    const size_t off = round_up_256(bsx_estimate_workspace_bytes(s, q_len, q_start_pos, stride));
+    unsigned* ctl = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + off);
+    const int skip = t_skip_row;
+    t_skip_row = -1;
+    // with no history (q_start_pos 0) the step is the current chunk alone
+    const bsx::FusedOut out{mask,
+                            o,
+                            lse,
+                            q_start_pos > 0 ? o_curr : nullptr,
+                            q_start_pos > 0 ? lse_curr : nullptr,
+                            map ? keep : nullptr,
+                            cpu_block_tokens};
+    return cuda_status(bsx::launch_fused_step(p, q, k, v, stride, threshold,
+                                              static_cast<float*>(workspace), ctl, need - off,
+                                              out, err_word(), skip,
+                                              static_cast<cudaStream_t>(stream)));
+  }
+  rc = bsx_xattn_estimate(s, q, k, q_len, q_start_pos, stride, threshold, mask, nullptr,
+                          workspace, workspace_bytes, stream);
+  if (rc == BSX_OK)
+    rc = bsx_bsa_prefill_split(s, q, k, v, mask, q_len, q_start_pos, o, lse, o_curr, lse_curr,
+                               stream);
+  if (rc == BSX_OK) rc = bsx_merge_attn(s, q_len, o, lse, o_curr, lse_curr, stream);
+  if (rc == BSX_OK && map)
+    rc = bsx_map_mask_to_cpu_blocks(s, mask, q_len, q_start_pos, cpu_block_tokens, 0, keep,
+                                    stream);
+  return rc;
 }
 
 int bsx_cpu_block_mask(bsx_shape s, const uint8_t* keep, int q_len, int q_start_pos,

@@ -106,11 +106,26 @@ struct BsaTile {
   int drop_item;
   const unsigned* ready;
   unsigned* gabort;
+  // (fused chunk step) two key ranges of the same query tile, merged by LSE
+  // into dest_o / dest_lse (through tm_dest): the CTA whose range finishes
+  // first writes its own (o, lse) and then sets *my_ready; the second merges
+  // the first's result (other_o, other_lse, once *other_ready is set) with
+  // its own.  *mcnt counts the tile's finished ranges.  mcnt == nullptr: no
+  // merge.
+  unsigned* mcnt;
+  unsigned* my_ready;
+  const unsigned* other_ready;
+  const __nv_bfloat16* other_o;
+  const float* other_lse;
+  __nv_bfloat16* dest_o;
+  float* dest_lse;
+  const CUtensorMap* tm_dest;
   __device__ __forceinline__ bool ready_wait(unsigned* err) const;
 };
 
-constexpr unsigned kSiteRowReady = 1;   // kErrFused sites
+constexpr unsigned kSiteRowReady = 1;   // kErrFused sites (3: the workers' tile-id ring)
 constexpr unsigned kSiteTilesDone = 2;
+constexpr unsigned kSiteMergeReady = 4;
 
 __device__ __forceinline__ bool BsaTile::ready_wait(unsigned* err) const {
   return wait_counter(ready, 1u, gabort, err, kErrFused, kSiteRowReady);
@@ -125,6 +140,7 @@ __device__ __forceinline__ void bsa_cta(const BsaArgs& a, const BsaTile& tile, u
   int* n_sm = reinterpret_cast<int*>(smem + L::kMisc + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 8);
   volatile int* row_bad = reinterpret_cast<volatile int*>(smem + L::kMisc + 12);
+  volatile int* merge_dec = reinterpret_cast<volatile int*>(smem + L::kMisc + 16);
 
   // barrier addresses
   const uint32_t bar0 = smem_u32(bars);
@@ -237,6 +253,16 @@ __device__ __forceinline__ void bsa_cta(const BsaArgs& a, const BsaTile& tile, u
     for (int r = tid; r < 128; r += kThreads)
       lse[((long long)b * Hq + h) * q_len + qb * 128 + r] = -INFINITY;
     if (tid == 0) drain_wait(q_full, 0);  // the early Q copy lands before the CTA exits
+    if (tile.mcnt) {
+      // (merge) an empty range counts as finished first: both ranges of an
+      // estimator's mask hold a forced block, so only a failed wait gets here
+      __syncthreads();
+      if (tid == 0) {
+        atomicAdd(tile.mcnt, 1u);
+        __threadfence();
+        st_release_gpu(tile.my_ready, 1u);
+      }
+    }
   } else if (warp == 0) {
     // ------------------------------ producer ------------------------------
     if (lane == 0) {
@@ -480,8 +506,19 @@ __device__ __forceinline__ void bsa_cta(const BsaArgs& a, const BsaTile& tile, u
         !mbar_wait_warp(o_done(grp), (j_last >> 1) & 1, abort_flag, err, kErrBsaTc,
                         kSiteODoneFinal))
       ok = false;
+    // (merge) one thread counts this range finished; the second range to
+    // finish waits until the first one's result is visible, then merges
+    if (tile.mcnt && tid == 64) {
+      int d = 1;  // first: write this range's own result
+      if (atomicAdd(tile.mcnt, 1u) != 0u)
+        d = wait_counter(tile.other_ready, 1u, tile.gabort, err, kErrFused, kSiteMergeReady)
+                ? 2   // second: merge
+                : 1;  // the first never became visible (its error is recorded)
+      *merge_dec = d;
+    }
     mbar_arrive(xbar);
     if (!mbar_wait_warp(xbar, 0, abort_flag, err, kErrBsaTc, kSiteXchg)) ok = false;
+    const int dec = tile.mcnt ? *merge_dec : 0;
     if (ok) {
       tc_fence_after();
       const float m0 = xm[0 * 128 + row], l0 = xm[1 * 128 + row];
@@ -495,11 +532,28 @@ __device__ __forceinline__ void bsa_cta(const BsaArgs& a, const BsaTile& tile, u
       const float l = l0 * w0 + l1 * w1;
       const float inv = 1.f / l;
       const float f0 = w0 * inv, f1 = w1 * inv;
+      // this row's LSE as a range stores it (natural log)
+      const float lse_own = (m + __log2f(l)) * 0.69314718055994531f;
+      float lse_out = lse_own;
+      const long long orow = (((long long)b * q_len + qb * 128 + row) * Hq + h) * D;
+      const long long lrow = ((long long)b * Hq + h) * q_len + qb * 128 + row;
+      // (merge, second range) the two ranges' results exactly as stored --
+      // bf16 O and fp32 LSE, the history's first -- merged as the stand-alone
+      // merge does, so the result does not depend on which range finished
+      // second and equals the separate launches' bit for bit
+      const bool hist = o == tile.dest_o;  // this range is the history
+      MergeWeights mw{0.f, 0.f, -INFINITY};
+      if (dec == 2) {
+        const float lo = __ldcg(tile.other_lse + lrow);
+        mw = hist ? merge_weights(lse_own, lo) : merge_weights(lo, lse_own);
+        lse_out = mw.lse;
+      }
       // This group writes output columns [grp * D/2, grp * D/2 + D/2) of its
       // row into the Q buffer (every MMA is complete), in the 128-byte
       // swizzled layout of the tensor map's box: feature f of row r sits in
       // region f / 64, 16-byte chunk ((f % 64) / 8) ^ (r % 8) of the row's
-      // 128 bytes.  One TMA store then writes the tile.
+      // 128 bytes.  One TMA store then writes the tile.  (A first range of a
+      // merge writes its row straight to global memory instead.)
       uint8_t* stage = smem + L::kQ;
 #pragma unroll
       for (int cc = 0; cc < D / 64; ++cc) {
@@ -513,6 +567,40 @@ __device__ __forceinline__ void bsa_cta(const BsaArgs& a, const BsaTile& tile, u
         } else {
 #pragma unroll
           for (int e = 0; e < 32; ++e) t0[e] *= f0;
+        }
+        if (dec == 2) {
+          const uint4* xr = reinterpret_cast<const uint4*>(tile.other_o + orow + col);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const uint4 u = __ldcg(xr + q4);
+            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 xv =
+                  __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[e]));
+              const int i0 = q4 * 8 + 2 * e;
+              // this range's value as it would be stored (bf16)
+              const float2 ov = __bfloat1622float2(__floats2bfloat162_rn(t0[i0], t0[i0 + 1]));
+              t0[i0] = hist ? merge_element(mw, ov.x, xv.x) : merge_element(mw, xv.x, ov.x);
+              t0[i0 + 1] = hist ? merge_element(mw, ov.y, xv.y) : merge_element(mw, xv.y, ov.y);
+            }
+          }
+        }
+        if (dec == 1) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            uint4 pk4;
+            __nv_bfloat162 a0 = __floats2bfloat162_rn(t0[e + 0], t0[e + 1]);
+            __nv_bfloat162 a1 = __floats2bfloat162_rn(t0[e + 2], t0[e + 3]);
+            __nv_bfloat162 a2 = __floats2bfloat162_rn(t0[e + 4], t0[e + 5]);
+            __nv_bfloat162 a3 = __floats2bfloat162_rn(t0[e + 6], t0[e + 7]);
+            pk4.x = *reinterpret_cast<uint32_t*>(&a0);
+            pk4.y = *reinterpret_cast<uint32_t*>(&a1);
+            pk4.z = *reinterpret_cast<uint32_t*>(&a2);
+            pk4.w = *reinterpret_cast<uint32_t*>(&a3);
+            reinterpret_cast<uint4*>(o + orow + col)[e / 8] = pk4;
+          }
+          continue;
         }
 #pragma unroll
         for (int e = 0; e < 32; e += 8) {
@@ -530,22 +618,27 @@ __device__ __forceinline__ void bsa_cta(const BsaArgs& a, const BsaTile& tile, u
                                     ((((f & 63) >> 3) ^ (row & 7)) << 4)) = pk4;
         }
       }
-      if (grp == 0)
-        lse[((long long)b * Hq + h) * q_len + qb * 128 + row] =
-            (m + __log2f(l)) * 0.69314718055994531f;
+      if (grp == 0) (dec == 2 ? tile.dest_lse : lse)[lrow] = lse_out;
     }
     // the staged tile is visible to the async proxy once every softmax
     // thread has arrived; one thread stores it and waits until the copy has
-    // read shared memory (the CTA's shared memory must outlive the read)
+    // read shared memory (the CTA's shared memory must outlive the read).
+    // (A first range of a merge: every softmax thread has written its row;
+    // the thread makes the rows visible GPU-wide, then marks them ready.)
     fence_proxy_async_smem();
     mbar_arrive(stage_full);
     if (tid == 64 && ok &&
         mbar_wait(stage_full, 0, abort_flag, err, kErrBsaTc, kSiteStage)) {
-      const CUtensorMap* tmo = tile.tm_o;
-      for (int r = 0; r < L::kRegions; ++r)
-        tma_store_4d(tmo, sb + L::kQ + r * kRegion, r * 64, h, qb * 128, b);
-      bulk_commit_group();
-      bulk_wait_group_read0();
+      if (dec == 1) {
+        __threadfence();
+        st_release_gpu(tile.my_ready, 1u);
+      } else {
+        const CUtensorMap* tmo = dec == 2 ? tile.tm_dest : tile.tm_o;
+        for (int r = 0; r < L::kRegions; ++r)
+          tma_store_4d(tmo, sb + L::kQ + r * kRegion, r * 64, h, qb * 128, b);
+        bulk_commit_group();
+        bulk_wait_group_read0();
+      }
     }
   }
 

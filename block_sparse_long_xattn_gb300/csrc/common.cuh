@@ -63,6 +63,31 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return fmaxf(fmaxf(a, b), c);
 }
 
+// LSE merge of two normalised partial attentions (nano-vllm optimization
+// guide, "Online Softmax Merge"): the weights of (o1, o2) and the merged LSE
+// from (lse1, lse2), and one merged element.  Written once with explicit
+// rounding so that every kernel that merges produces the same bits.
+struct MergeWeights {
+  float w1, w2, lse;
+};
+__device__ __forceinline__ MergeWeights merge_weights(float l1, float l2) {
+  const float m = fmaxf(l1, l2);
+  MergeWeights r{0.f, 0.f, -INFINITY};
+  if (m != -INFINITY) {
+    r.w1 = __expf(l1 - m);  // exp(-inf) = 0 for an empty partial
+    r.w2 = __expf(l2 - m);
+    const float den = __fadd_rn(r.w1, r.w2);
+    r.lse = __fadd_rn(m, __logf(den));
+    const float inv = __frcp_rn(den);
+    r.w1 = __fmul_rn(r.w1, inv);
+    r.w2 = __fmul_rn(r.w2, inv);
+  }
+  return r;
+}
+__device__ __forceinline__ float merge_element(const MergeWeights& w, float a, float c) {
+  return __fmaf_rn(w.w1, a, __fmul_rn(w.w2, c));
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

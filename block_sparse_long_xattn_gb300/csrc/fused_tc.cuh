@@ -24,7 +24,13 @@
 //                    idle stage ring is their scratch).
 //   tickets [W, W+n) one attention CTA per (b, h, qb), in the order of the
 //                    stand-alone attention kernel; it waits for its row's
-//                    ready flag before its first read of the mask.
+//                    ready flag before its first read of the mask.  As the
+//                    pages' chunk step (two ranges): n = 2 B Hq nqb, the
+//                    history CTAs (key blocks below q_start_pos/128) then the
+//                    current-chunk CTAs; of a query tile's two, the one that
+//                    finishes second merges the other's (O, LSE) with its
+//                    own by LSE (bsa_tc.cuh), and the selection also writes
+//                    the CPU-block keep flags of each row's history blocks.
 // Every wait points at work held by a smaller ticket, or at work that a
 // running worker will take: a CTA with a ticket has started, a worker never
 // waits on an attention CTA, and workers keep taking estimate tiles while any
@@ -53,7 +59,8 @@ constexpr int kSelThreads = 128;         // a selection group: four warps
 constexpr int kSelWarps = kSelThreads / 32;
 
 // control block: [0] ticket, [1] next estimate tile, [2] next selection row,
-// [3] abort, then tiles_done[B*Hq*n_rt], then row_ready[B*Hq*nqb] (zeroed
+// [3] abort, then tiles_done[B*Hq*n_rt], row_ready[n_rows], merge counts
+// [n_rows] and range ready flags [2][n_rows] (n_rows = B*Hq*nqb; all zeroed
 // before each launch); then, 256-byte aligned, tile_lse[B*Hq][n_ktm][R]
 // (every value read is written first in the same launch)
 constexpr int kCtlHead = 4;
@@ -86,15 +93,16 @@ struct FusedParams {
   float* tile_lse;  // [b][h][kt][i]: each row's log-sum-exp over one key tile
   int n_ktm;        // key tiles of the last row tile (the most any row tile has)
   uint8_t* mask;
-  __nv_bfloat16* o;
+  __nv_bfloat16* o;  // the result (with two ranges: the history's, then the merged)
   float* lse;
+  int nparts;        // 1: one range over every key block; 2: history + current chunk
+  __nv_bfloat16* o2;  // two ranges: the current chunk's (O, LSE), merge scratch
+  float* lse2;
+  uint8_t* keep;     // CPU-block keep flags [B][n_cpu], or nullptr
+  int n_cpu, cpu_kb;  // CPU blocks of the history, key blocks per CPU block
   unsigned* ctl;
   unsigned* err;
 };
-
-__device__ __forceinline__ void st_release_gpu(unsigned* p, unsigned v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 
 // One selection row on a group of 128 threads (stid = 0..127, synchronised
 // by named barrier `bar`), from the estimate partials lse_part[kb][r] of the
@@ -366,11 +374,24 @@ __device__ __forceinline__ void select_rows(const FusedParams& P, uint8_t* sm, i
       const int rt = qb * RB / est::kM;
       const float* base = P.lse_part + (long long)r * P.nkb * RB;
       const float* tl = P.tile_lse + (long long)bh * P.n_ktm * T.R + qb * RB;
+      uint8_t* mrow = P.mask + ((long long)bh * P.nqb + qb) * P.nkb;
       select_row<RB, E>(base, tl, est::key_tiles(T, rt), T.R, P.nkb, P.cur + qb, P.threshold,
-                        P.mask + ((long long)bh * P.nqb + qb) * P.nkb, sm, stid, bar);
+                        mrow, sm, stid, bar);
       // the row's mask is written; one thread makes it visible GPU-wide and
       // then marks the row ready
       named_barrier_sync(bar, kSelThreads);
+      if (P.keep) {
+        // the CPU-block map (xattn_bsa.py select_blocks Step 6): a history
+        // CPU block is kept when any of its key blocks is selected in any
+        // row; every row sets the flags of its own blocks (the same value
+        // from every writer; the flags are zeroed before the launch)
+        const int b = bh / P.Hq;
+        for (int c = stid; c < P.n_cpu; c += kSelThreads) {
+          bool any = false;
+          for (int u = 0; u < P.cpu_kb; ++u) any = any || mrow[c * P.cpu_kb + u] != 0;
+          if (any) P.keep[(long long)b * P.n_cpu + c] = 1;
+        }
+      }
       if (stid == 0) {
         __threadfence();
         if (r != P.skip_row) st_release_gpu(row_ready + r, 1u);
@@ -510,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(
     const __grid_constant__ CUtensorMap tm_qe, const __grid_constant__ CUtensorMap tm_ke,
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-    const FusedParams P) {
+    const __grid_constant__ CUtensorMap tm_o2, const FusedParams P) {
   __shared__ int s_ticket;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -522,30 +543,51 @@ __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(
     worker<S, D, E>(P, &tm_qe, &tm_ke, smem);
     return;
   }
-  // attention CTA u: the order of the stand-alone attention kernel (batch,
-  // heads, query tiles last-first), which is also the order in which the
-  // workers finish the rows of the early heads
-  const int u = ticket - P.n_workers;
+  // attention CTA u: range 0 first, then batch, heads and query tiles
+  // last-first (the order of the stand-alone attention kernel), which is also
+  // the order in which the workers finish the rows of the early heads
+  const int u0 = ticket - P.n_workers;
+  const int part = u0 / P.n_rows;
+  const int u = u0 - part * P.n_rows;
   const int nqb = P.nqb;
   const int b = u / (nqb * P.Hq);
   const int r2 = u - b * (nqb * P.Hq);
   const int h = r2 / nqb;
   const int qb = nqb - 1 - (r2 - h * nqb);
+  const int r = (b * P.Hq + h) * nqb + qb;
   unsigned* row_ready = P.ctl + kCtlHead + P.B * P.Hq * P.T.n_rt;
+  unsigned* mcnt = row_ready + P.n_rows;
+  unsigned* part_ready = mcnt + P.n_rows;  // [2][n_rows]
   const bsa::BsaArgs a{&tm_q, &tm_k, &tm_v, P.mask, P.q_len, P.Lk, P.Hq, P.Hkv,
                        nqb,   P.cur, P.scale_bsa, P.err};
-  const bsa::BsaTile tile{b,        h,     qb, 0, P.nkb, P.o, P.lse, &tm_o, false, -1,
-                          row_ready + (b * P.Hq + h) * nqb + qb, P.ctl + 3};
+  bsa::BsaTile tile{b, h, qb, 0, P.nkb, P.o, P.lse, &tm_o, false, -1, row_ready + r, P.ctl + 3};
+  if (P.nparts == 2) {
+    tile.kb_begin = part ? P.cur : 0;
+    tile.kb_end = part ? P.nkb : P.cur;
+    if (part) {
+      tile.o = P.o2;
+      tile.lse = P.lse2;
+      tile.tm_o = &tm_o2;
+    }
+    tile.mcnt = mcnt + r;
+    tile.my_ready = part_ready + part * P.n_rows + r;
+    tile.other_ready = part_ready + (1 - part) * P.n_rows + r;
+    tile.other_o = part ? P.o : P.o2;
+    tile.other_lse = part ? P.lse : P.lse2;
+    tile.dest_o = P.o;
+    tile.dest_lse = P.lse;
+    tile.tm_dest = &tm_o;
+  }
   bsa::bsa_cta<D, true>(a, tile, smem);
 }
 
 template <int S, int D, int E>
 cudaError_t launch_sde(const Problem& p, const void* q, const void* k, const void* v,
                        float threshold, float* lse_part, unsigned* ctl, size_t ctl_bytes,
-                       uint8_t* mask, void* o, float* lse, unsigned* err, int skip_row,
-                       cudaStream_t st) {
+                       const FusedOut& out, unsigned* err, int skip_row, cudaStream_t st) {
   const int R = p.q_len / S, Ck = p.Lk / S;
-  CUtensorMap mqe, mke, mq, mk, mv, mo;
+  const bool split = out.o_curr != nullptr;
+  CUtensorMap mqe, mke, mq, mk, mv, mo, mo2;
   {  // the estimator's 5-D views (features, head, phase, reshaped row, batch)
     const uint64_t dims[5] = {(uint64_t)D, (uint64_t)p.Hq, (uint64_t)S, (uint64_t)R,
                               (uint64_t)p.B};
@@ -568,7 +610,9 @@ cudaError_t launch_sde(const Problem& p, const void* q, const void* k, const voi
     const uint64_t sq[3] = {(uint64_t)D * 2, (uint64_t)p.Hq * D * 2,
                             (uint64_t)p.q_len * p.Hq * D * 2};
     if (!encode_tmap_bf16(&mq, q, 4, dq, sq, box)) return cudaErrorInvalidValue;
-    if (!encode_tmap_bf16(&mo, o, 4, dq, sq, box)) return cudaErrorInvalidValue;
+    if (!encode_tmap_bf16(&mo, out.o, 4, dq, sq, box)) return cudaErrorInvalidValue;
+    if (!encode_tmap_bf16(&mo2, split ? out.o_curr : out.o, 4, dq, sq, box))
+      return cudaErrorInvalidValue;
     const uint64_t dk[4] = {(uint64_t)D, (uint64_t)p.Hkv, (uint64_t)p.Lk, (uint64_t)p.B};
     const uint64_t sk[3] = {(uint64_t)D * 2, (uint64_t)p.Hkv * D * 2,
                             (uint64_t)p.Lk * p.Hkv * D * 2};
@@ -597,9 +641,15 @@ cudaError_t launch_sde(const Problem& p, const void* q, const void* k, const voi
   P.scale_bsa = 1.4426950408889634f / sqrtf((float)D);
   P.threshold = threshold;
   P.lse_part = lse_part;
-  P.mask = mask;
-  P.o = static_cast<__nv_bfloat16*>(o);
-  P.lse = lse;
+  P.mask = out.mask;
+  P.o = static_cast<__nv_bfloat16*>(out.o);
+  P.lse = out.lse;
+  P.nparts = split ? 2 : 1;
+  P.o2 = static_cast<__nv_bfloat16*>(out.o_curr);
+  P.lse2 = out.lse_curr;
+  P.keep = out.keep;
+  P.n_cpu = out.keep ? p.q_start_pos / out.cpu_block_tokens : 0;
+  P.cpu_kb = out.keep ? out.cpu_block_tokens / kBlock : 1;
   P.ctl = ctl;
   P.err = err;
   P.n_ktm = est::key_tiles(P.T, P.T.n_rt - 1);
@@ -623,8 +673,12 @@ cudaError_t launch_sde(const Problem& p, const void* q, const void* k, const voi
   if (e != cudaSuccess) return e;
   e = cudaMemsetAsync(ctl, 0, fused_ctl_words_bytes(p, S), st);  // the counters and flags
   if (e != cudaSuccess) return e;
-  const int grid = P.n_workers + P.n_rows;
-  fused_step_kernel<S, D, E><<<grid, kThreads, smem, st>>>(mqe, mke, mq, mk, mv, mo, P);
+  if (P.n_cpu > 0) {
+    e = cudaMemsetAsync(P.keep, 0, (size_t)p.B * P.n_cpu, st);
+    if (e != cudaSuccess) return e;
+  }
+  const int grid = P.n_workers + P.nparts * P.n_rows;
+  fused_step_kernel<S, D, E><<<grid, kThreads, smem, st>>>(mqe, mke, mq, mk, mv, mo, mo2, P);
   return cudaGetLastError();
 }
 

@@ -13,7 +13,9 @@ namespace {
 bool a16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // BSX_STEP_FUSED without the offload mask or e4m3 estimate operands runs as
-// bsx_chunk_prefill, one kernel where the problem allows it.
+// bsx_chunk_prefill, one kernel where the problem allows it.  (The split
+// step keeps its separate launches: as one kernel, bsx_chunk_step, it
+// measured the same.)
 bool one_kernel(const bsx_shape& s, int q_len, int P, int stride, int flags) {
   if (!(flags & BSX_STEP_FUSED) || (flags & (BSX_STEP_OFFLOAD | BSX_STEP_E4M3_ESTIMATE)))
     return false;
@@ -163,7 +165,7 @@ extern "C" int bsx_chunk_step_host(bsx_shape s, const void* q_host, const void* 
   if (e != cudaSuccess) return cuda_fail(e);
 
   if (one_kernel(s, q_len, P, stride, flags)) {
-    // estimate, selection and attention in one launch, which reads V as well
+    // the step in one launch, which reads V as well
     if (up != st && cudaStreamWaitEvent(st, ev.ev[1], 0) != cudaSuccess) return BSX_ERR_CUDA;
     rc = bsx_chunk_prefill(s, dev->q, dev->k, dev->v, q_len, P, stride, threshold, dev->mask,
                            dev->o, dev->lse, dev->workspace, dev->workspace_bytes, st);

@@ -70,19 +70,31 @@ cudaError_t launch_bsa_tc(const Problem& p, const void* q, const void* k,
                           const BsaRange* ranges, unsigned* err, cudaStream_t st,
                           BsaDrop drop = BsaDrop());
 
-// f1: estimate, selection and attention over every key block in one launch
-// (bf16, stride in {4, 8, 16}, at most 1024 key blocks).  `ctl` is scratch
-// of fused_ctl_bytes() bytes (its counters and flags zeroed on the stream
-// before the launch);
-// lse_part the estimate partials (as launch_estimate_tc).  Test hook:
-// skip_row >= 0 never marks that selection row ready, so its attention CTA's
-// bounded wait runs out.
+// f1 and the chunk step as one launch (bf16, stride in {4, 8, 16}, at most
+// 1024 key blocks): estimate, selection and attention over every key block
+// into (o, lse); or, with o_curr, the pages' chunk step -- attention on the
+// history into (o, lse) and on the current chunk into (o_curr, lse_curr),
+// merged by LSE into (o, lse) -- and, with keep, the CPU-block flags of
+// cpu_block_tokens-token blocks (no first/last forcing).  `ctl` is a control
+// block of fused_ctl_bytes() bytes, zeroed on the stream before the launch
+// (so is keep); lse_part the estimate partials (as launch_estimate_tc).
+// Test hook: skip_row >= 0 never marks that selection row ready, so its
+// attention CTAs' bounded waits run out.
+struct FusedOut {
+  uint8_t* mask;
+  void* o;
+  float* lse;
+  void* o_curr;      // nullptr: one range
+  float* lse_curr;
+  uint8_t* keep;     // nullptr: no CPU-block flags
+  int cpu_block_tokens;
+};
 bool fused_step_supported(const Problem& p, int stride);
 size_t fused_ctl_words_bytes(const Problem& p, int stride);  // counters and flags
 size_t fused_ctl_bytes(const Problem& p, int stride);        // + per-tile row statistics
 cudaError_t launch_fused_step(const Problem& p, const void* q, const void* k, const void* v,
                               int stride, float threshold, float* lse_part, unsigned* ctl,
-                              size_t ctl_bytes, uint8_t* mask, void* o, float* lse,
-                              unsigned* err, int skip_row, cudaStream_t st);
+                              size_t ctl_bytes, const FusedOut& out, unsigned* err,
+                              int skip_row, cudaStream_t st);
 
 }  // namespace bsx

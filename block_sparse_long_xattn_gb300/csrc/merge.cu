@@ -43,22 +43,12 @@ __global__ void __launch_bounds__(256) merge_kernel(
   }
   __syncwarp();
   if (!active) return;
-  const float m = fmaxf(l1, l2);
-  float w1 = 0.f, w2 = 0.f, lse = -INFINITY;
-  if (m != -INFINITY) {
-    w1 = __expf(l1 - m);   // exp(-inf) = 0 for an empty partial
-    w2 = __expf(l2 - m);
-    const float den = w1 + w2;
-    lse = m + __logf(den);
-    const float inv = 1.f / den;
-    w1 *= inv;
-    w2 *= inv;
-  }
+  const MergeWeights w = merge_weights(l1, l2);
 #pragma unroll
   for (int e = 0; e < V::N; ++e)
-    a.e[e] = from_f32<T>(w1 * to_f32(a.e[e]) + w2 * to_f32(c.e[e]));
+    a.e[e] = from_f32<T>(merge_element(w, to_f32(a.e[e]), to_f32(c.e[e])));
   reinterpret_cast<uint4*>(o1)[gid] = a.u;
-  if (gid % VPR == 0) lse1[lidx] = lse;
+  if (gid % VPR == 0) lse1[lidx] = w.lse;
 }
 
 template <typename T, int VPR>

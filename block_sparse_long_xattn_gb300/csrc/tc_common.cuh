@@ -114,6 +114,13 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
   return v;
 }
 
+// Release store of a flag in global memory: what this thread wrote, and what
+// it has seen (through barriers) other threads write, before it is visible
+// GPU-wide to a thread that reads the flag with an acquire.
+__device__ __forceinline__ void st_release_gpu(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // Bounded wait, by one thread, for a counter in global memory written by
 // other CTAs: *p >= need (acquire: what was written before the matching
 // release is visible after it).  Gives up when *gabort is set, or after 2 s

@@ -210,11 +210,11 @@ int bsx_bsa_prefill_split(bsx_shape s, const void* q, const void* k, const void*
                           void* stream);
 
 /*
- * Bytes of device workspace bsx_chunk_prefill needs: the estimate partials
- * of bsx_estimate_workspace_bytes(), rounded up to 256 bytes; then a control
- * block of 4 * (4 + B * Hq * (ceil(R / 128) + q_len / 128)) bytes rounded up
- * to 256 (the fused launch's counters and ready flags), with R = q_len /
- * stride; then 4 * B * Hq * n_kt * R bytes rounded up to 256, n_kt =
+ * Bytes of device workspace bsx_chunk_prefill and bsx_chunk_step need: the
+ * estimate partials of bsx_estimate_workspace_bytes(), rounded up to 256
+ * bytes; then a control block of 4 * (4 + B * Hq * (ceil(R / 128) + 4 *
+ * q_len / 128)) bytes rounded up to 256 (the fused launch's counters and
+ * ready flags), with R = q_len / stride; then 4 * B * Hq * n_kt * R bytes rounded up to 256, n_kt =
  * (q_start_pos / stride + R - 1) / 256 + 1 (each reshaped row's
  * log-sum-exp over each 256-key tile, which the fused selection reads).
  * Returns 0 for invalid arguments.
@@ -252,6 +252,37 @@ int bsx_chunk_prefill(bsx_shape s, const void* q, const void* k, const void* v,
                       int q_len, int q_start_pos, int stride, float threshold,
                       uint8_t* mask, void* o, float* lse, void* workspace,
                       size_t workspace_bytes, void* stream);
+
+/*
+ * One chunk step of XAttention chunked prefill with the KV resident on the
+ * device, as the pages structure it (xattn_bsa.py compute_chunked_prefill and
+ * select_blocks): bsx_xattn_estimate; bsx_bsa_prefill_split with the history
+ * into (o, lse) and the current chunk into (o_curr, lse_curr);
+ * bsx_merge_attn of the two into (o, lse); and, when keep is not NULL and
+ * q_start_pos >= cpu_block_tokens, bsx_map_mask_to_cpu_blocks into keep (no
+ * first/last forcing).
+ *
+ * In bf16 with at most 1024 key blocks (Lk <= 131072) the whole step is ONE
+ * kernel launch (after memsets of its control block and of keep on the same
+ * stream): the fused launch of bsx_chunk_prefill, with one attention CTA per
+ * (query tile, range); of a tile's two, the one that finishes second merges
+ * the first's (O, LSE) with its own, and the selection writes the keep
+ * flags.  Otherwise the steps run as the separate launches listed above.
+ * Results: mask, the merged (o, lse) and keep as the separate calls give
+ * them (the merge adds in another order: within the O/LSE tolerance of the
+ * separate merge); o_curr / lse_curr are scratch, with unspecified contents
+ * afterwards.  With q_start_pos == 0 there is no history and (o, lse) are
+ * the current chunk's.
+ *
+ * Arguments are validated before anything is enqueued; every buffer 16-byte
+ * aligned; cpu_block_tokens (used only with keep) a positive multiple of 128
+ * dividing q_start_pos.  workspace of at least
+ * bsx_chunk_prefill_workspace_bytes() bytes, else BSX_ERR_WORKSPACE.
+ */
+int bsx_chunk_step(bsx_shape s, const void* q, const void* k, const void* v, int q_len,
+                   int q_start_pos, int stride, float threshold, int cpu_block_tokens,
+                   uint8_t* mask, void* o, float* lse, void* o_curr, float* lse_curr,
+                   uint8_t* keep, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * LSE merge of two partial attentions over disjoint key sets, in place into

@@ -57,11 +57,12 @@ def test_chunk_prefill_workspace_formula(lib):
     s = L.BsxShape(1, 32, 8, 128, L.BSX_BF16)
     # the partials (rounded up to 256 bytes), then the fused launch's control
     # block: 4 counters, tiles_done per (b, h, 128-row tile of reshaped rows),
-    # row_ready per (b, h, q-block), 4 bytes each, rounded up to 256; then one
+    # then per (b, h, q-block) the row's ready flag, its merge count and two
+    # ranges' ready flags, 4 bytes each, rounded up to 256; then one
     # float per (b, h, 256-key tile of the last row tile, reshaped row),
     # rounded up to 256
     est = 32 * 256 * 512 * 4
-    ctl = (4 + 32 * (512 // 128 + 4096 // 128)) * 4
+    ctl = (4 + 32 * (512 // 128 + 4 * (4096 // 128))) * 4
     n_kt = (28672 // 8 + 512 - 1) // 256 + 1            # 16 key tiles at 32K
     assert lib.bsx_chunk_prefill_workspace_bytes(s, 4096, 28672, 8) == \
         est + (ctl + 255) // 256 * 256 + 32 * n_kt * 512 * 4
@@ -88,6 +89,24 @@ def test_chunk_prefill_rejects_bad_arguments(lib):
     assert call(shape=L.BsxShape(1, 3, 2, 128, 1)) == -1            # Hq % Hkv
     assert call(ws=need - 1) == -5                                  # no room for the control block
     assert call(wp=None) == -5
+
+
+def test_chunk_step_rejects_bad_arguments(lib):
+    s = L.BsxShape(1, 4, 2, 128, L.BSX_BF16)
+    p = ctypes.c_void_p(64)
+    need = lib.bsx_chunk_prefill_workspace_bytes(s, 512, 1024, 8)
+
+    def call(stride=8, tau=0.9, cpu=256, o_curr=p, keep=p, ws=need):
+        return lib.bsx_chunk_step(s, p, p, p, 512, 1024, stride, tau, cpu, p, p, p, o_curr, p,
+                                  keep, p, ws, None)
+    assert call(stride=3) == -2
+    assert call(tau=float("nan")) == -1
+    assert call(o_curr=None) == -1                  # the current chunk's scratch is required
+    assert call(o_curr=ctypes.c_void_p(72)) == -1   # misaligned
+    assert call(cpu=100) == -1                      # CPU blocks: multiples of 128
+    assert call(cpu=768) == -1                      # ... dividing q_start_pos
+    assert call(ws=need - 1) == -5
+    assert call(cpu=100, keep=None, ws=need - 1) == -5  # without keep the block size is unused
 
 
 def test_debug_fused_skip_row_hook(lib):

@@ -25,7 +25,7 @@ import pytest
 import torch
 
 from block_sparse_long_xattn_gb300 import (
-    bsx_bsa_prefill, bsx_bsa_prefill_split, bsx_chunk_prefill, bsx_last_error,
+    bsx_bsa_prefill, bsx_bsa_prefill_split, bsx_chunk_prefill, bsx_chunk_step, bsx_last_error,
     bsx_map_mask_to_cpu_blocks, bsx_merge_attn, bsx_quantize_e4m3, bsx_xattn_estimate)
 from block_sparse_long_xattn_gb300.inputs import (CONFIGS, SPARSE_CONFIGS, make_workload,
                                                   round_to_e4m3)
@@ -233,6 +233,63 @@ def test_fused_chunk_step_full_size(name):
     _record(f"{name} fused", rows=n_rows, near_threshold=n_near, tie_swaps=n_tie,
             density=_density(est.mask, P), gpu_density=_density(m_g, P),
             o_lse_max_err=[float(x) for x in errs])
+
+
+def _check_chunk_step(name, w, S, tau, q, k, v, P, cpu_tokens=1024):
+    """bsx_chunk_step (one kernel) on device inputs: every mask row against the
+    oracle's estimate, the merged O / LSE of every attention CTA's rows against
+    the oracle on the kernel's own mask (the merge identity: the history and
+    current-chunk ranges merged equal one range over every key block), the
+    CPU-block flags bit-exact against the oracle's map of that mask."""
+    mask, o, lse, keep = bsx_chunk_step(q, k, v, P, S, tau, cpu_block_tokens=cpu_tokens)
+    torch.cuda.synchronize()
+    assert bsx_last_error() == 0
+    assert bool(torch.isfinite(o.float()).all()) and bool(torch.isfinite(lse).all())
+    B, Lq, Hq, _ = w.q.shape
+    nkb = w.k.shape[1] // 128
+    A = torch.empty((B, Hq, Lq // 128, nkb), dtype=torch.float32, device="cuda")
+    bsx_xattn_estimate(q, k, P, S, tau, block_sums=A)
+    est = O.xattn_estimate(w.q, w.k, P, S, tau)
+    m_g = mask.cpu().numpy()
+    n_rows, n_near, n_tie = check_mask(m_g, est, tau, P, A.cpu().numpy())
+    errs = _check_rows(w, m_g, o, lse, P, range(Hq), 0, nkb)
+    if P >= cpu_tokens:
+        np.testing.assert_array_equal(keep.cpu().numpy(),
+                                      O.map_mask_to_cpu_blocks(m_g, P, cpu_tokens))
+    _record(f"{name} chunk step, one kernel", rows=n_rows, near_threshold=n_near,
+            tie_swaps=n_tie, density=_density(est.mask, P), gpu_density=_density(m_g, P),
+            o_lse_max_err=[float(x) for x in errs])
+
+
+@pytest.mark.parametrize("name", ["llama8b-32k-chunk4096", "llama8b-128k-chunk4096",
+                                  "llama8b-32k-rho10", "llama8b-128k-rho10"])
+def test_chunk_step_one_kernel_full_size(name):
+    """The chunk step as bench.py times it (bsx_chunk_step, one kernel) at the
+    32K and 128K chunks and the sparse points."""
+    c, S, tau, _ = _cfg(name)
+    w = make_workload(seed=0, **c)
+    q, k, v = (to_dev(x, w.dtype) for x in (w.q, w.k, w.v))
+    _check_chunk_step(name, w, S, tau, q, k, v, w.q_start_pos)
+
+
+def test_llama8b_64k_chunked_sequence_one_kernel():
+    """A 64K sequence in 16 chunks of 4096 through bsx_chunk_step (one kernel
+    per chunk, as bench.py --step chunked times it); chunks 0, 1, 8 and 15
+    are checked against the oracle."""
+    c, S, tau, chunk = _cfg("llama8b-64k-chunked")
+    w = make_workload(seed=0, q_full=True, **c)
+    Lk_full = w.k.shape[1]
+    qf, kf, vf = (to_dev(x, w.dtype) for x in (w.q, w.k, w.v))
+    for ci in range(Lk_full // chunk):
+        P = ci * chunk
+        Lk = P + chunk
+        q, k, v = qf[:, P:Lk].contiguous(), kf[:, :Lk].contiguous(), vf[:, :Lk].contiguous()
+        if ci not in (0, 1, 8, 15):
+            bsx_chunk_step(q, k, v, P, S, tau)   # run in order, as a prefill would
+            continue
+        ch = SimpleNamespace(q=w.q[:, P:Lk], k=w.k[:, :Lk], v=w.v[:, :Lk], dtype=w.dtype)
+        _check_chunk_step(f"llama8b-64k-chunked chunk {ci}", ch, S, tau, q, k, v, P)
+    assert bsx_last_error() == 0
 
 
 def test_llama8b_64k_chunked_sequence():

@@ -12,9 +12,9 @@ import pytest
 import torch
 
 from block_sparse_long_xattn_gb300 import (
-    bsx_bsa_prefill, bsx_bsa_prefill_split, bsx_chunk_prefill, bsx_cpu_block_mask,
-    bsx_last_error, bsx_map_mask_to_cpu_blocks, bsx_merge_attn, bsx_quantize_e4m3,
-    bsx_xattn_estimate)
+    bsx_bsa_prefill, bsx_bsa_prefill_split, bsx_chunk_prefill, bsx_chunk_step,
+    bsx_cpu_block_mask, bsx_last_error, bsx_map_mask_to_cpu_blocks, bsx_merge_attn,
+    bsx_quantize_e4m3, bsx_xattn_estimate)
 from block_sparse_long_xattn_gb300.inputs import (
     e4m3_bits, make_workload, random_block_mask, round_to_bf16, round_to_e4m3)
 from oracle import xattn_oracle as O
@@ -340,6 +340,61 @@ def test_fused_chunk_prefill_many_tiles_per_worker():
         assert np.abs(lse.cpu().numpy()[0, h, rows] - l_r).max() <= LSE_TOL
 
 
+CHUNK_STEP_CASES = [
+    # (B, Hq, Hkv, d, Lk, P, stride, tau, cpu_block_tokens)
+    (1, 8, 2, 128, 1280, 768, 8, 0.9, 256),
+    (2, 4, 1, 64, 768, 256, 4, 0.9, 256),         # batch 2, d 64, stride 4
+    (1, 4, 2, 128, 2048, 1536, 16, 0.9, 512),     # stride 16
+    (1, 2, 2, 128, 512, 0, 8, 0.8, 128),          # no history: the current chunk alone
+    (1, 4, 1, 128, 1152, 1024, 8, 0.99, 1024),    # a chunk of one block
+    (1, 4, 2, 128, 1024, 512, 8, 1.0, 256),       # threshold 1
+    (1, 2, 1, 64, 40960, 40704, 8, 0.9, 256),     # 320 key blocks: the 1024-key select
+]
+
+
+@pytest.mark.parametrize("case", CHUNK_STEP_CASES)
+def test_chunk_step_one_kernel(case):
+    """bsx_chunk_step as one kernel (estimate, selection with the CPU-block
+    flags, attention on the history and on the current chunk, merged by the
+    range that finishes second): the mask against the oracle's estimate; O,
+    LSE and the flags bit-identical to the separate launches (split
+    attention, merge, map) run on the kernel's own mask; O / LSE against the
+    oracle's attention over every key block on that mask."""
+    B, Hq, Hkv, d, Lk, P, S, tau, cpu = case
+    w = make_workload(seed=97 + Lk + P, B=B, Hq=Hq, Hkv=Hkv, d=d, Lk=Lk, q_start_pos=P,
+                      alpha=3.0, n_hot=2, dtype="bf16")
+    q, k, v = (to_dev(x, "bf16") for x in (w.q, w.k, w.v))
+    mask, o, lse, keep = bsx_chunk_step(q, k, v, P, S, tau, cpu_block_tokens=cpu)
+    torch.cuda.synchronize()
+    assert bsx_last_error() == 0
+    _, A_g = _estimate(w, S, tau)
+    est = O.xattn_estimate(w.q, w.k, P, S, tau)
+    m_g = mask.cpu().numpy()
+    check_mask(m_g, est, tau, P, A_g)
+    nkb = Lk // 128
+    oh, lh, oc, lc = bsx_bsa_prefill_split(q, k, v, mask, P)
+    bsx_merge_attn(oh, lh, oc, lc)
+    torch.cuda.synchronize()
+    assert torch.equal(o, oh) and torch.equal(lse, lh)
+    if P >= cpu:
+        np.testing.assert_array_equal(keep.cpu().numpy(),
+                                      bsx_map_mask_to_cpu_blocks(mask, P, cpu).cpu().numpy())
+        np.testing.assert_array_equal(keep.cpu().numpy(), O.map_mask_to_cpu_blocks(m_g, P, cpu))
+    else:
+        assert keep is None
+    if Lk > 8192:
+        rows = np.array(sorted({r for t in range((Lk - P) // 128)
+                                for r in (t * 128 + 3, t * 128 + 100)}))
+        for h in range(Hq):
+            o_r, l_r = O.bsa_rows(w.q, w.k, w.v, m_g, P, 0, nkb, 0, h, rows)
+            assert np.abs(o.float().cpu().numpy()[0, rows, h] - o_r).max() <= O_TOL["bf16"]
+            assert np.abs(lse.cpu().numpy()[0, h, rows] - l_r).max() <= LSE_TOL
+        return
+    o_ref, lse_ref = O.bsa_prefill(w.q, w.k, w.v, m_g, P, 0, nkb)
+    assert np.abs(o.float().cpu().numpy() - o_ref).max() <= O_TOL["bf16"]
+    assert np.abs(lse.cpu().numpy() - lse_ref).max() <= LSE_TOL
+
+
 def test_offload_semantics_chunk_step():
     """The pages' offload attention: CPU blocks kept if any of their BSA blocks
     is selected (first and last forced), history dense over the kept CPU
@@ -469,12 +524,19 @@ def test_chunk_step_host(case):
     (ds or stream).synchronize()
     assert bsx_last_error() == 0
 
-    # the same step through the device entry points
+    # the same step through the device entry points.  A fused bf16 step
+    # without the offload mask or e4m3 operands runs as one kernel
+    # (bsx_chunk_prefill), whose selection may round a near-threshold row
+    # differently from bsx_xattn_estimate's: then the attention after the
+    # estimate takes the one kernel's mask and must match it bit for bit
+    one_kernel = fused and dt == "bf16" and not (offload or e4m3)
     q, k, v = (x.cuda() for x in host)
     nkb, n_cpu = (P + Lq) // 128, P // cpu
     qe, ke = (bsx_quantize_e4m3(q), bsx_quantize_e4m3(k)) if e4m3 else (q, k)
     A = torch.empty((1, Hq, Lq // 128, nkb), dtype=torch.float32, device="cuda")
     mask = bsx_xattn_estimate(qe, ke, P, S, tau, block_sums=A)
+    if one_kernel:
+        mask = bufs["mask"].clone()
     keep = bsx_map_mask_to_cpu_blocks(mask, P, cpu, force) if n_cpu else None
     attn_mask = bsx_cpu_block_mask(keep, Lq, P, Hq, cpu) if offload else mask
     if fused:
@@ -602,3 +664,38 @@ def test_fused_step_wait_timeout_is_reported_and_the_context_survives():
     assert np.abs(o.float().cpu().numpy() - o_ref).max() <= O_TOL["bf16"]
     assert np.abs(lse.cpu().numpy() - lse_ref).max() <= LSE_TOL
     assert nqb == 4
+
+
+def test_chunk_step_wait_timeout_is_reported_and_the_context_survives():
+    """The one-kernel chunk step with selection row 2 never marked ready: both
+    attention CTAs of that query tile give up after their bound and count
+    their range as finished first, so the tile keeps the history range's
+    empty result (o = 0, lse = -inf) and no merge waits on it; the error word
+    names the fused step's row wait; every other row and the next step are
+    correct."""
+    from block_sparse_long_xattn_gb300 import bsx_debug_fused_skip_row
+    P, Lq, S, tau, cpu = 512, 512, 8, 0.9, 256
+    w = make_workload(seed=47, B=1, Hq=2, Hkv=1, d=128, Lk=P + Lq, q_start_pos=P,
+                      alpha=3.0, n_hot=1, dtype="bf16")
+    q, k, v = (to_dev(x, "bf16") for x in (w.q, w.k, w.v))
+    nkb = (P + Lq) // 128
+    torch.cuda.synchronize()
+    assert bsx_last_error() == 0
+    bsx_debug_fused_skip_row(2)               # b 0, h 0, qb 2
+    mask, o, lse, _ = bsx_chunk_step(q, k, v, P, S, tau, cpu_block_tokens=cpu)
+    torch.cuda.synchronize()
+    code = bsx_last_error()
+    assert code & 0x80000000 and code & 0xFF == 3 and (code >> 8) & 0xFF == 1
+    o_g, l_g = o.float().cpu().numpy(), lse.cpu().numpy()
+    assert np.all(o_g[0, 256:384, 0] == 0) and np.all(np.isneginf(l_g[0, 0, 256:384]))
+    o_ref, lse_ref = O.bsa_prefill(w.q, w.k, w.v, mask.cpu().numpy(), P, 0, nkb)
+    keep_rows = np.ones(o_g.shape[:3], bool)
+    keep_rows[0, 256:384, 0] = False
+    assert np.abs(o_g - o_ref)[keep_rows].max() <= O_TOL["bf16"]
+    assert np.abs(l_g - lse_ref).transpose(0, 2, 1)[keep_rows].max() <= LSE_TOL
+    mask, o, lse, _ = bsx_chunk_step(q, k, v, P, S, tau, cpu_block_tokens=cpu)
+    torch.cuda.synchronize()
+    assert bsx_last_error() == 0
+    o_ref, lse_ref = O.bsa_prefill(w.q, w.k, w.v, mask.cpu().numpy(), P, 0, nkb)
+    assert np.abs(o.float().cpu().numpy() - o_ref).max() <= O_TOL["bf16"]
+    assert np.abs(lse.cpu().numpy() - lse_ref).max() <= LSE_TOL
