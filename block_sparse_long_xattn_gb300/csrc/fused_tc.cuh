@@ -31,11 +31,12 @@
 //                    finishes second merges the other's (O, LSE) with its
 //                    own by LSE (bsa_tc.cuh), and the selection also writes
 //                    the CPU-block keep flags of each row's history blocks.
-// Every wait points at work held by a smaller ticket, or at work that a
-// running worker will take: a CTA with a ticket has started, a worker never
-// waits on an attention CTA, and workers keep taking estimate tiles while any
-// are left.  So the launch cannot deadlock, whatever number of CTAs the GPU
-// keeps resident.  Every wait is bounded; one that gives up records the
+// Every wait points at work held by a smaller ticket, at work that a running
+// worker will take, or (the merge) at a range that has already counted
+// itself finished and whose epilogue waits on nothing: a CTA with a ticket
+// has started, a worker never waits on an attention CTA, and workers keep
+// taking estimate tiles and rows while any are left.  So the launch cannot
+// deadlock, whatever number of CTAs the GPU keeps resident.  Every wait is bounded; one that gives up records the
 // device error word and sets a shared abort flag that ends the others' waits.
 //
 // The control block (counters, tiles_done, row_ready) sits in the caller's
