@@ -14,6 +14,10 @@
  *                            selected 128-token blocks -> O and LSE
  *   bsx_merge_attn           LSE merge of two partial (O, LSE) pairs
  *   bsx_map_mask_to_cpu_blocks  1024-token CPU-block keep flags
+ *   bsx_chunk_step           the whole chunk step on device inputs (the four
+ *                            steps; one kernel launch where supported)
+ *   bsx_chunk_prefill        estimate + attention over every key block (the
+ *                            merge identity; one kernel launch where supported)
  *   bsx_chunk_step_host      the whole chunk step from host inputs to host
  *                            outputs (uploads, the four steps, read-back)
  *
