@@ -53,7 +53,8 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_tc_kernel(
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const BsaArgs a{&tm_q, &tm_k, &tm_v, mask, q_len, Lk, Hq, Hkv, nqb, cur, scale_log2, err};
-  const BsaTile tile{b, h, qb, kb_begin, kb_end, o, lse, part ? &tm_o1 : &tm_o0,
+  const BsaTile tile{b,       h,      qb,  kb_begin, kb_end,  kb_end,
+                     o,       lse,    part ? &tm_o1 : &tm_o0, nullptr,
                      (int)blockIdx.x == parts.drop_cta, parts.drop_item, nullptr, nullptr};
   bsa_cta<D, false>(a, tile, smem);
 }

@@ -74,8 +74,11 @@ __device__ __forceinline__ MergeWeights merge_weights(float l1, float l2) {
   const float m = fmaxf(l1, l2);
   MergeWeights r{0.f, 0.f, -INFINITY};
   if (m != -INFINITY) {
-    r.w1 = __expf(l1 - m);  // exp(-inf) = 0 for an empty partial
-    r.w2 = __expf(l2 - m);
+    // exp(-inf) = 0 for an empty partial; the differences are rounded on
+    // their own, so that an LSE computed just before (not loaded) cannot fuse
+    // into them
+    r.w1 = __expf(__fsub_rn(l1, m));
+    r.w2 = __expf(__fsub_rn(l2, m));
     const float den = __fadd_rn(r.w1, r.w2);
     r.lse = __fadd_rn(m, __logf(den));
     const float inv = __frcp_rn(den);

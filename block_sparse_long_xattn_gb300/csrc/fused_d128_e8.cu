@@ -1,27 +1,9 @@
-// f1 fused chunk step: the kernels for d = 128 and rows of up to 1024 key
-// blocks (one translation unit per pair, so that they compile in parallel).
+// f1 fused chunk step: the kernels for d = 128, rows of up to 1024 key blocks
+// and one range over every key block.
 #include "fused_tc.cuh"
 
 namespace bsx {
 
-cudaError_t launch_fused_d128_e8(const Problem& p, const void* q, const void* k,
-                                  const void* v, int stride, float threshold, float* lse_part,
-                                  unsigned* ctl, size_t ctl_bytes, const FusedOut& out,
-                                  unsigned* err, int skip_row, cudaStream_t st) {
-  using namespace fused;
-  switch (stride) {
-    case 4:
-      return launch_sde<4, 128, 8>(p, q, k, v, threshold, lse_part, ctl, ctl_bytes, out, err,
-                                    skip_row, st);
-    case 8:
-      return launch_sde<8, 128, 8>(p, q, k, v, threshold, lse_part, ctl, ctl_bytes, out, err,
-                                    skip_row, st);
-    case 16:
-      return launch_sde<16, 128, 8>(p, q, k, v, threshold, lse_part, ctl, ctl_bytes, out,
-                                     err, skip_row, st);
-    default:
-      return cudaErrorInvalidValue;
-  }
-}
+BSX_FUSED_LAUNCHER(launch_fused_d128_e8, 128, 8, false)
 
 }  // namespace bsx

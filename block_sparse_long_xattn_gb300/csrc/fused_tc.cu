@@ -1,27 +1,29 @@
 // f1 fused chunk step: host-side dispatch to the kernel instantiations
-// (fused_d*_e*.cu) and the control block's size.  The kernel is described in
+// (fused_d*_e*.cu, fused_two_d*_e*.cu) and the control block's size.  The kernel is described in
 // fused_tc.cuh.
 #include "fused_tc.cuh"
 
 namespace bsx {
 
-#define BSX_FUSED_DECL(D, E)                                                            \
-  cudaError_t launch_fused_d##D##_e##E(const Problem& p, const void* q, const void* k, \
-                                       const void* v, int stride, float threshold,     \
-                                       float* lse_part, unsigned* ctl, size_t ctl_bytes, \
-                                       const FusedOut& out, unsigned* err, int skip_row, \
-                                       cudaStream_t st);
-BSX_FUSED_DECL(64, 2)
-BSX_FUSED_DECL(64, 8)
-BSX_FUSED_DECL(128, 2)
-BSX_FUSED_DECL(128, 8)
+#define BSX_FUSED_DECL(NAME)                                                            \
+  cudaError_t NAME(const Problem& p, const void* q, const void* k, const void* v, int stride, \
+                   float threshold, float* lse_part, unsigned* ctl, size_t ctl_bytes,         \
+                   const FusedOut& out, unsigned* err, int skip_row, cudaStream_t st);
+BSX_FUSED_DECL(launch_fused_d64_e2)
+BSX_FUSED_DECL(launch_fused_d64_e8)
+BSX_FUSED_DECL(launch_fused_d128_e2)
+BSX_FUSED_DECL(launch_fused_d128_e8)
+BSX_FUSED_DECL(launch_fused_two_d64_e2)
+BSX_FUSED_DECL(launch_fused_two_d64_e8)
+BSX_FUSED_DECL(launch_fused_two_d128_e2)
+BSX_FUSED_DECL(launch_fused_two_d128_e8)
 #undef BSX_FUSED_DECL
 
 size_t fused_ctl_words_bytes(const Problem& p, int stride) {
   const long long R = p.q_len / stride;
   const long long n_rt = (R + est::kM - 1) / est::kM;
-  // the head, tiles_done, row_ready, the merge counts and two ready flags per row
-  const long long words = fused::kCtlHead + (long long)p.B * p.Hq * (n_rt + 4LL * p.nqb);
+  // the head, tiles_done and row_ready
+  const long long words = fused::kCtlHead + (long long)p.B * p.Hq * (n_rt + (long long)p.nqb);
   return (size_t)((words * 4 + 255) / 256 * 256);
 }
 
@@ -43,8 +45,12 @@ cudaError_t launch_fused_step(const Problem& p, const void* q, const void* k, co
                               int skip_row, cudaStream_t st) {
   if (!fused_step_supported(p, stride)) return cudaErrorInvalidValue;
   const bool small = p.nkb <= 2 * fused::kSelThreads;  // rows of up to 256 key blocks
-  auto launch = p.d == 64 ? (small ? launch_fused_d64_e2 : launch_fused_d64_e8)
-                          : (small ? launch_fused_d128_e2 : launch_fused_d128_e8);
+  const bool two = out.o_curr != nullptr;  // the chunk step's two ranges
+  auto launch =
+      two ? (p.d == 64 ? (small ? launch_fused_two_d64_e2 : launch_fused_two_d64_e8)
+                       : (small ? launch_fused_two_d128_e2 : launch_fused_two_d128_e8))
+          : (p.d == 64 ? (small ? launch_fused_d64_e2 : launch_fused_d64_e8)
+                       : (small ? launch_fused_d128_e2 : launch_fused_d128_e8));
   return launch(p, q, k, v, stride, threshold, lse_part, ctl, ctl_bytes, out, err, skip_row, st);
 }
 

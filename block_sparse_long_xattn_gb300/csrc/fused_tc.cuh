@@ -22,22 +22,22 @@
 //                    Once the counter has no estimate tile left, the four
 //                    epilogue warps become a second selection group (the
 //                    idle stage ring is their scratch).
-//   tickets [W, W+n) one attention CTA per (b, h, qb), in the order of the
-//                    stand-alone attention kernel; it waits for its row's
-//                    ready flag before its first read of the mask.  As the
-//                    pages' chunk step (two ranges): n = 2 B Hq nqb, the
-//                    history CTAs (key blocks below q_start_pos/128) then the
-//                    current-chunk CTAs; of a query tile's two, the one that
-//                    finishes second merges the other's (O, LSE) with its
-//                    own by LSE (bsa_tc.cuh), and the selection also writes
-//                    the CPU-block keep flags of each row's history blocks.
-// Every wait points at work held by a smaller ticket, at work that a running
-// worker will take, or (the merge) at a range that has already counted
-// itself finished and whose epilogue waits on nothing: a CTA with a ticket
-// has started, a worker never waits on an attention CTA, and workers keep
-// taking estimate tiles and rows while any are left.  So the launch cannot
-// deadlock, whatever number of CTAs the GPU keeps resident.  Every wait is bounded; one that gives up records the
-// device error word and sets a shared abort flag that ends the others' waits.
+//   tickets [W, W+n) one attention CTA per (b, h, qb), n = B Hq nqb, in the
+//                    order of the stand-alone attention kernel; it waits for
+//                    its row's ready flag before its first read of the mask.
+//                    As the pages' chunk step (two ranges), the CTA attends
+//                    to the history (key blocks below q_start_pos/128) and
+//                    to the current chunk as two ranges and merges the two
+//                    results by LSE itself (bsa_tc.cuh), and the selection
+//                    also writes the CPU-block keep flags of each row's
+//                    history blocks.
+// Every wait points at work held by a smaller ticket or at work that a
+// running worker will take: a CTA with a ticket has started, a worker never
+// waits on an attention CTA, and workers keep taking estimate tiles and rows
+// while any are left.  So the launch cannot deadlock, whatever number of
+// CTAs the GPU keeps resident.  Every wait is bounded; one that gives up
+// records the device error word and sets a shared abort flag that ends the
+// others' waits.
 //
 // The control block (counters, tiles_done, row_ready) sits in the caller's
 // workspace after the estimate partials and is zeroed on the stream before
@@ -60,10 +60,10 @@ constexpr int kSelThreads = 128;         // a selection group: four warps
 constexpr int kSelWarps = kSelThreads / 32;
 
 // control block: [0] ticket, [1] next estimate tile, [2] next selection row,
-// [3] abort, then tiles_done[B*Hq*n_rt], row_ready[n_rows], merge counts
-// [n_rows] and range ready flags [2][n_rows] (n_rows = B*Hq*nqb; all zeroed
-// before each launch); then, 256-byte aligned, tile_lse[B*Hq][n_ktm][R]
-// (every value read is written first in the same launch)
+// [3] abort, then tiles_done[B*Hq*n_rt] and row_ready[n_rows] (n_rows =
+// B*Hq*nqb; all zeroed before each launch); then, 256-byte aligned,
+// tile_lse[B*Hq][n_ktm][R] (every value read is written first in the same
+// launch)
 constexpr int kCtlHead = 4;
 
 // worker shared memory
@@ -94,11 +94,10 @@ struct FusedParams {
   float* tile_lse;  // [b][h][kt][i]: each row's log-sum-exp over one key tile
   int n_ktm;        // key tiles of the last row tile (the most any row tile has)
   uint8_t* mask;
-  __nv_bfloat16* o;  // the result (with two ranges: the history's, then the merged)
+  __nv_bfloat16* o;  // the result (with two ranges: merged)
   float* lse;
-  int nparts;        // 1: one range over every key block; 2: history + current chunk
-  __nv_bfloat16* o2;  // two ranges: the current chunk's (O, LSE), merge scratch
-  float* lse2;
+  bool two;          // false: one range over every key block; true: history + current chunk
+  __nv_bfloat16* o_scratch;  // two ranges: the history's O on its way to the merge
   uint8_t* keep;     // CPU-block keep flags [B][n_cpu], or nullptr
   int n_cpu, cpu_kb;  // CPU blocks of the history, key blocks per CPU block
   unsigned* ctl;
@@ -527,12 +526,12 @@ __device__ __forceinline__ void worker(const FusedParams& P, const CUtensorMap* 
   if (tid == 0 && *abort_flag) atomicExch(gabort, 1u);
 }
 
-template <int S, int D, int E>
+template <int S, int D, int E, bool kTwo>
 __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(
     const __grid_constant__ CUtensorMap tm_qe, const __grid_constant__ CUtensorMap tm_ke,
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-    const __grid_constant__ CUtensorMap tm_o2, const FusedParams P) {
+    const FusedParams P) {
   __shared__ int s_ticket;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -544,12 +543,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(
     worker<S, D, E>(P, &tm_qe, &tm_ke, smem);
     return;
   }
-  // attention CTA u: range 0 first, then batch, heads and query tiles
-  // last-first (the order of the stand-alone attention kernel), which is also
-  // the order in which the workers finish the rows of the early heads
-  const int u0 = ticket - P.n_workers;
-  const int part = u0 / P.n_rows;
-  const int u = u0 - part * P.n_rows;
+  // attention CTA u: batch, heads, then query tiles last-first (the order
+  // of the stand-alone attention kernel), which is also the order in which
+  // the workers finish the rows of the early heads
+  const int u = ticket - P.n_workers;
   const int nqb = P.nqb;
   const int b = u / (nqb * P.Hq);
   const int r2 = u - b * (nqb * P.Hq);
@@ -557,38 +554,22 @@ __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(
   const int qb = nqb - 1 - (r2 - h * nqb);
   const int r = (b * P.Hq + h) * nqb + qb;
   unsigned* row_ready = P.ctl + kCtlHead + P.B * P.Hq * P.T.n_rt;
-  unsigned* mcnt = row_ready + P.n_rows;
-  unsigned* part_ready = mcnt + P.n_rows;  // [2][n_rows]
   const bsa::BsaArgs a{&tm_q, &tm_k, &tm_v, P.mask, P.q_len, P.Lk, P.Hq, P.Hkv,
                        nqb,   P.cur, P.scale_bsa, P.err};
-  bsa::BsaTile tile{b, h, qb, 0, P.nkb, P.o, P.lse, &tm_o, false, -1, row_ready + r, P.ctl + 3};
-  if (P.nparts == 2) {
-    tile.kb_begin = part ? P.cur : 0;
-    tile.kb_end = part ? P.nkb : P.cur;
-    if (part) {
-      tile.o = P.o2;
-      tile.lse = P.lse2;
-      tile.tm_o = &tm_o2;
-    }
-    tile.mcnt = mcnt + r;
-    tile.my_ready = part_ready + part * P.n_rows + r;
-    tile.other_ready = part_ready + (1 - part) * P.n_rows + r;
-    tile.other_o = part ? P.o : P.o2;
-    tile.other_lse = part ? P.lse : P.lse2;
-    tile.dest_o = P.o;
-    tile.dest_lse = P.lse;
-    tile.tm_dest = &tm_o;
-  }
-  bsa::bsa_cta<D, true>(a, tile, smem);
+  const bsa::BsaTile tile{b,     h,          qb,          0,     P.two ? P.cur : P.nkb,
+                          P.nkb, P.o,        P.lse,       &tm_o, P.o_scratch,
+                          false, -1,         row_ready + r, P.ctl + 3};
+  bsa::bsa_cta<D, true, kTwo>(a, tile, smem);
 }
 
-template <int S, int D, int E>
+template <int S, int D, int E, bool kTwo>
 cudaError_t launch_sde(const Problem& p, const void* q, const void* k, const void* v,
                        float threshold, float* lse_part, unsigned* ctl, size_t ctl_bytes,
                        const FusedOut& out, unsigned* err, int skip_row, cudaStream_t st) {
   const int R = p.q_len / S, Ck = p.Lk / S;
   const bool split = out.o_curr != nullptr;
-  CUtensorMap mqe, mke, mq, mk, mv, mo, mo2;
+  if (split != kTwo) return cudaErrorInvalidValue;
+  CUtensorMap mqe, mke, mq, mk, mv, mo;
   {  // the estimator's 5-D views (features, head, phase, reshaped row, batch)
     const uint64_t dims[5] = {(uint64_t)D, (uint64_t)p.Hq, (uint64_t)S, (uint64_t)R,
                               (uint64_t)p.B};
@@ -612,8 +593,6 @@ cudaError_t launch_sde(const Problem& p, const void* q, const void* k, const voi
                             (uint64_t)p.q_len * p.Hq * D * 2};
     if (!encode_tmap_bf16(&mq, q, 4, dq, sq, box)) return cudaErrorInvalidValue;
     if (!encode_tmap_bf16(&mo, out.o, 4, dq, sq, box)) return cudaErrorInvalidValue;
-    if (!encode_tmap_bf16(&mo2, split ? out.o_curr : out.o, 4, dq, sq, box))
-      return cudaErrorInvalidValue;
     const uint64_t dk[4] = {(uint64_t)D, (uint64_t)p.Hkv, (uint64_t)p.Lk, (uint64_t)p.B};
     const uint64_t sk[3] = {(uint64_t)D * 2, (uint64_t)p.Hkv * D * 2,
                             (uint64_t)p.Lk * p.Hkv * D * 2};
@@ -645,9 +624,8 @@ cudaError_t launch_sde(const Problem& p, const void* q, const void* k, const voi
   P.mask = out.mask;
   P.o = static_cast<__nv_bfloat16*>(out.o);
   P.lse = out.lse;
-  P.nparts = split ? 2 : 1;
-  P.o2 = static_cast<__nv_bfloat16*>(out.o_curr);
-  P.lse2 = out.lse_curr;
+  P.two = split;
+  P.o_scratch = static_cast<__nv_bfloat16*>(out.o_curr);
   P.keep = out.keep;
   P.n_cpu = out.keep ? p.q_start_pos / out.cpu_block_tokens : 0;
   P.cpu_kb = out.keep ? out.cpu_block_tokens / kBlock : 1;
@@ -669,7 +647,7 @@ cudaError_t launch_sde(const Problem& p, const void* q, const void* k, const voi
   // after the attention's own layout
   constexpr int kBytes = std::max(kWorkerBytes, bsa::Layout<D>::kBytes + 1024);
   const size_t smem = kBytes + 1024;
-  e = cudaFuncSetAttribute(fused_step_kernel<S, D, E>,
+  e = cudaFuncSetAttribute(fused_step_kernel<S, D, E, kTwo>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   e = cudaMemsetAsync(ctl, 0, fused_ctl_words_bytes(p, S), st);  // the counters and flags
@@ -678,10 +656,32 @@ cudaError_t launch_sde(const Problem& p, const void* q, const void* k, const voi
     e = cudaMemsetAsync(P.keep, 0, (size_t)p.B * P.n_cpu, st);
     if (e != cudaSuccess) return e;
   }
-  const int grid = P.n_workers + P.nparts * P.n_rows;
-  fused_step_kernel<S, D, E><<<grid, kThreads, smem, st>>>(mqe, mke, mq, mk, mv, mo, mo2, P);
+  const int grid = P.n_workers + P.n_rows;
+  fused_step_kernel<S, D, E, kTwo><<<grid, kThreads, smem, st>>>(mqe, mke, mq, mk, mv, mo, P);
   return cudaGetLastError();
 }
 
 }  // namespace fused
 }  // namespace bsx
+
+// One host launcher per (d, E, ranges): the kernels of the three strides.
+// Each fused_*.cu translation unit defines one, so that they compile in
+// parallel.
+#define BSX_FUSED_LAUNCHER(NAME, D, E, TWO)                                                  \
+  cudaError_t NAME(const Problem& p, const void* q, const void* k, const void* v, int stride, \
+                   float threshold, float* lse_part, unsigned* ctl, size_t ctl_bytes,         \
+                   const FusedOut& out, unsigned* err, int skip_row, cudaStream_t st) {       \
+    switch (stride) {                                                                         \
+      case 4:                                                                                 \
+        return fused::launch_sde<4, D, E, TWO>(p, q, k, v, threshold, lse_part, ctl,          \
+                                               ctl_bytes, out, err, skip_row, st);            \
+      case 8:                                                                                 \
+        return fused::launch_sde<8, D, E, TWO>(p, q, k, v, threshold, lse_part, ctl,          \
+                                               ctl_bytes, out, err, skip_row, st);            \
+      case 16:                                                                                \
+        return fused::launch_sde<16, D, E, TWO>(p, q, k, v, threshold, lse_part, ctl,         \
+                                                ctl_bytes, out, err, skip_row, st);           \
+      default:                                                                                \
+        return cudaErrorInvalidValue;                                                         \
+    }                                                                                         \
+  }

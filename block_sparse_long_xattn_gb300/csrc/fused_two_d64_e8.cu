@@ -1,0 +1,9 @@
+// f1 fused chunk step: the kernels for d = 64, rows of up to 1024 key blocks
+// and the chunk step's two ranges (history and current chunk, merged in each attention CTA).
+#include "fused_tc.cuh"
+
+namespace bsx {
+
+BSX_FUSED_LAUNCHER(launch_fused_two_d64_e8, 64, 8, true)
+
+}  // namespace bsx

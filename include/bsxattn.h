@@ -216,7 +216,7 @@ int bsx_bsa_prefill_split(bsx_shape s, const void* q, const void* k, const void*
 /*
  * Bytes of device workspace bsx_chunk_prefill and bsx_chunk_step need: the
  * estimate partials of bsx_estimate_workspace_bytes(), rounded up to 256
- * bytes; then a control block of 4 * (4 + B * Hq * (ceil(R / 128) + 4 *
+ * bytes; then a control block of 4 * (4 + B * Hq * (ceil(R / 128) +
  * q_len / 128)) bytes rounded up to 256 (the fused launch's counters and
  * ready flags), with R = q_len / stride; then 4 * B * Hq * n_kt * R bytes rounded up to 256, n_kt =
  * (q_start_pos / stride + R - 1) / 256 + 1 (each reshaped row's
@@ -268,15 +268,14 @@ int bsx_chunk_prefill(bsx_shape s, const void* q, const void* k, const void* v,
  *
  * In bf16 with at most 1024 key blocks (Lk <= 131072) the whole step is ONE
  * kernel launch (after memsets of its control block and of keep on the same
- * stream): the fused launch of bsx_chunk_prefill, with one attention CTA per
- * (query tile, range); of a tile's two, the one that finishes second merges
- * the first's (O, LSE) with its own, and the selection writes the keep
+ * stream): the fused launch of bsx_chunk_prefill, whose attention CTA for a
+ * query tile attends to the history and to the current chunk as two ranges
+ * and merges the two results itself, and whose selection writes the keep
  * flags.  Otherwise the steps run as the separate launches listed above.
- * Results: mask, the merged (o, lse) and keep as the separate calls give
- * them (the merge adds in another order: within the O/LSE tolerance of the
- * separate merge); o_curr / lse_curr are scratch, with unspecified contents
- * afterwards.  With q_start_pos == 0 there is no history and (o, lse) are
- * the current chunk's.
+ * Results: mask, the merged (o, lse) and keep, bit for bit as the separate
+ * calls give them on the same mask; o_curr / lse_curr are scratch, with
+ * unspecified contents afterwards.  With q_start_pos == 0 there is no
+ * history and (o, lse) are the current chunk's.
  *
  * Arguments are validated before anything is enqueued; every buffer 16-byte
  * aligned; cpu_block_tokens (used only with keep) a positive multiple of 128

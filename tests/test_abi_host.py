@@ -57,12 +57,12 @@ def test_chunk_prefill_workspace_formula(lib):
     s = L.BsxShape(1, 32, 8, 128, L.BSX_BF16)
     # the partials (rounded up to 256 bytes), then the fused launch's control
     # block: 4 counters, tiles_done per (b, h, 128-row tile of reshaped rows),
-    # then per (b, h, q-block) the row's ready flag, its merge count and two
-    # ranges' ready flags, 4 bytes each, rounded up to 256; then one
+    # then per (b, h, q-block) the row's ready flag, 4 bytes each, rounded up
+    # to 256; then one
     # float per (b, h, 256-key tile of the last row tile, reshaped row),
     # rounded up to 256
     est = 32 * 256 * 512 * 4
-    ctl = (4 + 32 * (512 // 128 + 4 * (4096 // 128))) * 4
+    ctl = (4 + 32 * (512 // 128 + 4096 // 128)) * 4
     n_kt = (28672 // 8 + 512 - 1) // 256 + 1            # 16 key tiles at 32K
     assert lib.bsx_chunk_prefill_workspace_bytes(s, 4096, 28672, 8) == \
         est + (ctl + 255) // 256 * 256 + 32 * n_kt * 512 * 4

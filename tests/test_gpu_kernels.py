@@ -667,12 +667,11 @@ def test_fused_step_wait_timeout_is_reported_and_the_context_survives():
 
 
 def test_chunk_step_wait_timeout_is_reported_and_the_context_survives():
-    """The one-kernel chunk step with selection row 2 never marked ready: both
-    attention CTAs of that query tile give up after their bound and count
-    their range as finished first, so the tile keeps the history range's
-    empty result (o = 0, lse = -inf) and no merge waits on it; the error word
-    names the fused step's row wait; every other row and the next step are
-    correct."""
+    """The one-kernel chunk step with selection row 2 never marked ready: the
+    attention CTA of that query tile gives up after its bound and writes the
+    empty result (o = 0, lse = -inf, the merge of two empty ranges); the
+    error word names the fused step's row wait; every other row and the next
+    step are correct."""
     from block_sparse_long_xattn_gb300 import bsx_debug_fused_skip_row
     P, Lq, S, tau, cpu = 512, 512, 8, 0.9, 256
     w = make_workload(seed=47, B=1, Hq=2, Hkv=1, d=128, Lk=P + Lq, q_start_pos=P,
