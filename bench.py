@@ -52,8 +52,8 @@ DOMINANT = "bsa_prefill"
 MMA_FLOP_PER_CLK_SM = 8192
 DATASHEET_BF16_TFLOPS = 2250.0
 BSA_SOURCES = ("bsa_tc.cu", "bsa_tc.cuh", "bsa_simt.cu", "common.cuh", "tc_common.cuh")
-FUSED_SOURCES = ("fused_tc.cuh", "fused_tc.cu", "fused_d128_e2.cu", "estimate_tc.cuh", "bsa_tc.cuh",
-                 "common.cuh", "tc_common.cuh")
+FUSED_SOURCES = ("fused_tc.cuh", "fused_tc.cu", "fused_d128_e2.cu", "fused_two_d128_e2.cu",
+                 "estimate_tc.cuh", "bsa_tc.cuh", "common.cuh", "tc_common.cuh")
 
 
 def _env_rank():
