@@ -525,10 +525,11 @@ def run_chunked(args):
     step runs the chunk step (estimate over history + chunk, attention on
     history and current chunk in one launch, merge, CPU-block map) for every
     chunk in order, each chunk's queries against all keys before its end.
-    value = sequence tokens / step time.  The end-to-end leg uploads each
-    chunk's Q, K and V rows from pinned host memory (appending to the device
-    KV, as a prefill does), runs the chunk step after its upload and reads the
-    chunk's O and LSE back, on three streams."""
+    value = sequence tokens / step time.  With --step chunk_kernel each
+    chunk's step is bsx_chunk_step, one kernel.  The end-to-end leg uploads
+    each chunk's Q, K and V rows from pinned host memory (appending to the
+    device KV, as a prefill does), runs the chunk step after its upload and
+    reads the chunk's O and LSE back, on three streams."""
     import torch
     import torch.distributed as dist
 
@@ -564,11 +565,27 @@ def run_chunked(args):
                      dtype=torch.uint8, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
+    one_kernel = args.step == "chunk_kernel"
+    if one_kernel:
+        wsc = torch.empty(bsx.bsx_chunk_prefill_workspace_bytes(bsx.shape_of(dq, dk), chunk,
+                                                                L - chunk, S),
+                          dtype=torch.uint8, device=dev)
 
     def chunk_step(c, ev=None):
         P = c * chunk
         q, k, v = dq[:, P:P + chunk], dk[:, :P + chunk], dv[:, :P + chunk]
         o = o_full[:, P:P + chunk]
+        if one_kernel:
+            # the whole chunk step in one kernel; ev brackets it
+            if ev:
+                ev[0].record(stream)
+            bsx.bsx_chunk_step(q, k, v, P, S, tau, cpu_block_tokens=cpu_tokens, mask=masks[c],
+                               o=o, lse=lse[c], o_curr=oc, lse_curr=lc,
+                               keep=keeps[c] if P >= cpu_tokens else None, workspace=wsc,
+                               stream=stream)
+            if ev:
+                ev[1].record(stream)
+            return
         bsx.bsx_xattn_estimate(q, k, P, S, tau, mask=masks[c], workspace=ws, stream=stream)
         if ev:
             ev[0].record(stream)
@@ -651,6 +668,9 @@ def run_chunked(args):
     (ms_step, ms_e2e), tokens, value = aggregate_ranks(
         [ms_step, float(np.mean(e2e_ms))], B * L, world, dev)
     hbm_peak, tc_peak, tc_sustained, peak_src = _peaks()
+    if one_kernel:
+        # the one kernel's algorithmic flops: the estimate's and the attention's
+        flops += sum(estimate_flops(cfg, chunk, c * chunk, S) for c in range(n_chunks))
     achieved = flops / (bsa_ms / 1e3) / 1e12
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -658,21 +678,24 @@ def run_chunked(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic (seeded planted-direction N(0,1) inputs)",
         "config": config_dict(args, world),
-        "roofline": {"kernel": DOMINANT, "bound": "tensor", "achieved": achieved,
+        "roofline": {"kernel": "chunk_step" if one_kernel else DOMINANT, "bound": "tensor",
+                     "achieved": achieved,
                      "peak": tc_peak, "unit": "TFLOP/s", "frac": achieved / tc_peak,
                      "traffic": None, "peak_source": peak_src, "peak_sustained": tc_sustained,
                      "frac_vs_sustained": achieved / tc_sustained if tc_sustained else None,
                      "flops_per_launch": flops / n_chunks, "ms_per_launch": bsa_ms / n_chunks,
                      "launches_per_step": n_chunks},
-        "kernels": {"bsa_ms_per_step": bsa_ms, "rest_ms_per_step": ms_step - bsa_ms},
+        "kernels": ({"chunk_step_ms_per_step": bsa_ms, "rest_ms_per_step": ms_step - bsa_ms}
+                    if one_kernel else
+                    {"bsa_ms_per_step": bsa_ms, "rest_ms_per_step": ms_step - bsa_ms}),
         "density": density,
         "e2e": {"value": tokens / (ms_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e, "steps": n_e2e,
                 "overlap": "chunk c+1's upload runs while chunk c computes; each chunk's "
                            "O/LSE read back while the next computes"},
-        "gpu_launches": args.steps * (4 * n_chunks - sum(1 for c in range(n_chunks)
-                                                         if c * chunk < cpu_tokens)
-                                      + n_chunks),
+        "gpu_launches": args.steps * (n_chunks if one_kernel else
+                                      4 * n_chunks - sum(1 for c in range(n_chunks)
+                                                         if c * chunk < cpu_tokens) + n_chunks),
         "clocks": clocks,
     }
     if rank == 0:
@@ -962,7 +985,7 @@ def config_dict(args, world):
            "cpu_block_tokens": 1024, "parallelism": f"replicas{world}",
            "l2": "flushed (256 MiB write) between timed steps", "seed": args.seed,
            "estimator_operands": args.estimator}
-    if "chunk" in cfg and args.step == "chunked":
+    if "chunk" in cfg and args.step in ("chunked", "chunk_kernel"):
         out.update({"seq_len": cfg["Lk"], "chunk": cfg["chunk"],
                     "chunks": cfg["Lk"] // cfg["chunk"]})
     else:
@@ -1022,7 +1045,8 @@ def main():
                          "(bsx_chunk_step); fused: bsx_chunk_prefill, estimate, selection "
                          "and attention over all key blocks in one kernel; offload: the pages' CPU-block-dense history; prefill: "
                          "fused on a whole-sequence workload; chunked: the chunk step on "
-                         "every chunk of a whole sequence in order (64K in 16 chunks)")
+                         "every chunk of a whole sequence in order (64K in 16 chunks; "
+                         "with chunk_kernel and a chunked workload, one kernel per chunk)")
     ap.add_argument("--estimator", default="bf16", choices=["bf16", "e4m3"],
                     help="operand type of the estimator's scores (e4m3: Q and the chunk's K "
                          "quantized each step, the history's K kept in e4m3)")
@@ -1059,7 +1083,9 @@ def main():
         run_sweep(args)
     elif args.sparse:
         run_sparse(args)
-    elif args.step == "chunked":
+    elif args.step == "chunked" or (args.step == "chunk_kernel" and
+                                    "chunk" in CONFIGS[args.workload]):
+        # a whole sequence chunk by chunk (chunk_kernel: one kernel per chunk)
         run_chunked(args)
     else:
         run_gpu(args)
