@@ -548,12 +548,13 @@ __device__ __forceinline__ void bsa_cta(const BsaArgs& a, const BsaTile& tile, u
     const long long lrow = ((long long)b * Hq + h) * q_len + qb * 128 + row;
     // (two ranges) this row's LSE over the first range, once it is finished
     float lse_first = -INFINITY;
-    // The blocks [rs, re) of the row that this group takes, j = grp (mod 2):
-    // with two ranges each group's sequence runs on across the boundary.  The
-    // loop is compiled once per range (a finish of the first range inside a
-    // single loop slowed it down), and so is the issuer's.
-    auto softmax_range = [&](const int rs, const int re) {
-      for (int j = rs + ((grp - rs) & 1); ok && j < re; j += 2) {
+    // This group's blocks j = j0, j0 + 2, ... below re (j0 = grp mod 2) of the
+    // range that starts at block rs: with two ranges each group's sequence
+    // runs on across the boundary.  The loop is compiled once per use (a
+    // finish of the first range inside a single loop slowed it down), and so
+    // is the issuer's.
+    auto softmax_blocks = [&](const int j0, const int re, const int rs) {
+      for (int j = j0; ok && j < re; j += 2) {
         const int jr = j - rs;  // the block's index within its range
         if (!mbar_wait_warp(s_full(grp), (j >> 1) & 1, abort_flag, err, kErrBsaTc, kSiteSFull)) {
           ok = false;
@@ -648,20 +649,25 @@ __device__ __forceinline__ void bsa_cta(const BsaArgs& a, const BsaTile& tile, u
       }
     };
     if (two) {
-      softmax_range(0, n0);
-      // the end of the first range (with the other group); the second range
-      // starts this group's running statistics afresh
+      softmax_blocks(grp, n0, 0);
+      // This group's first block of the second range (S of it is already
+      // computed) goes first, with fresh running statistics, so that its P
+      // is ready when the issuer resumes; then the end of the first range
+      // (with the other group), then the rest of the second range.
+      const float m_first = m_run, l_first = l_run;
+      m_run = -INFINITY;
+      l_run = 0.f;
+      const int y = n0 + ((grp - n0) & 1);
+      softmax_blocks(y, y + 1 < n ? y + 1 : n, n0);
       const FirstResult fr = finish_first_range<D>(
-          FirstRange{grp, row, lane_base, tmem_o0, n0, m_run, l_run, xm, o_done(grp), xbar,
+          FirstRange{grp, row, lane_base, tmem_o0, n0, m_first, l_first, xm, o_done(grp), xbar,
                      range_done, abort_flag, err, tile.o_scratch + orow},
           ok);
       lse_first = fr.lse;
       ok = fr.ok;
-      m_run = -INFINITY;
-      l_run = 0.f;
-      softmax_range(n0, n);
+      softmax_blocks(y + 2, n, n0);
     } else {
-      softmax_range(0, n);
+      softmax_blocks(grp, n, 0);
     }
     // ---- end of the (last) range: the two groups' results merged per row ----
     {
@@ -673,6 +679,19 @@ __device__ __forceinline__ void bsa_cta(const BsaArgs& a, const BsaTile& tile, u
       const bool h1 = nr >= 2 || (nr == 1 && (rs & 1) == 1);
       const bool mine = grp ? h1 : h0;
       const int j_last = !mine ? -1 : (((re - 1) & 1) == grp ? re - 1 : re - 2);
+      // (two ranges) the first range's O of this thread's columns, this
+      // thread's own stores to o_scratch, loaded before the waits below so
+      // that their latency is hidden
+      uint4 first_o[D / 64][4];
+      if (two) {
+#pragma unroll
+        for (int cc = 0; cc < D / 64; ++cc) {
+          const uint4* scr =
+              reinterpret_cast<const uint4*>(tile.o_scratch + orow + grp * (D / 2) + cc * 32);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) first_o[cc][q4] = scr[q4];
+        }
+      }
       float* xr = xm + (two ? 2 * 2 * 128 : 0);
       xr[(grp * 2 + 0) * 128 + row] = m_run;
       xr[(grp * 2 + 1) * 128 + row] = l_run;
@@ -702,11 +721,9 @@ __device__ __forceinline__ void bsa_cta(const BsaArgs& a, const BsaTile& tile, u
           uint4 pk4[4];
           range_out32<D>(tmem_o0 + lane_base + col, h0, h1, rw, pk4);
           if (two) {
-            // the first range's O, this thread's own store (o_scratch)
-            const uint4* scr = reinterpret_cast<const uint4*>(tile.o_scratch + orow + col);
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
-              const uint4 u = scr[q4];
+              const uint4 u = first_o[cc][q4];
               const uint32_t a4[4] = {u.x, u.y, u.z, u.w};
               const uint32_t c4[4] = {pk4[q4].x, pk4[q4].y, pk4[q4].z, pk4[q4].w};
               uint32_t w4[4];

@@ -232,7 +232,7 @@ __device__ __forceinline__ void select_row(const float* __restrict__ base,
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       const int kb = e * NT + stid;
-      if (kb < nkb) mrow[kb] = kb < ncausal ? 1 : 0;
+      if (kb < nkb) mrow[kb] = sel[kb] = kb < ncausal ? 1 : 0;
     }
     return;
   }
@@ -329,10 +329,12 @@ __device__ __forceinline__ void select_row(const float* __restrict__ base,
       sel[0xFFFFFFFFu - (unsigned)(key[e] & 0xFFFFFFFFull)] = 1;
   }
   sel_sync();
+  // the row's mask, also left in sel[] (each thread rewrites only the
+  // entries it reads) for the CPU-block flags
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     const int kb = e * NT + stid;
-    if (kb < nkb) mrow[kb] = (kb < ncausal && (kb == 0 || kb == diag || sel[kb])) ? 1 : 0;
+    if (kb < nkb) mrow[kb] = sel[kb] = (kb < ncausal && (kb == 0 || kb == diag || sel[kb])) ? 1 : 0;
   }
 }
 
@@ -385,10 +387,14 @@ __device__ __forceinline__ void select_rows(const FusedParams& P, uint8_t* sm, i
         // CPU block is kept when any of its key blocks is selected in any
         // row; every row sets the flags of its own blocks (the same value
         // from every writer; the flags are zeroed before the launch)
+        // (read from the copy of the row's mask that the selection left in
+        // shared memory: a re-read of the row from global memory made the
+        // workers finish 3-5 us later)
         const int b = bh / P.Hq;
+        const uint8_t* srow = sm + SelLayout<RB, E>::kSel;
         for (int c = stid; c < P.n_cpu; c += kSelThreads) {
           bool any = false;
-          for (int u = 0; u < P.cpu_kb; ++u) any = any || mrow[c * P.cpu_kb + u] != 0;
+          for (int u = 0; u < P.cpu_kb; ++u) any = any || srow[c * P.cpu_kb + u] != 0;
           if (any) P.keep[(long long)b * P.n_cpu + c] = 1;
         }
       }
