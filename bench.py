@@ -802,8 +802,9 @@ def run_sparse(args):
     selects about 6-50% of the causal blocks).  One JSON line per workload:
     the mask density, the step's tokens/s and its roofline fraction, the
     attention launch's TFLOP/s over the selected blocks and its fractions,
-    and the fused step (bsx_chunk_prefill, one kernel) on the same inputs with
-    its fraction (estimate and attention flops over its time).
+    and the fused step (bsx_chunk_prefill, one kernel) and the chunk step as
+    one kernel (bsx_chunk_step) on the same inputs with their fractions
+    (estimate and attention flops over their time).
     Device-resident inputs, L2 flushed between timed steps."""
     import torch
 
@@ -893,6 +894,28 @@ def run_sparse(args):
             ef[i][1].record(stream)
         torch.cuda.synchronize()
         t_fused = float(np.mean([e[0].elapsed_time(e[1]) for e in ef]))
+
+        # the chunk step as one kernel: bsx_chunk_step (estimate, selection
+        # with the CPU-block flags, attention on history and current chunk
+        # merged in each CTA)
+        keepk = torch.empty((B, P // 1024), dtype=torch.uint8, device=dev) if P >= 1024 else None
+
+        def chunk_kernel():
+            bsx.bsx_chunk_step(q, k, v, P, S, tau, mask=maskf, o=oh, lse=lh, o_curr=oc,
+                               lse_curr=lc, keep=keepk, workspace=wsf, stream=stream)
+        for _ in range(args.warmup):
+            chunk_kernel()
+        torch.cuda.synchronize()
+        fl_k = (bsa_flops(maskf.cpu().numpy(), P, 0, cur, d) +
+                bsa_flops(maskf.cpu().numpy(), P, cur, nkb, d) + est_fl)
+        ek = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.zero_()
+            ek[i][0].record(stream)
+            chunk_kernel()
+            ek[i][1].record(stream)
+        torch.cuda.synchronize()
+        t_kernel = float(np.mean([e[0].elapsed_time(e[1]) for e in ek]))
         ms = t_est + t_bsa + t_rest
         bsa_tf = fl / (t_bsa / 1e3) / 1e12
         roof_ms = (max(est_fl / (tc_peak * 1e12), est_bytes / (hbm_peak * 1e9))
@@ -913,6 +936,8 @@ def run_sparse(args):
                            "flops": fl_f, "frac": fl_f / (t_fused / 1e3) / 1e12 / tc_peak,
                            "frac_at_clock": (fl_f / (t_fused / 1e3) / 1e12 / at_clock
                                              if at_clock else None)},
+            "chunk_kernel": {"ms": t_kernel, "tokens_per_s_layer": B * Lq / (t_kernel / 1e3),
+                             "flops": fl_k, "frac": fl_k / (t_kernel / 1e3) / 1e12 / tc_peak},
             "steps": args.steps, "warmup": args.warmup,
             "peak_source": peak_src, "clocks": clocks}), flush=True)
         del q, k, v, ws, wsf, oh, oc
