@@ -30,6 +30,11 @@
 // Each group's chain S(j) -> softmax -> P V(j) -> S(j + 2) interleaves with
 // the other group's on the tensor pipe, and no per-block exchange between
 // warps is needed.  TMEM: S/P buffers in columns 0-255, O_0 and O_1 after.
+// Two ranges (the fused chunk step, a separate instantiation): the blocks of
+// the history and then of the current chunk run as one sequence; at the
+// boundary the groups finish the history range (its O to a scratch buffer,
+// its LSE in registers) and restart their statistics, and the final
+// epilogue merges the two results as bsx_merge_attn does.
 // Every wait is bounded (2 s of wall time); on expiry the CTA records the wait
 // in the device error word, drains its in-flight copies and MMAs, frees TMEM
 // and exits.
