@@ -272,9 +272,11 @@ int bsx_chunk_prefill(bsx_shape s, const void* q, const void* k, const void* v,
  * query tile attends to the history and to the current chunk as two ranges
  * and merges the two results itself, and whose selection writes the keep
  * flags.  Otherwise the steps run as the separate launches listed above.
- * Results: mask, the merged (o, lse) and keep, bit for bit as the separate
- * calls give them on the same mask; o_curr / lse_curr are scratch, with
- * unspecified contents afterwards.  With q_start_pos == 0 there is no
+ * Results: the merged (o, lse) and keep bit for bit as the separate calls
+ * give them on the kernel's mask; the mask as bsx_chunk_prefill's (the fused
+ * selection adds its row sums in another order than bsx_xattn_estimate,
+ * which can only change near-threshold rows); o_curr / lse_curr are
+ * scratch, with unspecified contents afterwards.  With q_start_pos == 0 there is no
  * history and (o, lse) are the current chunk's.
  *
  * Arguments are validated before anything is enqueued; every buffer 16-byte
